@@ -1,0 +1,487 @@
+"""RMSNorm-for-training benchmark on GB300: one step = forward + backward over one batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--T 65536] [--H 4096] [--nondet]
+
+Workload (default): plain rows T=65536, H=4096, BF16 x and dy ~ N(0,1), BF16 weight
+1 + 0.1*N(0,1), eps 1e-6 (the pages' plain-rows configuration at its largest T); the
+backward runs deterministic=True unless --nondet.  Inputs are 512 MiB per tensor, larger
+than the 129 MB L2, so no flush is needed between iterations.
+
+`value` is whole-job HBM throughput in GB/s: the algorithmic bytes of a step (forward
+4*R*H + 4*R + |w|, backward 6*R*H + 4*R + |w| + 4*H; R = T*nh rows) times the steps of
+all ranks, over the slowest rank's device time (CUDA events, inputs resident in HBM).
+`e2e` is the same metric through the public C ABI with pinned host buffers, the
+host->device input copies and the device->host result copies inside the timed region.
+`roofline` is for the backward (the dominant op: its dx row pass with fused dw partials
+plus the dw finish), timed by events around it on its launch stream.
+`cpu_baseline` times the FP64 oracle on a bounded row sample on this host's cores.
+
+With --gpus N under torchrun each rank runs an independent replica (the op has no
+exchange step); timings are max-reduced over ranks on the host (gloo).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm fwd/bwd µs and HBM GB/s per (T,H) vs GB300 peak; max dw err / budget"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "rmsnorm_fwd_02_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ---- byte model ----------------------------------------------------------------------
+
+def fwd_bytes(R: int, H: int, wbytes: int) -> int:
+    return 4 * R * H + 4 * R + wbytes * H
+
+
+def bwd_bytes(R: int, H: int, wbytes: int) -> int:
+    return 6 * R * H + 4 * R + wbytes * H + 4 * H
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_gb_s"):
+            if key in d:
+                return float(d[key]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_for(workload_key: str):
+    """DRAM bytes per backward launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(workload_key)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_op")
+
+
+# ---- distributed replicas --------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws: int):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
+    return dist
+
+
+def reduce_max(value: float, dist) -> float:
+    """Max of a host scalar over ranks (host-side gloo; not a data-path collective)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---- clocks during the timed region -----------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.lines = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1 + 0.25:
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[6:10]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(dev: int):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# ---- the CPU oracle baseline ------------------------------------------------------------
+
+def oracle_step(case, rows: np.ndarray):
+    """One forward + backward of the FP64 oracle over the rows `rows` of `case`."""
+    import oracle
+    H = case.H
+    sub_x = case.x.reshape(-1, H)[rows].reshape(-1)
+    sub_dy = case.dy.reshape(-1, H)[rows].reshape(-1)
+    n = rows.size
+    _, r64, _ = oracle.fwd(sub_x, case.w, case.eps, n, 1, H, H, H)
+    r_in = r64.astype(np.float32).astype(np.float64)
+    oracle.bwd_dx(sub_x, sub_dy, r_in, case.w, n, 1, H, H, H)
+    oracle.bwd_dw(sub_x, sub_dy, r_in, n, 1, H, H, H)
+
+
+def cpu_baseline(case, wbytes: int, budget_s: float = 10.0, rows_per_step: int = 64):
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(case.R, size=min(rows_per_step, case.R), replace=False))
+    n_steps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(case, rows)
+        n_steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    nbytes = (fwd_bytes(rows.size, case.H, wbytes) + bwd_bytes(rows.size, case.H, wbytes))
+    return {
+        "value": nbytes * n_steps / el / 1e9,
+        "unit": "GB/s",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": (f"{n_steps} x forward+backward of {rows.size} random rows of the "
+                   f"[{case.T},{case.H}] workload, {el:.1f} s single-threaded FP64"),
+    }
+
+
+# ---- the reference arm: the oracle, as it stands ---------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from rmsnorm_fwd_02_gb300 import synth
+    case = synth.make_case(0, args.T, args.H)
+    wbytes = 2
+    rows = np.arange(min(64, case.R), dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_step(case, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(case, rows)
+    el = time.perf_counter() - t0
+    nbytes = fwd_bytes(rows.size, case.H, wbytes) + bwd_bytes(rows.size, case.H, wbytes)
+    value = nbytes * args.steps / el / 1e9
+    sample = f"each step: forward+backward of {rows.size} rows of [{args.T},{args.H}]"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(args):
+    mode = "non-deterministic" if args.nondet else "deterministic"
+    return {
+        "workload": (f"plain rows T={args.T} H={args.H}: BF16 x, dy ~ N(0,1), BF16 w = "
+                     f"1+0.1*N(0,1), eps 1e-6; step = forward + backward ({mode})"),
+        "T": args.T, "H": args.H, "nh": 1, "w": "bf16", "storage": "bf16",
+        "deterministic": not args.nondet,
+        "l2": "inputs larger than L2 (no flush): 2*T*H bytes per tensor",
+    }
+
+
+# ---- our arm -------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    from rmsnorm_fwd_02_gb300 import _native as N
+    from rmsnorm_fwd_02_gb300 import synth
+
+    ws, rank, local = dist_env()
+    dist = dist_init(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    det = not args.nondet
+
+    case = synth.make_case(0, args.T, args.H)
+    R, H, T = case.R, case.H, case.T
+    wbytes = 2
+
+    def dbf(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, dy, w = dbf(case.x), dbf(case.dy), dbf(case.w)
+    y = torch.empty(R * H, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty_like(y)
+    rstd = torch.empty(R, dtype=torch.float32, device=dev)
+    dw = torch.empty(H, dtype=torch.float32, device=dev)
+    nws = N.rmsnorm_train_bwd_workspace_bytes(T, 1, H, det)
+    wsb = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    lib = N.lib()
+
+    def fwd_call(xp, wp, yp, rp):
+        st = lib.rmsnorm_train_fwd(xp, None, wp, 0, yp, None, rp, T, 1, H, H, H, 1e-6, sh)
+        if st:
+            raise N.RmsnError("rmsnorm_train_fwd", st)
+
+    def bwd_call(xp, dyp, wp, dxp, rp, dwp):
+        st = lib.rmsnorm_train_bwd(xp, dyp, None, rp, wp, 0, dxp, dwp, wsb.data_ptr(), nws,
+                                   T, 1, H, H, H, int(det), sh)
+        if st:
+            raise N.RmsnError("rmsnorm_train_bwd", st)
+
+    xp, dyp, wp = x.data_ptr(), dy.data_ptr(), w.data_ptr()
+    yp, dxp, rp, dwp = y.data_ptr(), dx.data_ptr(), rstd.data_ptr(), dw.data_ptr()
+
+    def step():
+        fwd_call(xp, wp, yp, rp)
+        bwd_call(xp, dyp, wp, dxp, rp, dwp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region 1: K whole steps back to back (the headline) ----
+    sampler = ClockSampler(gpu_uuid(local)) if rank == 0 else None
+    time.sleep(0.5 if sampler else 0.0)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_begin.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    total_ms = t_begin.elapsed_time(t_end)
+
+    # ---- device-timed region 2: the same steps with events around each op ----
+    k2 = min(args.steps, 500)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k2)]
+    torch.cuda.synchronize()
+    for i in range(k2):
+        ev[i][0].record(stream)
+        fwd_call(xp, wp, yp, rp)
+        ev[i][1].record(stream)
+        bwd_call(xp, dyp, wp, dxp, rp, dwp)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    max_ms = reduce_max(total_ms, dist)
+
+    step_bytes = fwd_bytes(R, H, wbytes) + bwd_bytes(R, H, wbytes)
+    value = step_bytes * args.steps * ws / (max_ms * 1e-3) / 1e9
+    fwd_us = statistics.mean(fwd_ms) * 1e3
+    bwd_us = statistics.mean(bwd_ms) * 1e3
+
+    # ---- end to end through the C ABI with pinned host buffers ----
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    hx = torch.from_numpy(case.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hdy = torch.from_numpy(case.dy.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hw = torch.from_numpy(case.w.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.empty(R * H, dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty(R * H, dtype=torch.bfloat16).pin_memory()
+    hr = torch.empty(R, dtype=torch.float32).pin_memory()
+    hdw = torch.empty(H, dtype=torch.float32).pin_memory()
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hr.copy_(rstd, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hdw.copy_(dw, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dist)
+    h2d = 2 * R * H * 2 + H * wbytes
+    d2h = 2 * R * H * 2 + 4 * R + 4 * H
+    e2e_value = step_bytes * e2e_steps * ws / (e2e_ms * 1e-3) / 1e9
+
+    # ---- dw error vs the oracle (outside every timed region) ----
+    dw_ratio = None
+    if rank == 0 and not args.skip_dw_check:
+        import oracle
+        _, r64, _ = oracle.fwd(case.x, case.w, case.eps, T, 1, H, H, H, want_y=False)
+        r32 = r64.astype(np.float32)
+        rin = torch.from_numpy(r32).to(dev)
+        x.copy_(hx)
+        dy.copy_(hdy)
+        w.copy_(hw)
+        st = lib.rmsnorm_train_bwd(x.data_ptr(), dy.data_ptr(), None, rin.data_ptr(),
+                                   w.data_ptr(), 0, dx.data_ptr(), dw.data_ptr(),
+                                   wsb.data_ptr(), nws, T, 1, H, H, H, int(det), sh)
+        assert st == 0
+        dw64 = oracle.bwd_dw(case.x, case.dy, r32.astype(np.float64), T, 1, H, H, H)
+        err = np.abs(dw.cpu().numpy().astype(np.float64) - dw64)
+        dw_ratio = float((err / (1e-4 + 1e-4 * np.abs(dw64))).max())
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peak()
+    bwd_achieved = bwd_bytes(R, H, wbytes) / (bwd_us * 1e-6) / 1e9
+    fwd_achieved = fwd_bytes(R, H, wbytes) / (fwd_us * 1e-6) / 1e9
+    wkey = f"bwd_plain_T{T}_H{H}_{'det' if det else 'nondet'}"
+    cpu = cpu_baseline(case, wbytes, budget_s=args.cpu_seconds) if ws == 1 else None
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(args),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "backward op (dx row pass with fused dw partials + dw finish)",
+            "achieved": bwd_achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "unit": "GB/s",
+            "frac": bwd_achieved / peak,
+            "traffic": traffic_for(wkey),
+        },
+        "fwd": {"us": fwd_us, "GBps": fwd_achieved, "frac": fwd_achieved / peak},
+        "bwd": {"us": bwd_us, "GBps": bwd_achieved, "frac": bwd_achieved / peak},
+        "dw_err_over_budget": dw_ratio,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,  # fwd + bwd row pass + dw finish per step
+        "clocks": clocks,
+        "source_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--T", type=int, default=65536)
+    ap.add_argument("--H", type=int, default=4096)
+    ap.add_argument("--nondet", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-dw-check", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,128 @@
+/*
+ * rmsnorm_train.h -- C ABI of the GB300 (sm_103a) RMSNorm-for-training library.
+ *
+ * The operation (flashinfer PR #8827 "fix(cake_rmsnorm): sm_100a and sm_107a dw-accuracy
+ * backward routes", description, and its Measurement section's workload line):
+ *
+ *   forward   rstd = 1 / sqrt(mean_j(x_j^2) + eps)        FP32, one per normalized row
+ *             y_j  = BF16(x_j * rstd * w_j)                BF16, round to nearest even
+ *             residual form: x := h = BF16(x_in + residual), and h is written too
+ *   backward  xhat = x * rstd,  g = dy * w,  c = mean_j(g_j * xhat_j)
+ *             dx_j = BF16(rstd * (g_j - xhat_j * c) [+ dh_j])
+ *             dw_j = sum over all normalized rows of dy_j * xhat_j   (FP32)
+ *
+ * Two backward modes share one forward: deterministic != 0 gives bit-identical dw run to
+ * run and across GPUs of any SM count (the row -> partial mapping depends on T, nh and H
+ * only); deterministic == 0 may size its partition to the current GPU.  dx is the same in
+ * both modes, bit for bit.
+ *
+ * Rows and views (same PR, description: per-head views [T,24,256] strided and [T,4,256]
+ * contiguous with a shared w[256]).  A normalized row is a pair (token t, head h),
+ * r = t*nh + h, with H elements; plain rows are nh = 1.  The forward's input activation
+ * (x / x_in / residual) and the backward's saved input are read through element strides:
+ * row r starts at element t*s_tok + h*s_head.  Every other tensor is contiguous:
+ * y, h_out, dy, dh, dx are [T, nh, H]; rstd is [T, nh]; w and dw are [H].
+ *
+ * Conventions common to every entry point:
+ *  - Pointers are DEVICE pointers on the current CUDA device, except where a comment says
+ *    otherwise.  BF16 = IEEE bfloat16 bit patterns (uint16 storage).
+ *  - Ownership: the caller owns every buffer, the workspace included.  The library never
+ *    allocates, frees or synchronizes; all work is enqueued on `stream` (a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream) and is asynchronous.
+ *  - Alignment: every tensor pointer 16-byte aligned; H a multiple of 8; s_tok and
+ *    s_head multiples of 8 elements (each row is a 16-byte-aligned run).
+ *  - Limits: 8 <= H <= 16384, T >= 0, nh >= 1, T*nh < 2^31.
+ *  - Outputs must not overlap inputs.
+ *  - Errors: argument checks happen before anything is enqueued and return a nonzero
+ *    status without touching memory; RMSN_ERR_CUDA reports a failed launch (the CUDA
+ *    error is left for cudaGetLastError()).  rmsnorm_train_status_str names a status.
+ */
+#ifndef RMSNORM_TRAIN_H
+#define RMSNORM_TRAIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RMSN_OK 0
+#define RMSN_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, stride or dtype */
+#define RMSN_ERR_UNSUPPORTED 2 /* H outside [8, 16384] or T*nh too large */
+#define RMSN_ERR_WORKSPACE 3   /* workspace missing or smaller than required */
+#define RMSN_ERR_CUDA 4        /* a CUDA runtime call or launch failed */
+#define RMSN_ERR_DEVICE 5      /* current device is not compute capability 10.3 */
+
+#define RMSN_W_BF16 0 /* w is BF16 [H] */
+#define RMSN_W_FP32 1 /* w is FP32 [H] */
+
+/*
+ * Forward: y (BF16) and rstd (FP32); with `residual` != NULL also h_out = BF16(x + residual)
+ * and the norm is taken of h_out.  (PR #8827 description: the forward's outputs, and the
+ * fused residual add at H6144; the workload line: eps 1e-6, y / h_new BF16, rstd FP32.)
+ *
+ *   x         BF16, read through (s_tok, s_head): the activation (x_in in residual form)
+ *   residual  BF16 or NULL, same strides as x
+ *   w         [H], dtype w_dtype (RMSN_W_BF16 or RMSN_W_FP32)
+ *   y         BF16 [T, nh, H] out
+ *   h_out     BF16 [T, nh, H] out; required iff residual != NULL, else must be NULL
+ *   rstd      FP32 [T, nh] out
+ *   eps       added to mean(x^2) inside the square root; finite, >= 0
+ * T*nh == 0 returns RMSN_OK with nothing enqueued.
+ */
+int rmsnorm_train_fwd(const void* x, const void* residual, const void* w, int w_dtype,
+                      void* y, void* h_out, float* rstd,
+                      int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head,
+                      float eps, void* stream);
+
+/*
+ * Bytes of device workspace rmsnorm_train_bwd needs for this shape and mode (0 is never
+ * returned for T*nh > 0).  For deterministic == 0 the size depends on the current device
+ * (its SM count); for deterministic != 0 it depends on (T, nh, H) only.  Returns 0 on
+ * invalid sizes.  Host-only computation apart from a device-attribute query.
+ */
+size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int deterministic);
+
+/*
+ * Backward: dx (BF16) and dw (FP32).  (PR #8827 description: the backward's outputs and
+ * the two modes; PR #8849 and the route notes of PR #8827: dw must stay within per-element
+ * atol 1e-4 + rtol 1e-4 of an FP64 sum, which this library meets with compensated FP32
+ * per-partition sums and a fixed-order compensated finish.)
+ *
+ *   x          BF16, the forward's normalized input (x, or h_out of the residual form),
+ *              read through (s_tok, s_head)
+ *   dy         BF16 [T, nh, H], upstream gradient of y
+ *   dh         BF16 [T, nh, H] or NULL: upstream gradient of h_out in the residual form,
+ *              added to dx (the combined gradient of x_in and residual)
+ *   rstd       FP32 [T, nh] as returned by the forward
+ *   w          [H], dtype w_dtype
+ *   dx         BF16 [T, nh, H] out
+ *   dw         FP32 [H] out, overwritten (not accumulated); zero-filled when T*nh == 0
+ *   workspace  device scratch of >= rmsnorm_train_bwd_workspace_bytes(...) bytes,
+ *              16-byte aligned, no initial contents required; clobbered by the call
+ *   deterministic  0 or 1 (see the top of this file)
+ */
+int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float* rstd,
+                      const void* w, int w_dtype, void* dx, float* dw,
+                      void* workspace, size_t workspace_bytes,
+                      int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head,
+                      int deterministic, void* stream);
+
+/* Static string naming a status code (never NULL). */
+const char* rmsnorm_train_status_str(int status);
+
+/*
+ * Reads (and, if reset != 0, clears) the library's device-side error word on the current
+ * device into *flags (host pointer).  Nonzero means a kernel gave up on a bounded wait
+ * (bit 0: a consumer waited too long for staged data; bit 1: the staging producer waited
+ * too long for a free buffer); that call's outputs are then unspecified.  This entry point
+ * SYNCHRONIZES the device; it is meant for tests and diagnostics, not the hot path.
+ */
+int rmsnorm_train_device_error(unsigned int* flags, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_TRAIN_H */

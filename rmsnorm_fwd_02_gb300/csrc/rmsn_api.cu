@@ -1,0 +1,331 @@
+// rmsn_api.cu -- the C ABI (include/rmsnorm_train.h): argument checks, launch planning,
+// and kernel launches.  Never allocates, frees or synchronizes (except the diagnostic
+// rmsnorm_train_device_error); every launch goes on the caller's stream.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/rmsnorm_train.h"
+#include "rmsn_launch.h"
+
+namespace rmsn {
+
+// Device error word (bounded waits that gave up), one per device that loads the library.
+__device__ unsigned g_err_word = 0u;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kRingTarget = 96 * 1024;  // shared-memory ring bytes per CTA (target)
+constexpr int kMaxStages = 8;
+// Deterministic backward: at most this many dw partials (CTAs), a fixed function of the
+// shape only.  2 x 152 is one wave of two CTAs per SM on a 152-SM GB300.
+constexpr int kDetMaxPartials = 304;
+constexpr int kMinStagesPerCta = 4;  // smallest chunk a backward CTA takes, in stages
+
+std::mutex g_mu;
+std::unordered_map<uint64_t, int> g_occ;       // (device, fn, threads, smem) -> blocks/SM
+std::unordered_map<uint64_t, bool> g_prepared; // (device, fn) -> smem attribute set
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+uint64_t key(int dev, const void* fn, uint64_t extra) {
+  uint64_t h = reinterpret_cast<uint64_t>(fn);
+  h ^= (static_cast<uint64_t>(dev) + 0x9e3779b97f4a7c15ull) + (h << 6) + (h >> 2);
+  h ^= extra + 0x9e3779b97f4a7c15ull + (h << 6) + (h >> 2);
+  return h;
+}
+
+size_t shared_bytes(const Shape& s, int H) {
+  const size_t ring = static_cast<size_t>(s.stages) * s.tensors * s.groups * H * 2;
+  return ring + 16 * static_cast<size_t>(s.stages) + 256 * static_cast<size_t>(s.groups) + 16;
+}
+
+Shape make_shape(int H, int tensors) {
+  Shape s{};
+  const int nv = H / 8;
+  s.vpt = nv <= 32 ? 1 : 2;
+  const int per = (nv + s.vpt - 1) / s.vpt;
+  s.ntg = ((per + 31) / 32) * 32;
+  s.groups = s.ntg >= 256 ? 1 : 256 / s.ntg;
+  if (s.groups > 8) s.groups = 8;
+  s.tensors = tensors;
+  const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
+  int st = static_cast<int>(kRingTarget / stage_bytes);
+  s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
+  s.threads = s.groups * s.ntg + kProducerThreads;
+  s.smem = shared_bytes(s, H);
+  return s;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return RMSN_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return RMSN_ERR_DEVICE;
+  return RMSN_OK;
+}
+
+// Checks the device generation and caches its SM count and error-word address.
+int device_setup(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev]) return RMSN_OK;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return RMSN_ERR_CUDA;
+  if (major != 10 || minor != 3) return RMSN_ERR_DEVICE;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess || p == nullptr) return RMSN_ERR_CUDA;
+  g_sms[dev] = sms;
+  g_err_ptr[dev] = static_cast<unsigned*>(p);
+  return RMSN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by both directions; view strides apply to the strided input only.
+int check_view(int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head, int w_dtype) {
+  if (T < 0 || nh < 1) return RMSN_ERR_INVALID_ARG;
+  if (w_dtype != RMSN_W_BF16 && w_dtype != RMSN_W_FP32) return RMSN_ERR_INVALID_ARG;
+  if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
+  if (H > kMaxH) return RMSN_ERR_UNSUPPORTED;
+  if (T > 0 && T * static_cast<int64_t>(nh) > INT32_MAX - 1) return RMSN_ERR_UNSUPPORTED;
+  if (s_tok < 0 || (s_tok % 8) != 0) return RMSN_ERR_INVALID_ARG;
+  if (nh > 1 && (s_head < 0 || (s_head % 8) != 0)) return RMSN_ERR_INVALID_ARG;
+  return RMSN_OK;
+}
+
+bool is_contig(int32_t nh, int32_t H, int64_t s_tok, int64_t s_head) {
+  return s_tok == static_cast<int64_t>(nh) * H && (nh == 1 || s_head == H);
+}
+
+int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
+  const int64_t per = static_cast<int64_t>(s.groups) * kMinStagesPerCta;
+  int64_t want = (R + per - 1) / per;
+  if (want < 1) want = 1;
+  int64_t cap;
+  if (det) {
+    cap = kDetMaxPartials;
+  } else {
+    int occ = bwd_blocks_per_sm(s, fp32w);
+    cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
+  }
+  return static_cast<int>(want < cap ? want : cap);
+}
+
+}  // namespace
+
+// ---- helpers used by the kernel translation units ------------------------------------
+
+Shape fwd_shape(int H, bool residual) { return make_shape(H, residual ? 2 : 1); }
+Shape bwd_shape(int H, bool with_dh) { return make_shape(H, with_dh ? 3 : 2); }
+
+cudaError_t prepare_kernel(const void* fn, size_t smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t k = key(dev, fn, 0);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_prepared.count(k)) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(227 * 1024));
+  if (e != cudaSuccess) return e;
+  (void)smem;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prepared[k] = true;
+  return cudaSuccess;
+}
+
+int blocks_per_sm(const void* fn, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  const uint64_t k = key(dev, fn, (static_cast<uint64_t>(threads) << 32) ^ smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occ.find(k);
+    if (it != g_occ.end()) return it->second;
+  }
+  if (prepare_kernel(fn, smem) != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1)
+    n = 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occ[k] = n;
+  return n;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       void** args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+extern "C" {
+
+const char* rmsnorm_train_status_str(int status) {
+  switch (status) {
+    case RMSN_OK: return "ok";
+    case RMSN_ERR_INVALID_ARG: return "invalid argument";
+    case RMSN_ERR_UNSUPPORTED: return "unsupported size";
+    case RMSN_ERR_WORKSPACE: return "workspace missing or too small";
+    case RMSN_ERR_CUDA: return "CUDA runtime error";
+    case RMSN_ERR_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    default: return "unknown status";
+  }
+}
+
+int rmsnorm_train_fwd(const void* x, const void* residual, const void* w, int w_dtype,
+                      void* y, void* h_out, float* rstd, int64_t T, int32_t nh, int32_t H,
+                      int64_t s_tok, int64_t s_head, float eps, void* stream) {
+  int st = check_view(T, nh, H, s_tok, s_head, w_dtype);
+  if (st != RMSN_OK) return st;
+  if (!x || !w || !y || !rstd) return RMSN_ERR_INVALID_ARG;
+  if ((residual == nullptr) != (h_out == nullptr)) return RMSN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(residual) ||
+      !aligned16(h_out) || (reinterpret_cast<uintptr_t>(rstd) & 3u))
+    return RMSN_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return RMSN_ERR_INVALID_ARG;
+  const int64_t R = T * static_cast<int64_t>(nh);
+  if (R == 0) return RMSN_OK;
+
+  int dev = 0;
+  if ((st = current_device(&dev)) != RMSN_OK) return st;
+  if ((st = device_setup(dev)) != RMSN_OK) return st;
+
+  const bool fp32w = (w_dtype == RMSN_W_FP32);
+  const Shape s = fwd_shape(H, residual != nullptr);
+  const int occ = fwd_blocks_per_sm(s, fp32w);
+  int64_t P = (R + s.groups - 1) / s.groups;
+  const int64_t cap = static_cast<int64_t>(g_sms[dev]) * occ;
+  if (P > cap) P = cap;
+
+  FwdArgs a{};
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.res = static_cast<const __nv_bfloat16*>(residual);
+  a.w = w;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.h = static_cast<__nv_bfloat16*>(h_out);
+  a.rstd = rstd;
+  a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
+  a.R = static_cast<int32_t>(R);
+  a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
+  a.eps = eps;
+  a.groups = s.groups;
+  a.ntg = s.ntg;
+  a.stages = s.stages;
+  a.P = static_cast<int32_t>(P);
+  a.err = g_err_ptr[dev];
+  return launch_fwd(a, s, fp32w, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RMSN_OK
+             : RMSN_ERR_CUDA;
+}
+
+size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int deterministic) {
+  if (check_view(T, nh, H, static_cast<int64_t>(nh) * (H > 0 ? H : 0), H, RMSN_W_BF16) !=
+      RMSN_OK)
+    return 0;
+  const int64_t R = T * static_cast<int64_t>(nh);
+  if (R == 0) return 0;
+  const Shape s = bwd_shape(H, false);  // partial count does not depend on dh
+  int dev = 0;
+  if (!deterministic) {
+    if (current_device(&dev) != RMSN_OK || device_setup(dev) != RMSN_OK) return 0;
+  }
+  // the partition count of the non-deterministic mode is the larger of the two weight
+  // dtypes' occupancies, so one size serves both
+  int P = bwd_partials(static_cast<int32_t>(R), s, deterministic != 0, dev, false);
+  if (!deterministic) {
+    int P2 = bwd_partials(static_cast<int32_t>(R), s, false, dev, true);
+    if (P2 > P) P = P2;
+    const Shape sd = bwd_shape(H, true);
+    P2 = bwd_partials(static_cast<int32_t>(R), sd, false, dev, false);
+    if (P2 > P) P = P2;
+    P2 = bwd_partials(static_cast<int32_t>(R), sd, false, dev, true);
+    if (P2 > P) P = P2;
+  }
+  return static_cast<size_t>(P) * 2 * H * sizeof(float);
+}
+
+int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float* rstd,
+                      const void* w, int w_dtype, void* dx, float* dw, void* workspace,
+                      size_t workspace_bytes, int64_t T, int32_t nh, int32_t H, int64_t s_tok,
+                      int64_t s_head, int deterministic, void* stream) {
+  int st = check_view(T, nh, H, s_tok, s_head, w_dtype);
+  if (st != RMSN_OK) return st;
+  if (!x || !dy || !rstd || !w || !dx || !dw) return RMSN_ERR_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return RMSN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dh) || !aligned16(w) || !aligned16(dx) ||
+      !aligned16(dw) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(rstd) & 3u))
+    return RMSN_ERR_INVALID_ARG;
+  const int64_t R = T * static_cast<int64_t>(nh);
+
+  int dev = 0;
+  if ((st = current_device(&dev)) != RMSN_OK) return st;
+  if ((st = device_setup(dev)) != RMSN_OK) return st;
+  const cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+
+  const bool fp32w = (w_dtype == RMSN_W_FP32);
+  const Shape s = bwd_shape(H, dh != nullptr);
+  int P = 0;
+  if (R > 0) {
+    P = bwd_partials(static_cast<int32_t>(R), s, deterministic != 0, dev, fp32w);
+    const size_t need = static_cast<size_t>(P) * 2 * H * sizeof(float);
+    if (workspace == nullptr || workspace_bytes < need) return RMSN_ERR_WORKSPACE;
+
+    BwdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dy = static_cast<const __nv_bfloat16*>(dy);
+    a.dh = static_cast<const __nv_bfloat16*>(dh);
+    a.rstd = rstd;
+    a.w = w;
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.part = static_cast<float*>(workspace);
+    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
+    a.R = static_cast<int32_t>(R);
+    a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
+    a.groups = s.groups;
+    a.ntg = s.ntg;
+    a.stages = s.stages;
+    a.P = P;
+    a.err = g_err_ptr[dev];
+    if (launch_bwd_rows(a, s, fp32w, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
+  }
+  if (launch_dw_finish(static_cast<const float*>(workspace), dw, P, H, stream_) != cudaSuccess)
+    return RMSN_ERR_CUDA;
+  return RMSN_OK;
+}
+
+int rmsnorm_train_device_error(unsigned int* flags, int reset) {
+  if (!flags) return RMSN_ERR_INVALID_ARG;
+  int dev = 0, st;
+  if ((st = current_device(&dev)) != RMSN_OK) return st;
+  if ((st = device_setup(dev)) != RMSN_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return RMSN_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(flags, g_err_word, sizeof(unsigned)) != cudaSuccess)
+    return RMSN_ERR_CUDA;
+  if (reset) {
+    const unsigned zero = 0u;
+    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(unsigned)) != cudaSuccess)
+      return RMSN_ERR_CUDA;
+  }
+  return RMSN_OK;
+}
+
+}  // extern "C"

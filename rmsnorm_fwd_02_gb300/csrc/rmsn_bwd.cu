@@ -1,0 +1,324 @@
+// rmsn_bwd.cu -- RMSNorm training backward for sm_103a: dx row pass fused with the dw
+// partial sums, and the fixed-order dw finish.
+//
+// Per normalized row, with r the forward's rstd (flashinfer PR #8827, description: the
+// backward's BF16 dx and FP32 dw; the residual form's combined gradient):
+//   xhat_j = x_j * r,  g_j = dy_j * w_j,  c = (sum_j g_j * xhat_j) / H
+//   dx_j   = BF16((g_j - xhat_j * c) * r  [+ dh_j])
+//   dw_j  += dy_j * xhat_j          over every row of every CTA's chunk
+//
+// dw accuracy (PR #8849 and PR #8827's route notes: every dw element within
+// atol 1e-4 + rtol 1e-4 of an FP64 sum, a budget plain FP32 running sums break at large
+// T): each consumer thread keeps, for each of its columns, a running FP32 sum and a
+// running compensation term (Fast2Sum error of each addition).  A CTA writes its chunk's
+// partial as an unevaluated (hi, lo) FP32 pair per column; the finish kernel adds the P
+// pairs in a fixed order with Knuth's TwoSum.  The row -> CTA chunk mapping is fixed by
+// (R, P) and the finish order by P, so dw is bit-reproducible whenever P is; dx does not
+// depend on P at all.
+#include "rmsn_common.cuh"
+#include "rmsn_launch.h"
+
+namespace rmsn {
+
+// Knuth's TwoSum: s + err == a + b exactly, no ordering assumption.
+__device__ __forceinline__ float two_sum(float a, float b, float& err) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float ap = __fsub_rn(s, bp);
+  err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+  return s;
+}
+
+template <int VPT, bool kFp32W, bool kDh>
+__global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
+  const int H = a.map.H;
+  const int NV = H >> 3;
+  const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const size_t stage_elems = static_cast<size_t>(NT) * G * H;
+
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_elems * 2);
+  uint64_t* empty = full + S;
+  float* red = reinterpret_cast<float*>(empty + S);  // [2][G][32]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * G * 32);
+
+  const int tid = threadIdx.x;
+  const int ncons = G * NTg;
+  const int32_t k = blockIdx.x;
+  const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
+  const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
+  const int32_t nstage = (r1 - r0 + G - 1) / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], static_cast<uint32_t>(G));
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+
+  if (tid >= ncons) {  // ---- producer warp ----
+    if (tid == ncons) {
+      const uint64_t pol = l2_evict_first_policy();
+      const RowMap m{a.map.nh, H, a.map.s_tok, a.map.s_head};
+      for (int32_t j = 0; j < nstage; ++j) {
+        const int s = j % S;
+        if (j >= S &&
+            !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                               a.err, kErrProducerWait))
+          break;
+        const int32_t ra = r0 + j * G;
+        const int32_t rb = min(ra + G, r1);
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u * NT);
+        __nv_bfloat16* dst = ring + s * stage_elems;
+        if (a.contig)
+          copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
+        else
+          copy_rows(dst, a.x, m, ra, rb, &full[s], pol);
+        copy_rows_contig(dst + G * H, a.dy, H, ra, rb, &full[s], pol);
+        if constexpr (kDh) copy_rows_contig(dst + 2 * G * H, a.dh, H, ra, rb, &full[s], pol);
+      }
+    }
+    return;
+  }
+
+  // ---- consumers ----
+  const int g = tid / NTg;
+  const int lt = tid - g * NTg;
+  float wv[VPT][8];
+  float acc[VPT][8], cmp[VPT][8];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if (c < NV) load_w8<kFp32W>(a.w, c, wv[v]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      acc[v][e] = 0.f;
+      cmp[v][e] = 0.f;
+    }
+  }
+  const float hf = static_cast<float>(H);
+
+  float rs_next = (r0 + g < r1) ? __ldg(a.rstd + r0 + g) : 0.f;
+  for (int32_t j = 0; j < nstage; ++j) {
+    const int32_t row = r0 + j * G + g;
+    if (row >= r1) break;
+    const float rs = rs_next;
+    if (row + G < r1) rs_next = __ldg(a.rstd + row + G);  // one row ahead
+    const int s = j % S;
+    mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                      kErrConsumerWait);
+    const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+    const size_t out_row = static_cast<size_t>(row) * H;
+
+    uint4 xv[VPT], dv[VPT], hv[VPT];
+    float dot = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        xv[v] = lds128(st + c * 8);
+        dv[v] = lds128(st + static_cast<size_t>(G) * H + c * 8);
+        if constexpr (kDh) hv[v] = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+        float xf[8], df[8];
+        unpack8(xv[v], xf);
+        unpack8(dv[v], df);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          dot = fmaf(__fmul_rn(df[e], wv[v][e]), __fmul_rn(xf[e], rs), dot);
+      }
+    }
+    dot = warp_allsum(dot);
+    float* slot = red + ((j & 1) * G + g) * 32;
+    if (NTg > 32 && (lt & 31) == 0) slot[lt >> 5] = dot;
+
+    // dw: compensated running sums (independent of the row reduction, so they run while
+    // the other warps of the group reach the barrier)
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        float xf[8], df[8];
+        unpack8(xv[v], xf);
+        unpack8(dv[v], df);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float p = __fmul_rn(df[e], __fmul_rn(xf[e], rs));
+          const float t = __fadd_rn(acc[v][e], p);
+          cmp[v][e] = __fadd_rn(cmp[v][e], __fadd_rn(__fsub_rn(acc[v][e], t), p));
+          acc[v][e] = t;
+        }
+      }
+    }
+
+    if (NTg > 32) {
+      named_bar_sync(1 + g, NTg);
+      dot = 0.f;
+      for (int i = 0; i < (NTg >> 5); ++i) dot += slot[i];  // fixed order
+    } else {
+      __syncwarp();
+    }
+    if (lt == 0) mbar_arrive(&empty[s]);  // the group is done reading this stage
+
+    const float cc = __fdiv_rn(dot, hf);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        float xf[8], df[8], hd[8];
+        unpack8(xv[v], xf);
+        unpack8(dv[v], df);
+        if constexpr (kDh) unpack8(hv[v], hd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = __fmul_rn(xf[e], rs);
+          const float gg = __fmul_rn(df[e], wv[v][e]);
+          float d = __fmul_rn(fmaf(-xh, cc, gg), rs);
+          if constexpr (kDh) d = __fadd_rn(d, hd[e]);
+          xf[e] = d;
+        }
+        stg128(a.dx + out_row + c * 8, pack8(xf));
+      }
+    }
+  }
+
+  // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----
+  float* part = a.part + static_cast<size_t>(k) * 2 * H;
+  if (G == 1) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        float hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          hi[e] = __fadd_rn(acc[v][e], cmp[v][e]);
+          lo[e] = __fsub_rn(cmp[v][e], __fsub_rn(hi[e], acc[v][e]));
+        }
+        float4* ph = reinterpret_cast<float4*>(part + c * 8);
+        float4* pl = reinterpret_cast<float4*>(part + H + c * 8);
+        ph[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        ph[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
+        pl[0] = make_float4(lo[0], lo[1], lo[2], lo[3]);
+        pl[1] = make_float4(lo[4], lo[5], lo[6], lo[7]);
+      }
+    }
+    return;
+  }
+  // several row groups: combine them through shared memory in group order.  The ring is
+  // free once every consumer is past its loop (each stage was fully waited on by the
+  // group that owns its first row).
+  named_bar_sync(15, ncons);
+  float* cb = reinterpret_cast<float*>(smem);  // [G][2][H]
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if (c < NV) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float hi = __fadd_rn(acc[v][e], cmp[v][e]);
+        const float lo = __fsub_rn(cmp[v][e], __fsub_rn(hi, acc[v][e]));
+        cb[(2 * g) * H + c * 8 + e] = hi;
+        cb[(2 * g + 1) * H + c * 8 + e] = lo;
+      }
+    }
+  }
+  named_bar_sync(15, ncons);
+  for (int col = tid; col < H; col += ncons) {
+    float s = 0.f, e = 0.f;
+    for (int gg = 0; gg < G; ++gg) {
+      float err;
+      s = two_sum(s, cb[(2 * gg) * H + col], err);
+      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gg + 1) * H + col]));
+    }
+    const float hi = __fadd_rn(s, e);
+    part[col] = hi;
+    part[H + col] = __fsub_rn(e, __fsub_rn(hi, s));
+  }
+}
+
+// dw[col] = sum over k = 0..P-1 of (hi_k + lo_k), in a fixed order: slice i of the
+// kFinishSlices slices takes k in [i*P/slices, (i+1)*P/slices) in increasing k, then the
+// slice sums are added in slice order.  TwoSum carries the error terms throughout.
+__global__ void __launch_bounds__(kFinishCols* kFinishSlices)
+    rmsn_dw_finish_kernel(const float* __restrict__ part, float* __restrict__ dw, int P, int H) {
+  __shared__ float sh[kFinishSlices][kFinishCols];
+  __shared__ float se[kFinishSlices][kFinishCols];
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+  const int cl = threadIdx.x % kFinishCols;
+  const int sl = threadIdx.x / kFinishCols;
+  const int col = blockIdx.x * kFinishCols + cl;
+  float s = 0.f, e = 0.f;
+  if (col < H) {
+    const int ka = (sl * P) / kFinishSlices;
+    const int kb = ((sl + 1) * P) / kFinishSlices;
+    for (int kk = ka; kk < kb; ++kk) {
+      const float hi = part[static_cast<size_t>(kk) * 2 * H + col];
+      const float lo = part[static_cast<size_t>(kk) * 2 * H + H + col];
+      float err;
+      s = two_sum(s, hi, err);
+      e = __fadd_rn(e, __fadd_rn(err, lo));
+    }
+  }
+  sh[sl][cl] = s;
+  se[sl][cl] = e;
+  __syncthreads();
+  if (sl == 0 && col < H) {
+    float S = sh[0][cl], E = se[0][cl];
+    for (int i = 1; i < kFinishSlices; ++i) {
+      float err;
+      S = two_sum(S, sh[i][cl], err);
+      E = __fadd_rn(E, __fadd_rn(err, se[i][cl]));
+    }
+    dw[col] = __fadd_rn(S, E);
+  }
+}
+
+template <int VPT, bool kFp32W, bool kDh>
+static const void* bwd_kernel_ptr() {
+  return reinterpret_cast<const void*>(&rmsn_bwd_rows_kernel<VPT, kFp32W, kDh>);
+}
+
+static const void* pick_bwd(int vpt, bool fp32w, bool dh) {
+  if (vpt == 1) {
+    if (fp32w) return dh ? bwd_kernel_ptr<1, true, true>() : bwd_kernel_ptr<1, true, false>();
+    return dh ? bwd_kernel_ptr<1, false, true>() : bwd_kernel_ptr<1, false, false>();
+  }
+  if (fp32w) return dh ? bwd_kernel_ptr<2, true, true>() : bwd_kernel_ptr<2, true, false>();
+  return dh ? bwd_kernel_ptr<2, false, true>() : bwd_kernel_ptr<2, false, false>();
+}
+
+cudaError_t prepare_kernel(const void* fn, size_t smem);
+int blocks_per_sm(const void* fn, int threads, size_t smem);
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       void** args);
+
+int bwd_blocks_per_sm(const Shape& s, bool fp32w) {
+  return blocks_per_sm(pick_bwd(s.vpt, fp32w, s.tensors == 3), s.threads, s.smem);
+}
+
+cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st) {
+  const void* fn = pick_bwd(s.vpt, fp32w, a.dh != nullptr);
+  cudaError_t e = prepare_kernel(fn, s.smem);
+  if (e != cudaSuccess) return e;
+  BwdArgs copy = a;
+  void* args[] = {&copy};
+  return launch_pdl(fn, dim3(static_cast<unsigned>(a.P)), dim3(static_cast<unsigned>(s.threads)),
+                    s.smem, st, args);
+}
+
+cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st) {
+  const void* fn = reinterpret_cast<const void*>(&rmsn_dw_finish_kernel);
+  void* args[] = {&part, &dw, &P, &H};
+  const unsigned grid = static_cast<unsigned>((H + kFinishCols - 1) / kFinishCols);
+  return launch_pdl(fn, dim3(grid), dim3(kFinishCols * kFinishSlices), 0, st, args);
+}
+
+}  // namespace rmsn

@@ -1,0 +1,213 @@
+// rmsn_common.cuh -- device helpers shared by the forward and backward kernels.
+//
+// Staging model (both kernels): a CTA owns a contiguous chunk of normalized rows.  One
+// producer thread streams the chunk's rows from HBM into an S-stage shared-memory ring
+// with 1-D bulk asynchronous copies (cp.async.bulk, the TMA engine's untiled form), each
+// stage guarded by a "full" mbarrier (transaction bytes) and an "empty" mbarrier
+// (consumer releases).  Consumers are G row groups of NTg threads; group g takes row slot
+// g of every stage, and each thread owns the same VPT 16-byte column vectors of every row
+// it touches (column vector c = lt + v*NTg), so per-column state (the weight, the dw
+// partial sums) lives in registers for the whole chunk.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+// Device-side error bits (see rmsnorm_train_device_error in the public header).
+enum : unsigned { kErrConsumerWait = 1u, kErrProducerWait = 2u };
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete.  Bounded: after kWaitLimitNs it records
+// `errbit` in the device error word, raises the CTA's abort flag and returns false.  Once
+// the abort flag is up every later wait returns at once, so all threads still run the
+// same barriers (no named barrier can then hang) and the CTA drains and exits.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag,
+                                                  unsigned* err_word, unsigned errbit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err_word, errbit);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// L2 policy for data that is read exactly once.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transaction bytes on `bar`.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory, and allow the next
+// grid to be scheduled early.  Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- BF16 packing --------------------------------------------------------------------
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Two FP32 values -> one word of two BF16 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ void stg128(void* p, uint4 v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  f[0] = bf_lo(u.x); f[1] = bf_hi(u.x);
+  f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
+  f[4] = bf_lo(u.z); f[5] = bf_hi(u.z);
+  f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  u.x = pack_bf2(f[0], f[1]);
+  u.y = pack_bf2(f[2], f[3]);
+  u.z = pack_bf2(f[4], f[5]);
+  u.w = pack_bf2(f[6], f[7]);
+  return u;
+}
+
+// Loads the 8 weights of column vector c as FP32.
+template <bool kFp32W>
+__device__ __forceinline__ void load_w8(const void* w, int c, float (&f)[8]) {
+  if constexpr (kFp32W) {
+    const float4* p = reinterpret_cast<const float4*>(w) + 2 * c;
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(w) + c);
+    unpack8(u, f);
+  }
+}
+
+// Butterfly sum over a warp: every lane ends with the same bits (a+b == b+a exactly).
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---- row addressing and the producer -------------------------------------------------
+
+struct RowMap {
+  int32_t nh;
+  int32_t H;
+  int64_t s_tok;
+  int64_t s_head;
+  __device__ __forceinline__ int64_t offset(int32_t r) const {
+    int32_t t = r / nh;
+    int32_t h = r - t * nh;
+    return static_cast<int64_t>(t) * s_tok + static_cast<int64_t>(h) * s_head;
+  }
+};
+
+// Copies rows [ra, rb) of a BF16 tensor into consecutive H-element slots at `dst`,
+// merging rows that are adjacent in memory into one bulk copy.
+__device__ __forceinline__ void copy_rows(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                          const RowMap& m, int32_t ra, int32_t rb,
+                                          uint64_t* bar, uint64_t pol) {
+  int32_t r = ra;
+  while (r < rb) {
+    int64_t off = m.offset(r);
+    int32_t n = 1;
+    while (r + n < rb && m.offset(r + n) == off + static_cast<int64_t>(n) * m.H) ++n;
+    bulk_g2s(dst + static_cast<int64_t>(r - ra) * m.H, src + off,
+             static_cast<uint32_t>(n) * static_cast<uint32_t>(m.H) * 2u, bar, pol);
+    r += n;
+  }
+}
+
+// Contiguous [R, H] tensor: rows [ra, rb) in one copy.
+__device__ __forceinline__ void copy_rows_contig(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                                 int32_t H, int32_t ra, int32_t rb,
+                                                 uint64_t* bar, uint64_t pol) {
+  bulk_g2s(dst, src + static_cast<int64_t>(ra) * H,
+           static_cast<uint32_t>(rb - ra) * static_cast<uint32_t>(H) * 2u, bar, pol);
+}
+
+}  // namespace rmsn

@@ -1,0 +1,194 @@
+// rmsn_fwd.cu -- RMSNorm training forward for sm_103a.
+//
+// Computes, per normalized row (flashinfer PR #8827, description; Measurement workload
+// line: eps 1e-6, y and h_new BF16, rstd FP32):
+//   [residual form]  h = BF16(x_in + residual)        (written; the norm is taken of h)
+//   rstd = 1 / sqrt(sum_j x_j^2 / H + eps)             (FP32)
+//   y_j  = BF16((x_j * rstd) * w_j)                    (round to nearest even)
+//
+// HBM-bound: 4 bytes per element (8 in the residual form) for ~3 flops.  Rows are staged
+// into shared memory by bulk asynchronous copies (one producer thread, S-stage mbarrier
+// ring) and consumed by row groups whose threads own fixed 16-byte column vectors, so
+// every global access is a 16-byte coalesced vector and the weight stays in registers.
+// Precision: the sum of squares is accumulated in FP32 (BF16 squares are exact in FP32,
+// so only the additions round); the reciprocal square root is the correctly rounded
+// __frsqrt_rn, which keeps rstd within 1e-6 relative of the FP64 value.
+#include "rmsn_common.cuh"
+#include "rmsn_launch.h"
+
+namespace rmsn {
+
+template <int VPT, bool kFp32W, bool kRes>
+__global__ void __launch_bounds__(kMaxThreads, 1) rmsn_fwd_kernel(const FwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int NT = kRes ? 2 : 1;
+  const int H = a.map.H;
+  const int NV = H >> 3;
+  const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const size_t stage_elems = static_cast<size_t>(NT) * G * H;
+
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_elems * 2);
+  uint64_t* empty = full + S;
+  float* red = reinterpret_cast<float*>(empty + S);  // [2][G][32]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * G * 32);
+
+  const int tid = threadIdx.x;
+  const int ncons = G * NTg;
+  const int32_t k = blockIdx.x;
+  const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
+  const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
+  const int32_t nstage = (r1 - r0 + G - 1) / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], static_cast<uint32_t>(G));
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Inputs may come from the kernel before us on the stream: wait for it before any
+  // global read, then let the next kernel start its prologue.
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+
+  if (tid >= ncons) {  // ---- producer warp ----
+    if (tid == ncons) {
+      const uint64_t pol = l2_evict_first_policy();
+      const RowMap m{a.map.nh, H, a.map.s_tok, a.map.s_head};
+      for (int32_t j = 0; j < nstage; ++j) {
+        const int s = j % S;
+        if (j >= S &&
+            !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                               a.err, kErrProducerWait))
+          break;
+        const int32_t ra = r0 + j * G;
+        const int32_t rb = min(ra + G, r1);
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u * NT);
+        __nv_bfloat16* dst = ring + s * stage_elems;
+        if (a.contig) {
+          copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
+          if constexpr (kRes) copy_rows_contig(dst + G * H, a.res, H, ra, rb, &full[s], pol);
+        } else {
+          copy_rows(dst, a.x, m, ra, rb, &full[s], pol);
+          if constexpr (kRes) copy_rows(dst + G * H, a.res, m, ra, rb, &full[s], pol);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
+  const int g = tid / NTg;
+  const int lt = tid - g * NTg;
+  float wv[VPT][8];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if (c < NV) load_w8<kFp32W>(a.w, c, wv[v]);
+  }
+  const float hf = static_cast<float>(H);  // exact for H < 2^24
+
+  for (int32_t j = 0; j < nstage; ++j) {
+    const int32_t row = r0 + j * G + g;
+    if (row >= r1) break;
+    const int s = j % S;
+    mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                      kErrConsumerWait);
+    const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+    const size_t out_row = static_cast<size_t>(row) * H;
+
+    uint4 hv[VPT];
+    float ss = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        uint4 u = lds128(xs + c * 8);
+        if constexpr (kRes) {
+          // The FP32 sum of two BF16 values is exact unless their exponents differ by
+          // more than 16, and then the smaller one is far below half a BF16 ulp of the
+          // larger: either way pack8's rounding gives BF16_RNE of the exact sum.
+          const uint4 q = lds128(xs + static_cast<size_t>(G) * H + c * 8);
+          float fa[8], fb[8];
+          unpack8(u, fa);
+          unpack8(q, fb);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) fa[e] = __fadd_rn(fa[e], fb[e]);
+          u = pack8(fa);
+          stg128(a.h + out_row + c * 8, u);
+        }
+        hv[v] = u;
+        float f[8];
+        unpack8(u, f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+      } else {
+        hv[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    ss = warp_allsum(ss);
+    if (NTg > 32) {
+      float* slot = red + ((j & 1) * G + g) * 32;
+      if ((lt & 31) == 0) slot[lt >> 5] = ss;
+      named_bar_sync(1 + g, NTg);
+      ss = 0.f;
+      for (int i = 0; i < (NTg >> 5); ++i) ss += slot[i];  // fixed order
+    } else {
+      __syncwarp();
+    }
+    // every thread of the group has read its vectors of this stage: release the slot
+    if (lt == 0) mbar_arrive(&empty[s]);
+
+    const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        float f[8];
+        unpack8(hv[v], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], rs), wv[v][e]);
+        stg128(a.y + out_row + c * 8, pack8(f));
+      }
+    }
+    if (lt == 0) a.rstd[row] = rs;
+  }
+}
+
+template <int VPT, bool kFp32W, bool kRes>
+static const void* fwd_kernel_ptr() {
+  return reinterpret_cast<const void*>(&rmsn_fwd_kernel<VPT, kFp32W, kRes>);
+}
+
+static const void* pick_fwd(int vpt, bool fp32w, bool res) {
+  if (vpt == 1) {
+    if (fp32w) return res ? fwd_kernel_ptr<1, true, true>() : fwd_kernel_ptr<1, true, false>();
+    return res ? fwd_kernel_ptr<1, false, true>() : fwd_kernel_ptr<1, false, false>();
+  }
+  if (fp32w) return res ? fwd_kernel_ptr<2, true, true>() : fwd_kernel_ptr<2, true, false>();
+  return res ? fwd_kernel_ptr<2, false, true>() : fwd_kernel_ptr<2, false, false>();
+}
+
+cudaError_t prepare_kernel(const void* fn, size_t smem);       // rmsn_api.cu
+int blocks_per_sm(const void* fn, int threads, size_t smem);   // rmsn_api.cu
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       void** args);                           // rmsn_api.cu
+
+int fwd_blocks_per_sm(const Shape& s, bool fp32w) {
+  return blocks_per_sm(pick_fwd(s.vpt, fp32w, s.tensors == 2), s.threads, s.smem);
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st) {
+  const void* fn = pick_fwd(s.vpt, fp32w, a.res != nullptr);
+  cudaError_t e = prepare_kernel(fn, s.smem);
+  if (e != cudaSuccess) return e;
+  FwdArgs copy = a;
+  void* args[] = {&copy};
+  return launch_pdl(fn, dim3(static_cast<unsigned>(a.P)), dim3(static_cast<unsigned>(s.threads)),
+                    s.smem, st, args);
+}
+
+}  // namespace rmsn

@@ -1,0 +1,133 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every entry point the public
+header declares, and rejects bad arguments before touching CUDA (every check here
+returns before the first CUDA runtime call, so no device is needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+BAD_PTR = 0x1000        # never dereferenced: every call below fails validation first
+BAD_PTR2 = 0x2000
+MISALIGNED = 0x1008
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rmsnorm_fwd_02_gb300 import build as B
+    B.build()
+    from rmsnorm_fwd_02_gb300 import _native as N
+    return N.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(rmsnorm_train_\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("rmsnorm_train_fwd", "rmsnorm_train_bwd",
+                 "rmsnorm_train_bwd_workspace_bytes", "rmsnorm_train_status_str",
+                 "rmsnorm_train_device_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from rmsnorm_fwd_02_gb300 import _native as N
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in N.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    from rmsnorm_fwd_02_gb300 import _native as N
+    for st in range(0, 7):
+        assert isinstance(N.status_str(st), str) and N.status_str(st)
+    assert N.status_str(0) == "ok"
+
+
+def fwd(lib, x=BAD_PTR, res=None, w=BAD_PTR, wd=0, y=BAD_PTR2, h=None, rstd=BAD_PTR2,
+        T=4, nh=1, H=64, s_tok=64, s_head=64, eps=1e-6):
+    return lib.rmsnorm_train_fwd(x, res, w, wd, y, h, rstd, T, nh, H, s_tok, s_head, eps,
+                                 None)
+
+
+def bwd(lib, x=BAD_PTR, dy=BAD_PTR, dh=None, rstd=BAD_PTR2, w=BAD_PTR, wd=0, dx=BAD_PTR2,
+        dw=BAD_PTR2, ws=BAD_PTR, wsb=1 << 20, T=4, nh=1, H=64, s_tok=64, s_head=64, det=1):
+    return lib.rmsnorm_train_bwd(x, dy, dh, rstd, w, wd, dx, dw, ws, wsb, T, nh, H, s_tok,
+                                 s_head, det, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(H=60), INVALID),                   # H not a multiple of 8
+    (dict(H=0), INVALID),
+    (dict(H=8200, s_tok=8200), UNSUPPORTED),  # above the largest width
+    (dict(T=-1), INVALID),
+    (dict(nh=0), INVALID),
+    (dict(x=None), INVALID),
+    (dict(w=None), INVALID),
+    (dict(y=None), INVALID),
+    (dict(rstd=None), INVALID),
+    (dict(x=MISALIGNED), INVALID),
+    (dict(y=MISALIGNED), INVALID),
+    (dict(wd=2), INVALID),
+    (dict(res=BAD_PTR), INVALID),            # residual without h_out
+    (dict(h=BAD_PTR2), INVALID),             # h_out without residual
+    (dict(s_tok=60), INVALID),               # stride not a multiple of 8 elements
+    (dict(nh=2, s_head=12), INVALID),
+    (dict(eps=-1.0), INVALID),
+    (dict(eps=float("nan")), INVALID),
+    (dict(eps=float("inf")), INVALID),
+    (dict(T=1 << 20, nh=4096), UNSUPPORTED),  # T*nh >= 2^31
+    (dict(T=0), OK),                         # empty: nothing to do, no CUDA call
+])
+def test_fwd_rejects_before_any_cuda_call(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(H=12), INVALID),
+    (dict(det=2), INVALID),
+    (dict(det=-1), INVALID),
+    (dict(x=None), INVALID),
+    (dict(dy=None), INVALID),
+    (dict(rstd=None), INVALID),
+    (dict(w=None), INVALID),
+    (dict(dx=None), INVALID),
+    (dict(dw=None), INVALID),
+    (dict(dh=MISALIGNED), INVALID),
+    (dict(ws=MISALIGNED), INVALID),
+    (dict(rstd=BAD_PTR2 + 2), INVALID),
+    (dict(wd=5), INVALID),
+    (dict(H=16384, s_tok=16384), UNSUPPORTED),
+])
+def test_bwd_rejects_before_any_cuda_call(lib, kw, want):
+    assert bwd(lib, **kw) == want
+
+
+def test_deterministic_workspace_size_depends_on_shape_only(lib):
+    f = lib.rmsnorm_train_bwd_workspace_bytes
+    # at most 304 partials of 2*H floats; a CTA takes at least 4 stages of rows
+    assert f(65536, 1, 4096, 1) == 304 * 2 * 4096 * 4
+    assert f(1, 1, 4096, 1) == 1 * 2 * 4096 * 4
+    assert f(65, 1, 4096, 1) == 17 * 2 * 4096 * 4
+    # H = 256: 8 rows per stage -> 32 rows per partial at least
+    assert f(64, 1, 256, 1) == 2 * 2 * 256 * 4
+    assert f(65536, 24, 256, 1) == 304 * 2 * 256 * 4
+    assert f(0, 1, 4096, 1) == 0
+    assert f(10, 1, 12, 1) == 0       # invalid width
+
+
+def test_package_import_needs_no_gpu():
+    import rmsnorm_fwd_02_gb300 as R
+    assert callable(R.rmsnorm_fwd) and callable(R.rmsnorm_train)

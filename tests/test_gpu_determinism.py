@@ -1,0 +1,125 @@
+"""Determinism and bitwise invariants of the CUDA path (no oracle needed).
+
+- deterministic=True: dx and dw bit-identical over 10 runs (the op's det mode contract,
+  flashinfer PR #8827 description; its test list checks det bit for bit twice).
+- both modes run the same forward and the same row pass: dx identical across modes.
+- per-head views equal the plain path on a gathered contiguous copy, bit for bit (y,
+  rstd, dx; dw too in deterministic mode, where the partition depends on R and H only).
+- the residual form's y and rstd equal the plain forward run on its h.
+"""
+import numpy as np
+import pytest
+import torch
+
+from rmsnorm_fwd_02_gb300 import _native as N
+from rmsnorm_fwd_02_gb300 import synth
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return parity.bits_of(t)
+
+
+@pytest.mark.parametrize("mk", [lambda: synth.stress(32768, 5120),
+                                lambda: synth.heads_strided(4096),
+                                lambda: synth.plain(4096)])
+def test_det_bitwise_10_runs(mk):
+    c = mk()
+    dc = parity.DeviceCase(c)
+    y, rstd, _ = parity.gpu_fwd(dc, False)
+    ref = None
+    for _ in range(10):
+        dx, dw = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, rstd, True)
+        cur = (_bits(dx), dw.cpu().numpy().view(np.uint32))
+        if ref is None:
+            ref = cur
+        else:
+            assert np.array_equal(ref[0], cur[0]) and np.array_equal(ref[1], cur[1])
+    y2, rstd2, _ = parity.gpu_fwd(dc, False)
+    assert np.array_equal(_bits(y), _bits(y2))
+    assert torch.equal(rstd, rstd2)
+    # non-deterministic mode: same dx bits
+    dxn, _ = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, rstd, False)
+    assert np.array_equal(ref[0], _bits(dxn))
+    assert N.rmsnorm_train_device_error(reset=True) == 0
+
+
+@pytest.mark.parametrize("strided", [True, False])
+def test_per_head_equals_plain_bitwise(strided):
+    c = synth.heads_strided(1024) if strided else synth.heads_contig(1024)
+    dc = parity.DeviceCase(c)
+    y, rstd, _ = parity.gpu_fwd(dc, False)
+    dx, dw = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, rstd, True)
+    # gathered contiguous copy as plain rows [T*nh, 256]
+    rows = np.arange(c.R)
+    flat = parity.gather_rows(c.x, c, rows).reshape(-1)
+    p = synth.Case(T=c.R, nh=1, H=c.H, s_tok=c.H, s_head=c.H, x=flat, dy=c.dy, w=c.w)
+    dp = parity.DeviceCase(p)
+    y2, rstd2, _ = parity.gpu_fwd(dp, False)
+    dx2, dw2 = parity.gpu_bwd(dp, dp.x, p.s_tok, p.s_head, rstd2, True)
+    assert np.array_equal(_bits(y), _bits(y2))
+    assert torch.equal(rstd, rstd2)
+    assert np.array_equal(_bits(dx), _bits(dx2))
+    assert torch.equal(dw, dw2)
+
+
+def test_residual_forward_equals_plain_on_h():
+    c = synth.residual(300)
+    dc = parity.DeviceCase(c)
+    y, rstd, h = parity.gpu_fwd(dc, True)
+    p = synth.Case(T=c.T, nh=1, H=c.H, s_tok=c.H, s_head=c.H, x=_bits(h), dy=c.dy, w=c.w)
+    dp = parity.DeviceCase(p)
+    y2, rstd2, _ = parity.gpu_fwd(dp, False)
+    assert np.array_equal(_bits(y), _bits(y2))
+    assert torch.equal(rstd, rstd2)
+
+
+def test_empty_input_zero_fills_dw():
+    c = synth.make_case(0, 0, 512)
+    dc = parity.DeviceCase(synth.make_case(0, 1, 512))
+    dw = torch.full((512,), 7.0, device="cuda")
+    dx = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.ones(1, device="cuda")
+    for det in (0, 1):
+        N.rmsnorm_train_bwd(dc.x, dc.dy, None, rstd, dc.w, N.RMSN_W_BF16, dx, dw, None, 0,
+                            0, 1, 512, 512, 512, det)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(dw).item() == 0
+        dw.fill_(7.0)
+    # forward with T = 0 is a no-op
+    y = torch.empty(16, dtype=torch.bfloat16, device="cuda")
+    N.rmsnorm_train_fwd(dc.x, None, dc.w, N.RMSN_W_BF16, y, None, rstd, 0, 1, 512, 512, 512,
+                        1e-6)
+    assert c.R == 0
+
+
+def test_workspace_too_small_is_rejected():
+    c = synth.plain(64)
+    dc = parity.DeviceCase(c)
+    need = N.rmsnorm_train_bwd_workspace_bytes(c.T, 1, c.H, True)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dx = torch.empty(c.R * c.H, dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty(c.H, dtype=torch.float32, device="cuda")
+    rstd = torch.ones(c.R, device="cuda")
+    with pytest.raises(N.RmsnError) as ei:
+        N.rmsnorm_train_bwd(dc.x, dc.dy, None, rstd, dc.w, N.RMSN_W_BF16, dx, dw, ws,
+                            need - 16, c.T, 1, c.H, c.H, c.H, True)
+    assert ei.value.status == 3
+
+
+def test_autograd_wrapper_matches_direct_calls():
+    import rmsnorm_fwd_02_gb300 as R
+    c = synth.plain(100)
+    dc = parity.DeviceCase(c)
+    x = dc.x.view(c.T, c.H).clone().requires_grad_(True)
+    w = dc.w.clone().requires_grad_(True)
+    y = R.rmsnorm_train(x, w, 1e-6, deterministic=True)
+    dy = dc.dy.view(c.T, c.H)
+    y.backward(dy)
+    y0, rstd0 = R.rmsnorm_fwd(dc.x.view(c.T, c.H), dc.w)
+    dx0, dw0 = R.rmsnorm_bwd(dy, dc.x.view(c.T, c.H), rstd0, dc.w, True)
+    assert torch.equal(y, y0)
+    assert torch.equal(x.grad, dx0)
+    assert torch.equal(w.grad, dw0.to(w.dtype))
