@@ -191,6 +191,24 @@ def gpu_uuid(dev: int):
         return None
 
 
+def d2d_copy_gbps(torch, dev, stream, nbytes: int = 1 << 30, reps: int = 10) -> float:
+    """Read+write bandwidth of a plain 1 GiB device-to-device copy (context only)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        dst.copy_(src)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        dst.copy_(src)
+    b.record(stream)
+    torch.cuda.synchronize()
+    gbs = 2.0 * nbytes * reps / (a.elapsed_time(b) * 1e-3) / 1e9
+    del src, dst
+    return gbs
+
+
 # ---- the CPU oracle baseline ------------------------------------------------------------
 
 def oracle_step(case, rows: np.ndarray):
@@ -361,6 +379,9 @@ def run_ours(args):
         sampler.stop()
     max_ms = reduce_max(total_ms, dist)
 
+    # ---- context: the device-to-device copy bandwidth of this GPU (cudaMemcpyAsync) ----
+    copy_gbs = d2d_copy_gbps(torch, dev, stream)
+
     step_bytes = fwd_bytes(R, H, wbytes) + bwd_bytes(R, H, wbytes)
     value = step_bytes * args.steps * ws / (max_ms * 1e-3) / 1e9
     fwd_us = statistics.mean(fwd_ms) * 1e3
@@ -452,6 +473,7 @@ def run_ours(args):
         "fwd": {"us": fwd_us, "GBps": fwd_achieved, "frac": fwd_achieved / peak},
         "bwd": {"us": bwd_us, "GBps": bwd_achieved, "frac": bwd_achieved / peak},
         "dw_err_over_budget": dw_ratio,
+        "d2d_copy_GBps": copy_gbs,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},

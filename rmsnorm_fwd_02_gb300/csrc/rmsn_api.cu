@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <unordered_map>
 
@@ -20,9 +21,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr size_t kRingTarget = 96 * 1024;  // shared-memory ring bytes per CTA (target)
 constexpr int kMaxStages = 8;
-// Deterministic backward: at most this many dw partials (CTAs), a fixed function of the
-// shape only.  2 x 152 is one wave of two CTAs per SM on a 152-SM GB300.
-constexpr int kDetMaxPartials = 304;
+// Deterministic backward: at most kDetSMs x (the CTAs an SM the kernel is built to keep
+// resident) dw partials -- a function of the shape only, so the same on every device
+// whatever its SM count.  152 is GB300's SM count: there the partition is one wave.
+constexpr int kDetSMs = 152;
 constexpr int kMinStagesPerCta = 4;  // smallest chunk a backward CTA takes, in stages
 
 std::mutex g_mu;
@@ -43,10 +45,21 @@ size_t shared_bytes(const Shape& s, int H) {
   return ring + 16 * static_cast<size_t>(s.stages) + 256 * static_cast<size_t>(s.groups) + 16;
 }
 
-Shape make_shape(int H, int tensors) {
+// Column vectors per thread, from the instantiated set `allowed` (descending): the
+// largest whose row of NV vectors splits into whole warps, else the largest that fills
+// at least one warp.
+int pick_vpt(int nv, std::initializer_list<int> allowed) {
+  for (int v : allowed)
+    if (nv % (32 * v) == 0) return v;
+  for (int v : allowed)
+    if (nv >= 32 * v) return v;
+  return 1;
+}
+
+Shape make_shape(int H, int tensors, int vpt) {
   Shape s{};
   const int nv = H / 8;
-  s.vpt = nv <= 32 ? 1 : 2;
+  s.vpt = vpt;
   const int per = (nv + s.vpt - 1) / s.vpt;
   s.ntg = ((per + 31) / 32) * 32;
   s.groups = s.ntg >= 256 ? 1 : 256 / s.ntg;
@@ -107,9 +120,9 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
   if (want < 1) want = 1;
   int64_t cap;
   if (det) {
-    cap = kDetMaxPartials;
+    cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.vpt);
   } else {
-    int occ = bwd_blocks_per_sm(s, fp32w);
+    const int occ = bwd_blocks_per_sm(s, fp32w);
     cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
   }
   return static_cast<int>(want < cap ? want : cap);
@@ -119,8 +132,17 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
 
 // ---- helpers used by the kernel translation units ------------------------------------
 
-Shape fwd_shape(int H, bool residual) { return make_shape(H, residual ? 2 : 1); }
-Shape bwd_shape(int H, bool with_dh) { return make_shape(H, with_dh ? 3 : 2); }
+// Forward: up to 4 vectors (32 columns) a thread, so per-row work (reductions, rstd) is
+// spread over many elements.  Backward: 2 vectors a thread up to H = 6144 (registers
+// hold x_hat, g, w and the dw sum/compensation of 16 columns), 4 above.
+Shape fwd_shape(int H, bool residual) {
+  return make_shape(H, residual ? 2 : 1, pick_vpt(H / 8, {4, 3, 2, 1}));
+}
+Shape bwd_shape(int H, bool with_dh) {
+  const int nv = H / 8;
+  const int vpt = nv <= 32 ? 1 : (nv <= 768 ? 2 : 4);
+  return make_shape(H, with_dh ? 3 : 2, vpt);
+}
 
 cudaError_t prepare_kernel(const void* fn, size_t smem) {
   int dev = 0;

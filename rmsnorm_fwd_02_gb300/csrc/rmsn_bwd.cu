@@ -3,18 +3,24 @@
 //
 // Per normalized row, with r the forward's rstd (flashinfer PR #8827, description: the
 // backward's BF16 dx and FP32 dw; the residual form's combined gradient):
-//   xhat_j = x_j * r,  g_j = dy_j * w_j,  c = (sum_j g_j * xhat_j) / H
+//   xhat_j = x_j * r,  g_j = dy_j * w_j,  c = (sum_j g_j * xhat_j) * (1/H)
 //   dx_j   = BF16((g_j - xhat_j * c) * r  [+ dh_j])
 //   dw_j  += dy_j * xhat_j          over every row of every CTA's chunk
 //
 // dw accuracy (PR #8849 and PR #8827's route notes: every dw element within
 // atol 1e-4 + rtol 1e-4 of an FP64 sum, a budget plain FP32 running sums break at large
-// T): each consumer thread keeps, for each of its columns, a running FP32 sum and a
-// running compensation term (Fast2Sum error of each addition).  A CTA writes its chunk's
-// partial as an unevaluated (hi, lo) FP32 pair per column; the finish kernel adds the P
-// pairs in a fixed order with Knuth's TwoSum.  The row -> CTA chunk mapping is fixed by
-// (R, P) and the finish order by P, so dw is bit-reproducible whenever P is; dx does not
-// depend on P at all.
+// T).  Two error sources are removed: the rounding of each product and the rounding of
+// each addition.  With rstd split as rs_hi (its top 8 significant bits) + rs_lo, the
+// product dy*x*rs_hi is exact in FP32 (dy*x carries at most 16 significant bits), and
+// dy*x*rs_lo is 2^-8 smaller.  Each consumer thread keeps per column a running FP32 sum
+// of the exact products and a compensation term that collects each addition's Fast2Sum
+// error plus the small dy*x*rs_lo terms.  A CTA writes its chunk's partial as an
+// unevaluated (hi, lo) FP32 pair per column; the finish kernel adds the P pairs in a
+// fixed order with Knuth's TwoSum.  What remains is about the final rounding of dw to
+// FP32.  The row -> CTA chunk mapping is fixed by (R, P) and the finish order by P, so dw
+// is bit-reproducible whenever P is; dx does not depend on P at all.
+//
+// Arithmetic runs on packed FP32 pairs (f32x2): two columns per instruction.
 #include "rmsn_common.cuh"
 #include "rmsn_launch.h"
 
@@ -29,8 +35,17 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
   return s;
 }
 
+// Launch bounds per column-vector count: VPT=2 serves H <= 6144 (up to 384 consumers +
+// the producer warp) with ~125 registers a thread, VPT=4 serves H up to 8192 with 256
+// consumers, VPT=1 the narrow rows (8 one-warp groups, two CTAs an SM).
+template <int VPT>
+constexpr int bwd_max_threads() { return VPT == 2 ? 416 : 288; }
+template <int VPT>
+constexpr int bwd_min_blocks() { return bwd_design_blocks_per_sm(VPT); }
+
 template <int VPT, bool kFp32W, bool kDh>
-__global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(bwd_max_threads<VPT>(), bwd_min_blocks<VPT>())
+    rmsn_bwd_rows_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
   const int H = a.map.H;
@@ -91,19 +106,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const Bwd
   // ---- consumers ----
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
-  float wv[VPT][8];
-  float acc[VPT][8], cmp[VPT][8];
+  f2 wv[VPT][4];
+  f2 acc[VPT][4], cmp[VPT][4];
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
-    if (c < NV) load_w8<kFp32W>(a.w, c, wv[v]);
+    if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      acc[v][e] = 0.f;
-      cmp[v][e] = 0.f;
+    for (int q = 0; q < 4; ++q) {
+      acc[v][q] = f2_splat(0.f);
+      cmp[v][q] = f2_splat(0.f);
     }
   }
-  const float hf = static_cast<float>(H);
+  const float inv_h = 1.0f / static_cast<float>(H);
 
   float rs_next = (r0 + g < r1) ? __ldg(a.rstd + r0 + g) : 0.f;
   for (int32_t j = 0; j < nstage; ++j) {
@@ -111,53 +126,54 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const Bwd
     if (row >= r1) break;
     const float rs = rs_next;
     if (row + G < r1) rs_next = __ldg(a.rstd + row + G);  // one row ahead
+    // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has at
+    // most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in FP32,
+    // and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
+    const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
+    const float rs_lo = __fsub_rn(rs, rs_hi);
+    const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi), rl2 = f2_splat(rs_lo);
     const int s = j % S;
     mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
                       kErrConsumerWait);
     const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
     const size_t out_row = static_cast<size_t>(row) * H;
 
-    uint4 xv[VPT], dv[VPT], hv[VPT];
-    float dot = 0.f;
+    f2 xh[VPT][4], gg[VPT][4];
+    uint4 hv[VPT];
+    f2 dot0 = f2_splat(0.f), dot1 = f2_splat(0.f);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
       if (c < NV) {
-        xv[v] = lds128(st + c * 8);
-        dv[v] = lds128(st + static_cast<size_t>(G) * H + c * 8);
+        const uint4 xv = lds128(st + c * 8);
+        const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
         if constexpr (kDh) hv[v] = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
-        float xf[8], df[8];
-        unpack8(xv[v], xf);
-        unpack8(dv[v], df);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          dot = fmaf(__fmul_rn(df[e], wv[v][e]), __fmul_rn(xf[e], rs), dot);
-      }
-    }
-    dot = warp_allsum(dot);
-    float* slot = red + ((j & 1) * G + g) * 32;
-    if (NTg > 32 && (lt & 31) == 0) slot[lt >> 5] = dot;
-
-    // dw: compensated running sums (independent of the row reduction, so they run while
-    // the other warps of the group reach the barrier)
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = lt + v * NTg;
-      if (c < NV) {
-        float xf[8], df[8];
-        unpack8(xv[v], xf);
-        unpack8(dv[v], df);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float p = __fmul_rn(df[e], __fmul_rn(xf[e], rs));
-          const float t = __fadd_rn(acc[v][e], p);
-          cmp[v][e] = __fadd_rn(cmp[v][e], __fadd_rn(__fsub_rn(acc[v][e], t), p));
-          acc[v][e] = t;
+        for (int q = 0; q < 4; ++q) {
+          const f2 x2 = bf2_to_f2(u4_get(xv, q));
+          const f2 d2 = bf2_to_f2(u4_get(dv, q));
+          xh[v][q] = f2_mul(x2, rs2);
+          gg[v][q] = f2_mul(d2, wv[v][q]);
+          if (q & 1)
+            dot1 = f2_fma(gg[v][q], xh[v][q], dot1);
+          else
+            dot0 = f2_fma(gg[v][q], xh[v][q], dot0);
+          // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
+          // compensation term, which also collects dy*x*rs_lo
+          const f2 dyx = f2_mul(d2, x2);
+          const f2 p = f2_mul(dyx, rh2);
+          const f2 t = f2_add(acc[v][q], p);
+          const f2 e = f2_add(f2_sub(acc[v][q], t), p);
+          cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
+          acc[v][q] = t;
         }
       }
     }
-
+    const f2 dsum = f2_add(dot0, dot1);
+    float dot = warp_allsum(f2_lo(dsum) + f2_hi(dsum));
     if (NTg > 32) {
+      float* slot = red + ((j & 1) * G + g) * 32;
+      if ((lt & 31) == 0) slot[lt >> 5] = dot;
       named_bar_sync(1 + g, NTg);
       dot = 0.f;
       for (int i = 0; i < (NTg >> 5); ++i) dot += slot[i];  // fixed order
@@ -166,24 +182,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const Bwd
     }
     if (lt == 0) mbar_arrive(&empty[s]);  // the group is done reading this stage
 
-    const float cc = __fdiv_rn(dot, hf);
+    const f2 nc2 = f2_splat(-(dot * inv_h));
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
       if (c < NV) {
-        float xf[8], df[8], hd[8];
-        unpack8(xv[v], xf);
-        unpack8(dv[v], df);
-        if constexpr (kDh) unpack8(hv[v], hd);
+        uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xh = __fmul_rn(xf[e], rs);
-          const float gg = __fmul_rn(df[e], wv[v][e]);
-          float d = __fmul_rn(fmaf(-xh, cc, gg), rs);
-          if constexpr (kDh) d = __fadd_rn(d, hd[e]);
-          xf[e] = d;
+        for (int q = 0; q < 4; ++q) {
+          f2 d = f2_mul(f2_fma(xh[v][q], nc2, gg[v][q]), rs2);  // (g - xhat*c) * rstd
+          if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv[v], q)));
+          o[q] = f2_to_bf2(d);
         }
-        stg128(a.dx + out_row + c * 8, pack8(xf));
+        stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
       }
     }
   }
@@ -195,18 +206,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const Bwd
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
       if (c < NV) {
-        float hi[8], lo[8];
+        f2 hi[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          hi[e] = __fadd_rn(acc[v][e], cmp[v][e]);
-          lo[e] = __fsub_rn(cmp[v][e], __fsub_rn(hi[e], acc[v][e]));
+        for (int q = 0; q < 4; ++q) {
+          hi[q] = f2_add(acc[v][q], cmp[v][q]);
+          lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
         }
-        float4* ph = reinterpret_cast<float4*>(part + c * 8);
-        float4* pl = reinterpret_cast<float4*>(part + H + c * 8);
-        ph[0] = make_float4(hi[0], hi[1], hi[2], hi[3]);
-        ph[1] = make_float4(hi[4], hi[5], hi[6], hi[7]);
-        pl[0] = make_float4(lo[0], lo[1], lo[2], lo[3]);
-        pl[1] = make_float4(lo[4], lo[5], lo[6], lo[7]);
+        ulonglong2* ph = reinterpret_cast<ulonglong2*>(part + c * 8);
+        ulonglong2* pl = reinterpret_cast<ulonglong2*>(part + H + c * 8);
+        ph[0] = make_ulonglong2(hi[0].v, hi[1].v);
+        ph[1] = make_ulonglong2(hi[2].v, hi[3].v);
+        pl[0] = make_ulonglong2(lo[0].v, lo[1].v);
+        pl[1] = make_ulonglong2(lo[2].v, lo[3].v);
       }
     }
     return;
@@ -221,25 +232,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_bwd_rows_kernel(const Bwd
     const int c = lt + v * NTg;
     if (c < NV) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float hi = __fadd_rn(acc[v][e], cmp[v][e]);
-        const float lo = __fsub_rn(cmp[v][e], __fsub_rn(hi, acc[v][e]));
-        cb[(2 * g) * H + c * 8 + e] = hi;
-        cb[(2 * g + 1) * H + c * 8 + e] = lo;
+      for (int q = 0; q < 4; ++q) {
+        const f2 hi = f2_add(acc[v][q], cmp[v][q]);
+        const f2 lo = f2_sub(cmp[v][q], f2_sub(hi, acc[v][q]));
+        *reinterpret_cast<unsigned long long*>(cb + (2 * g) * H + c * 8 + 2 * q) = hi.v;
+        *reinterpret_cast<unsigned long long*>(cb + (2 * g + 1) * H + c * 8 + 2 * q) = lo.v;
       }
     }
   }
   named_bar_sync(15, ncons);
   for (int col = tid; col < H; col += ncons) {
-    float s = 0.f, e = 0.f;
-    for (int gg = 0; gg < G; ++gg) {
+    float sacc = 0.f, e = 0.f;
+    for (int gi = 0; gi < G; ++gi) {
       float err;
-      s = two_sum(s, cb[(2 * gg) * H + col], err);
-      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gg + 1) * H + col]));
+      sacc = two_sum(sacc, cb[(2 * gi) * H + col], err);
+      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + col]));
     }
-    const float hi = __fadd_rn(s, e);
+    const float hi = __fadd_rn(sacc, e);
     part[col] = hi;
-    part[H + col] = __fsub_rn(e, __fsub_rn(hi, s));
+    part[H + col] = __fsub_rn(e, __fsub_rn(hi, sacc));
   }
 }
 
@@ -286,13 +297,18 @@ static const void* bwd_kernel_ptr() {
   return reinterpret_cast<const void*>(&rmsn_bwd_rows_kernel<VPT, kFp32W, kDh>);
 }
 
+template <int VPT>
+static const void* pick_bwd_v(bool fp32w, bool dh) {
+  if (fp32w) return dh ? bwd_kernel_ptr<VPT, true, true>() : bwd_kernel_ptr<VPT, true, false>();
+  return dh ? bwd_kernel_ptr<VPT, false, true>() : bwd_kernel_ptr<VPT, false, false>();
+}
+
 static const void* pick_bwd(int vpt, bool fp32w, bool dh) {
-  if (vpt == 1) {
-    if (fp32w) return dh ? bwd_kernel_ptr<1, true, true>() : bwd_kernel_ptr<1, true, false>();
-    return dh ? bwd_kernel_ptr<1, false, true>() : bwd_kernel_ptr<1, false, false>();
+  switch (vpt) {
+    case 1: return pick_bwd_v<1>(fp32w, dh);
+    case 2: return pick_bwd_v<2>(fp32w, dh);
+    default: return pick_bwd_v<4>(fp32w, dh);
   }
-  if (fp32w) return dh ? bwd_kernel_ptr<2, true, true>() : bwd_kernel_ptr<2, true, false>();
-  return dh ? bwd_kernel_ptr<2, false, true>() : bwd_kernel_ptr<2, false, false>();
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem);

@@ -116,6 +116,66 @@ __device__ __forceinline__ void pdl_allow_next_grid() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---- packed FP32 pairs (sm_100+ f32x2 arithmetic, one instruction for two lanes) -----
+//
+// A pair lives in one 64-bit register pair; every operation rounds each lane to nearest
+// even exactly as its scalar counterpart would (no flush to zero).
+
+struct f2 {
+  unsigned long long v;
+};
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f2 f2_splat(float a) { return f2_make(a, a); }
+__device__ __forceinline__ float f2_lo(f2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(f2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return hi;
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+// a * b + c with one rounding per lane
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
+// One word of two BF16 (low half = element 2i) -> the pair of their FP32 values (exact).
+__device__ __forceinline__ f2 bf2_to_f2(uint32_t u) {
+  return f2_make(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// The pair rounded to two BF16 (nearest even), element 2i in the low half.
+__device__ __forceinline__ uint32_t f2_to_bf2(f2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // ---- BF16 packing --------------------------------------------------------------------
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -163,6 +223,29 @@ __device__ __forceinline__ void load_w8(const void* w, int c, float (&f)[8]) {
     uint4 u = __ldg(reinterpret_cast<const uint4*>(w) + c);
     unpack8(u, f);
   }
+}
+
+// Loads the 8 weights of column vector c as four FP32 pairs.
+template <bool kFp32W>
+__device__ __forceinline__ void load_w8_pairs(const void* w, int c, f2 (&p)[4]) {
+  if constexpr (kFp32W) {
+    const float4* q = reinterpret_cast<const float4*>(w) + 2 * c;
+    float4 a = __ldg(q), b = __ldg(q + 1);
+    p[0] = f2_make(a.x, a.y);
+    p[1] = f2_make(a.z, a.w);
+    p[2] = f2_make(b.x, b.y);
+    p[3] = f2_make(b.z, b.w);
+  } else {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(w) + c);
+    p[0] = bf2_to_f2(u.x);
+    p[1] = bf2_to_f2(u.y);
+    p[2] = bf2_to_f2(u.z);
+    p[3] = bf2_to_f2(u.w);
+  }
+}
+
+__device__ __forceinline__ uint32_t u4_get(const uint4& u, int q) {
+  return q == 0 ? u.x : (q == 1 ? u.y : (q == 2 ? u.z : u.w));
 }
 
 // Butterfly sum over a warp: every lane ends with the same bits (a+b == b+a exactly).

@@ -18,8 +18,9 @@
 
 namespace rmsn {
 
+// At most 256 consumers (G*NTg) + the producer warp; two CTAs an SM.
 template <int VPT, bool kFp32W, bool kRes>
-__global__ void __launch_bounds__(kMaxThreads, 1) rmsn_fwd_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kRes ? 2 : 1;
   const int H = a.map.H;
@@ -83,11 +84,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_fwd_kernel(const FwdArgs 
   // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
-  float wv[VPT][8];
+  f2 wv[VPT][4];
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
-    if (c < NV) load_w8<kFp32W>(a.w, c, wv[v]);
+    if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
   }
   const float hf = static_cast<float>(H);  // exact for H < 2^24
 
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_fwd_kernel(const FwdArgs 
     const size_t out_row = static_cast<size_t>(row) * H;
 
     uint4 hv[VPT];
-    float ss = 0.f;
+    f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);  // two chains, fixed combine order
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
@@ -110,26 +111,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_fwd_kernel(const FwdArgs 
         if constexpr (kRes) {
           // The FP32 sum of two BF16 values is exact unless their exponents differ by
           // more than 16, and then the smaller one is far below half a BF16 ulp of the
-          // larger: either way pack8's rounding gives BF16_RNE of the exact sum.
+          // larger: either way the rounding below gives BF16_RNE of the exact sum.
           const uint4 q = lds128(xs + static_cast<size_t>(G) * H + c * 8);
-          float fa[8], fb[8];
-          unpack8(u, fa);
-          unpack8(q, fb);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) fa[e] = __fadd_rn(fa[e], fb[e]);
-          u = pack8(fa);
+          u.x = f2_to_bf2(f2_add(bf2_to_f2(u.x), bf2_to_f2(q.x)));
+          u.y = f2_to_bf2(f2_add(bf2_to_f2(u.y), bf2_to_f2(q.y)));
+          u.z = f2_to_bf2(f2_add(bf2_to_f2(u.z), bf2_to_f2(q.z)));
+          u.w = f2_to_bf2(f2_add(bf2_to_f2(u.w), bf2_to_f2(q.w)));
           stg128(a.h + out_row + c * 8, u);
         }
         hv[v] = u;
-        float f[8];
-        unpack8(u, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        const f2 e0 = bf2_to_f2(u.x), e1 = bf2_to_f2(u.y);
+        const f2 e2 = bf2_to_f2(u.z), e3 = bf2_to_f2(u.w);
+        ss0 = f2_fma(e0, e0, ss0);
+        ss1 = f2_fma(e1, e1, ss1);
+        ss0 = f2_fma(e2, e2, ss0);
+        ss1 = f2_fma(e3, e3, ss1);
       } else {
         hv[v] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    ss = warp_allsum(ss);
+    const f2 sp = f2_add(ss0, ss1);
+    float ss = warp_allsum(f2_lo(sp) + f2_hi(sp));
     if (NTg > 32) {
       float* slot = red + ((j & 1) * G + g) * 32;
       if ((lt & 31) == 0) slot[lt >> 5] = ss;
@@ -143,15 +145,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) rmsn_fwd_kernel(const FwdArgs 
     if (lt == 0) mbar_arrive(&empty[s]);
 
     const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
+    const f2 rs2 = f2_splat(rs);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
       if (c < NV) {
-        float f[8];
-        unpack8(hv[v], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], rs), wv[v][e]);
-        stg128(a.y + out_row + c * 8, pack8(f));
+        uint4 o;
+        o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].x), rs2), wv[v][0]));
+        o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].y), rs2), wv[v][1]));
+        o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].z), rs2), wv[v][2]));
+        o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].w), rs2), wv[v][3]));
+        stg128(a.y + out_row + c * 8, o);
       }
     }
     if (lt == 0) a.rstd[row] = rs;
@@ -163,13 +167,19 @@ static const void* fwd_kernel_ptr() {
   return reinterpret_cast<const void*>(&rmsn_fwd_kernel<VPT, kFp32W, kRes>);
 }
 
+template <int VPT>
+static const void* pick_fwd_v(bool fp32w, bool res) {
+  if (fp32w) return res ? fwd_kernel_ptr<VPT, true, true>() : fwd_kernel_ptr<VPT, true, false>();
+  return res ? fwd_kernel_ptr<VPT, false, true>() : fwd_kernel_ptr<VPT, false, false>();
+}
+
 static const void* pick_fwd(int vpt, bool fp32w, bool res) {
-  if (vpt == 1) {
-    if (fp32w) return res ? fwd_kernel_ptr<1, true, true>() : fwd_kernel_ptr<1, true, false>();
-    return res ? fwd_kernel_ptr<1, false, true>() : fwd_kernel_ptr<1, false, false>();
+  switch (vpt) {
+    case 1: return pick_fwd_v<1>(fp32w, res);
+    case 2: return pick_fwd_v<2>(fp32w, res);
+    case 3: return pick_fwd_v<3>(fp32w, res);
+    default: return pick_fwd_v<4>(fp32w, res);
   }
-  if (fp32w) return res ? fwd_kernel_ptr<2, true, true>() : fwd_kernel_ptr<2, true, false>();
-  return res ? fwd_kernel_ptr<2, false, true>() : fwd_kernel_ptr<2, false, false>();
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem);       // rmsn_api.cu

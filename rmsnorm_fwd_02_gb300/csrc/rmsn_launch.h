@@ -72,6 +72,10 @@ cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
+// CTAs per SM the backward row kernel is built to keep resident (its launch bounds'
+// minimum), a compile-time property: 2 for one-vector threads, else 1.
+constexpr int bwd_design_blocks_per_sm(int vpt) { return vpt == 1 ? 2 : 1; }
+
 // Resident CTAs per SM of the chosen row kernel (cached per device).
 int fwd_blocks_per_sm(const Shape& s, bool fp32w);
 int bwd_blocks_per_sm(const Shape& s, bool fp32w);

@@ -117,13 +117,16 @@ def test_bwd_rejects_before_any_cuda_call(lib, kw, want):
 
 def test_deterministic_workspace_size_depends_on_shape_only(lib):
     f = lib.rmsnorm_train_bwd_workspace_bytes
-    # at most 304 partials of 2*H floats; a CTA takes at least 4 stages of rows
-    assert f(65536, 1, 4096, 1) == 304 * 2 * 4096 * 4
+    # H = 4096: one row group of 2-vector threads, one CTA an SM -> at most 152 partials
+    # of 2*H floats; a CTA takes at least 4 stages (4 rows)
+    assert f(65536, 1, 4096, 1) == 152 * 2 * 4096 * 4
     assert f(1, 1, 4096, 1) == 1 * 2 * 4096 * 4
     assert f(65, 1, 4096, 1) == 17 * 2 * 4096 * 4
-    # H = 256: 8 rows per stage -> 32 rows per partial at least
+    # H = 256: 8 one-warp row groups (8 rows a stage), two CTAs an SM -> at most 304
     assert f(64, 1, 256, 1) == 2 * 2 * 256 * 4
     assert f(65536, 24, 256, 1) == 304 * 2 * 256 * 4
+    # H = 8192: 4-vector threads, one CTA an SM
+    assert f(131072, 1, 8192, 1) == 152 * 2 * 8192 * 4
     assert f(0, 1, 4096, 1) == 0
     assert f(10, 1, 12, 1) == 0       # invalid width
 
