@@ -485,6 +485,113 @@ def run_ours(args):
     return 0
 
 
+# ---- per-workload sweep (one JSON line per op and workload; not the headline) -----------
+
+SWEEP = [
+    # label, T, H, nh, buf_heads, w_fp32, residual
+    ("plain", 16384, 4096, 1, None, False, False),
+    ("plain", 65536, 4096, 1, None, False, False),
+    ("stress", 32768, 1536, 1, None, True, False),
+    ("stress", 131072, 1536, 1, None, True, False),
+    ("stress", 32768, 2048, 1, None, True, False),
+    ("stress", 131072, 2048, 1, None, True, False),
+    ("stress", 32768, 5120, 1, None, True, False),
+    ("stress", 131072, 5120, 1, None, True, False),
+    ("residual", 30720, 6144, 1, None, False, True),
+    ("residual", 65536, 6144, 1, None, False, True),
+    ("heads24of32", 4096, 256, 24, 32, True, False),
+    ("heads24of32", 65536, 256, 24, 32, True, False),
+    ("heads4", 65536, 256, 4, None, True, False),
+]
+
+
+def run_sweep(args):
+    """Times each op of each workload: `reps` launches, each after an L2 flush (a 512 MiB
+    memset outside the events), CUDA events on the launch stream, median."""
+    import torch
+    from rmsnorm_fwd_02_gb300 import _native as N
+    from rmsnorm_fwd_02_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    lib = N.lib()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peak, peak_kind = measured_peak()
+
+    def dbf(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def timed(fn, reps):
+        out = []
+        for _ in range(3):
+            fn()
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(out)
+
+    for label, T, H, nh, bh, w32, res in SWEEP:
+        c = synth.make_case(0, T, H, nh=nh, buf_heads=bh, w_fp32=w32, residual=res, dh=res)
+        R = c.R
+        wbytes = 4 if w32 else 2
+        wd = 1 if w32 else 0
+        x, dy, w = dbf(c.x), dbf(c.dy), (torch.from_numpy(c.w).to(dev) if w32 else dbf(c.w))
+        rr = dbf(c.residual) if res else None
+        dh = dbf(c.dh) if res else None
+        y = torch.empty(R * H, dtype=torch.bfloat16, device=dev)
+        h = torch.empty_like(y) if res else None
+        dx = torch.empty_like(y)
+        rstd = torch.empty(R, dtype=torch.float32, device=dev)
+        dw = torch.empty(H, dtype=torch.float32, device=dev)
+
+        def fwd():
+            st = lib.rmsnorm_train_fwd(x.data_ptr(), rr.data_ptr() if res else None,
+                                       w.data_ptr(), wd, y.data_ptr(),
+                                       h.data_ptr() if res else None, rstd.data_ptr(), T, nh,
+                                       H, c.s_tok, c.s_head, 1e-6, sh)
+            assert st == 0, st
+
+        fwd()
+        xs = h if res else x
+        s_tok, s_head = (nh * H, H) if res else (c.s_tok, c.s_head)
+        rows = [("fwd", fwd, (8 if res else 4) * R * H + 4 * R + wbytes * H)]
+        for det in (1, 0):
+            for use_dh in ((False, True) if res else (False,)):
+                nws = N.rmsnorm_train_bwd_workspace_bytes(T, nh, H, det)
+                ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+
+                def bwd(det=det, use_dh=use_dh, ws=ws, nws=nws):
+                    st = lib.rmsnorm_train_bwd(xs.data_ptr(), dy.data_ptr(),
+                                               dh.data_ptr() if use_dh else None,
+                                               rstd.data_ptr(), w.data_ptr(), wd,
+                                               dx.data_ptr(), dw.data_ptr(), ws.data_ptr(),
+                                               nws, T, nh, H, s_tok, s_head, det, sh)
+                    assert st == 0, st
+
+                name = ("bwd_det" if det else "bwd_nondet") + ("+dh" if use_dh else "")
+                rows.append((name, bwd, (8 if use_dh else 6) * R * H + 4 * R + wbytes * H
+                             + 4 * H))
+        for name, fn, nbytes in rows:
+            us = timed(fn, args.sweep_reps)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            print(json.dumps({"sweep": label, "op": name, "T": T, "H": H, "nh": nh,
+                              "w": "fp32" if w32 else "bf16", "us": round(us, 2),
+                              "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "peak": peak, "peak_kind": peak_kind,
+                              "bytes": nbytes}), flush=True)
+        del x, dy, w, y, dx, rstd, dw, h, rr, dh
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -497,11 +604,16 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-dw-check", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time each op on every workload family (one line each) instead")
+    ap.add_argument("--sweep-reps", type=int, default=30)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -41,8 +41,7 @@ uint64_t key(int dev, const void* fn, uint64_t extra) {
 }
 
 size_t shared_bytes(const Shape& s, int H) {
-  const size_t ring = static_cast<size_t>(s.stages) * s.tensors * s.groups * H * 2;
-  return ring + 16 * static_cast<size_t>(s.stages) + 256 * static_cast<size_t>(s.groups) + 16;
+  return smem_layout(s.stages, s.tensors, s.groups, H).total;
 }
 
 // Column vectors per thread, from the instantiated set `allowed` (descending): the
@@ -69,6 +68,7 @@ Shape make_shape(int H, int tensors, int vpt) {
   int st = static_cast<int>(kRingTarget / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
   s.threads = s.groups * s.ntg + kProducerThreads;
+  s.wide = s.threads > 288 || s.vpt == 4;
   s.smem = shared_bytes(s, H);
   return s;
 }
@@ -120,7 +120,7 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
   if (want < 1) want = 1;
   int64_t cap;
   if (det) {
-    cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.vpt);
+    cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.vpt, s.wide);
   } else {
     const int occ = bwd_blocks_per_sm(s, fp32w);
     cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);

@@ -3,7 +3,8 @@
 //
 // Per normalized row, with r the forward's rstd (flashinfer PR #8827, description: the
 // backward's BF16 dx and FP32 dw; the residual form's combined gradient):
-//   xhat_j = x_j * r,  g_j = dy_j * w_j,  c = (sum_j g_j * xhat_j) * (1/H)
+//   xhat_j = x_j * r,  g_j = dy_j * w_j,  c = (1/H) sum_j g_j * xhat_j
+//        = (r/H) * sum_j (dy_j * w_j) * x_j
 //   dx_j   = BF16((g_j - xhat_j * c) * r  [+ dh_j])
 //   dw_j  += dy_j * xhat_j          over every row of every CTA's chunk
 //
@@ -20,6 +21,7 @@
 // FP32.  The row -> CTA chunk mapping is fixed by (R, P) and the finish order by P, so dw
 // is bit-reproducible whenever P is; dx does not depend on P at all.
 //
+// Split-phase rows (see the consumer loop) keep the row reduction off the critical path.
 // Arithmetic runs on packed FP32 pairs (f32x2): two columns per instruction.
 #include "rmsn_common.cuh"
 #include "rmsn_launch.h"
@@ -35,29 +37,32 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
   return s;
 }
 
-// Launch bounds per column-vector count: VPT=2 serves H <= 6144 (up to 384 consumers +
-// the producer warp) with ~125 registers a thread, VPT=4 serves H up to 8192 with 256
-// consumers, VPT=1 the narrow rows (8 one-warp groups, two CTAs an SM).
-template <int VPT>
-constexpr int bwd_max_threads() { return VPT == 2 ? 416 : 288; }
-template <int VPT>
-constexpr int bwd_min_blocks() { return bwd_design_blocks_per_sm(VPT); }
+// Launch bounds per shape class: up to 256 consumers + the producer warp, two CTAs an
+// SM (VPT 1 or 2, H <= 4096); "wide" VPT=2 rows of H 4104..6144 with up to 384 consumers,
+// one CTA an SM; VPT=4 (H up to 8192) with 256 consumers, one CTA an SM.
+template <int VPT, bool kWide>
+constexpr int bwd_max_threads() { return (kWide && VPT == 2) ? 416 : 288; }
+template <int VPT, bool kWide>
+constexpr int bwd_min_blocks() { return bwd_design_blocks_per_sm(VPT, kWide); }
 
-template <int VPT, bool kFp32W, bool kDh>
-__global__ void __launch_bounds__(bwd_max_threads<VPT>(), bwd_min_blocks<VPT>())
+template <int VPT, bool kWide, bool kFp32W, bool kDh>
+__global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<VPT, kWide>())
     rmsn_bwd_rows_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
   const int H = a.map.H;
   const int NV = H >> 3;
   const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
+  const SmemLayout L = smem_layout(S, NT, G, H);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_elems * 2);
-  uint64_t* empty = full + S;
-  float* red = reinterpret_cast<float*>(empty + S);  // [2][G][32]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * G * 32);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kRedBufs][G]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kRedBufs][G][32]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
 
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
@@ -69,8 +74,9 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT>(), bwd_min_blocks<VPT>())
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(G));
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NW));  // one arrival per warp
     }
+    for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -103,9 +109,15 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT>(), bwd_min_blocks<VPT>())
     return;
   }
 
-  // ---- consumers ----
+  // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
+  //
+  // Split-phase rows: phase A of row j forms each warp's partial of sum_j (dy*w)*x and
+  // arrives on the row's reduction mbarrier; phase B of row j-1 waits on that barrier
+  // (normally long complete), re-reads row j-1 from shared memory, and produces dx and
+  // the dw contributions.  Registers hold only w and the dw state across rows.
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
+  const int wg = lt >> 5, lane = lt & 31;
   f2 wv[VPT][4];
   f2 acc[VPT][4], cmp[VPT][4];
 #pragma unroll
@@ -119,84 +131,95 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT>(), bwd_min_blocks<VPT>())
     }
   }
   const float inv_h = 1.0f / static_cast<float>(H);
+  const int32_t ng = (r1 - r0 > g) ? (r1 - r0 - g + G - 1) / G : 0;  // rows of this group
 
-  float rs_next = (r0 + g < r1) ? __ldg(a.rstd + r0 + g) : 0.f;
-  for (int32_t j = 0; j < nstage; ++j) {
-    const int32_t row = r0 + j * G + g;
-    if (row >= r1) break;
-    const float rs = rs_next;
-    if (row + G < r1) rs_next = __ldg(a.rstd + row + G);  // one row ahead
-    // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has at
-    // most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in FP32,
-    // and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
-    const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
-    const float rs_lo = __fsub_rn(rs, rs_hi);
-    const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi), rl2 = f2_splat(rs_lo);
-    const int s = j % S;
-    mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                      kErrConsumerWait);
-    const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
-    const size_t out_row = static_cast<size_t>(row) * H;
-
-    f2 xh[VPT][4], gg[VPT][4];
-    uint4 hv[VPT];
-    f2 dot0 = f2_splat(0.f), dot1 = f2_splat(0.f);
+  float rs_prev = 0.f;  // rstd of row j-1 (loaded during phase A of row j-1)
+  for (int32_t j = 0; j <= ng; ++j) {
+    float rs_new = 0.f;
+    // ---- phase A, row j: partial of sum (dy*w)*x ----
+    if (j < ng) {
+      const int32_t row = r0 + j * G + g;
+      rs_new = __ldg(a.rstd + row);  // consumed one iteration later
+      const int s = j % S;
+      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                        kErrConsumerWait);
+      const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      f2 dot0 = f2_splat(0.f), dot1 = f2_splat(0.f);
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = lt + v * NTg;
-      if (c < NV) {
-        const uint4 xv = lds128(st + c * 8);
-        const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
-        if constexpr (kDh) hv[v] = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          const uint4 xv = lds128(st + c * 8);
+          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const f2 x2 = bf2_to_f2(u4_get(xv, q));
-          const f2 d2 = bf2_to_f2(u4_get(dv, q));
-          xh[v][q] = f2_mul(x2, rs2);
-          gg[v][q] = f2_mul(d2, wv[v][q]);
-          if (q & 1)
-            dot1 = f2_fma(gg[v][q], xh[v][q], dot1);
-          else
-            dot0 = f2_fma(gg[v][q], xh[v][q], dot0);
-          // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
-          // compensation term, which also collects dy*x*rs_lo
-          const f2 dyx = f2_mul(d2, x2);
-          const f2 p = f2_mul(dyx, rh2);
-          const f2 t = f2_add(acc[v][q], p);
-          const f2 e = f2_add(f2_sub(acc[v][q], t), p);
-          cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
-          acc[v][q] = t;
+          for (int q = 0; q < 4; ++q) {
+            const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wv[v][q]);
+            if (q & 1)
+              dot1 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot1);
+            else
+              dot0 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot0);
+          }
         }
       }
+      const f2 dsum = f2_add(dot0, dot1);
+      const float dot = warp_allsum(f2_lo(dsum) + f2_hi(dsum));
+      if (lane == 0) {
+        slots[((j % kRedBufs) * G + g) * 32 + wg] = dot;
+        mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+      }
     }
-    const f2 dsum = f2_add(dot0, dot1);
-    float dot = warp_allsum(f2_lo(dsum) + f2_hi(dsum));
-    if (NTg > 32) {
-      float* slot = red + ((j & 1) * G + g) * 32;
-      if ((lt & 31) == 0) slot[lt >> 5] = dot;
-      named_bar_sync(1 + g, NTg);
-      dot = 0.f;
-      for (int i = 0; i < (NTg >> 5); ++i) dot += slot[i];  // fixed order
-    } else {
+    // ---- phase B, row j-1: dx and the dw contributions ----
+    if (j >= 1) {
+      const int32_t jj = j - 1;
+      const int32_t row = r0 + jj * G + g;
+      const int s = jj % S;
+      const int rb = (jj % kRedBufs) * G + g;
+      const float rs = rs_prev;
+      // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
+      // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
+      // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
+      const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
+      const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi), rl2 = f2_splat(__fsub_rn(rs, rs_hi));
+      mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag,
+                        a.err, kErrConsumerWait);
+      // c = (1/H) sum g*xhat = (rstd/H) sum (dy*w)*x
+      const f2 nc2 = f2_splat(-(slot_sum(slots + rb * 32, NW) * (rs * inv_h)));
+      const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      const size_t out_row = static_cast<size_t>(row) * H;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          const uint4 xv = lds128(st + c * 8);
+          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+          uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (kDh) hv = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2 x2 = bf2_to_f2(u4_get(xv, q));
+            const f2 d2 = bf2_to_f2(u4_get(dv, q));
+            const f2 xh = f2_mul(x2, rs2);
+            const f2 gw = f2_mul(d2, wv[v][q]);
+            f2 d = f2_mul(f2_fma(xh, nc2, gw), rs2);  // (g - xhat*c) * rstd
+            if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
+            o[q] = f2_to_bf2(d);
+            // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
+            // compensation term, which also collects dy*x*rs_lo
+            const f2 dyx = f2_mul(d2, x2);
+            const f2 p = f2_mul(dyx, rh2);
+            const f2 t = f2_add(acc[v][q], p);
+            const f2 e = f2_add(f2_sub(acc[v][q], t), p);
+            cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
+            acc[v][q] = t;
+          }
+          stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+      }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
     }
-    if (lt == 0) mbar_arrive(&empty[s]);  // the group is done reading this stage
-
-    const f2 nc2 = f2_splat(-(dot * inv_h));
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = lt + v * NTg;
-      if (c < NV) {
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          f2 d = f2_mul(f2_fma(xh[v][q], nc2, gg[v][q]), rs2);  // (g - xhat*c) * rstd
-          if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv[v], q)));
-          o[q] = f2_to_bf2(d);
-        }
-        stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
-      }
-    }
+    rs_prev = rs_new;
   }
 
   // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----
@@ -223,8 +246,8 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT>(), bwd_min_blocks<VPT>())
     return;
   }
   // several row groups: combine them through shared memory in group order.  The ring is
-  // free once every consumer is past its loop (each stage was fully waited on by the
-  // group that owns its first row).
+  // free once every consumer is past its loop: each stage was waited on (full) by every
+  // group that had a row in it before that group finished.
   named_bar_sync(15, ncons);
   float* cb = reinterpret_cast<float*>(smem);  // [G][2][H]
 #pragma unroll
@@ -292,23 +315,22 @@ __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
   }
 }
 
-template <int VPT, bool kFp32W, bool kDh>
+template <int VPT, bool kWide, bool kFp32W, bool kDh>
 static const void* bwd_kernel_ptr() {
-  return reinterpret_cast<const void*>(&rmsn_bwd_rows_kernel<VPT, kFp32W, kDh>);
+  return reinterpret_cast<const void*>(&rmsn_bwd_rows_kernel<VPT, kWide, kFp32W, kDh>);
 }
 
-template <int VPT>
+template <int VPT, bool kWide>
 static const void* pick_bwd_v(bool fp32w, bool dh) {
-  if (fp32w) return dh ? bwd_kernel_ptr<VPT, true, true>() : bwd_kernel_ptr<VPT, true, false>();
-  return dh ? bwd_kernel_ptr<VPT, false, true>() : bwd_kernel_ptr<VPT, false, false>();
+  if (fp32w)
+    return dh ? bwd_kernel_ptr<VPT, kWide, true, true>() : bwd_kernel_ptr<VPT, kWide, true, false>();
+  return dh ? bwd_kernel_ptr<VPT, kWide, false, true>() : bwd_kernel_ptr<VPT, kWide, false, false>();
 }
 
-static const void* pick_bwd(int vpt, bool fp32w, bool dh) {
-  switch (vpt) {
-    case 1: return pick_bwd_v<1>(fp32w, dh);
-    case 2: return pick_bwd_v<2>(fp32w, dh);
-    default: return pick_bwd_v<4>(fp32w, dh);
-  }
+static const void* pick_bwd(const Shape& s, bool fp32w, bool dh) {
+  if (s.vpt == 1) return pick_bwd_v<1, false>(fp32w, dh);
+  if (s.vpt == 2) return s.wide ? pick_bwd_v<2, true>(fp32w, dh) : pick_bwd_v<2, false>(fp32w, dh);
+  return pick_bwd_v<4, true>(fp32w, dh);
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem);
@@ -317,11 +339,11 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
                        void** args);
 
 int bwd_blocks_per_sm(const Shape& s, bool fp32w) {
-  return blocks_per_sm(pick_bwd(s.vpt, fp32w, s.tensors == 3), s.threads, s.smem);
+  return blocks_per_sm(pick_bwd(s, fp32w, s.tensors == 3), s.threads, s.smem);
 }
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st) {
-  const void* fn = pick_bwd(s.vpt, fp32w, a.dh != nullptr);
+  const void* fn = pick_bwd(s, fp32w, a.dh != nullptr);
   cudaError_t e = prepare_kernel(fn, s.smem);
   if (e != cudaSuccess) return e;
   BwdArgs copy = a;

@@ -255,6 +255,20 @@ __device__ __forceinline__ float warp_allsum(float v) {
   return v;
 }
 
+// Sum of a row's nw per-warp partials in slot order (nw <= 16; the slot row is 16-byte
+// aligned, so four vector loads cover it).  Every thread gets the same bits.
+__device__ __forceinline__ float slot_sum(const float* slot, int nw) {
+  float acc = 0.f;
+  for (int i = 0; i < nw; i += 4) {
+    const float4 q = *reinterpret_cast<const float4*>(slot + i);
+    acc += q.x;
+    if (i + 1 < nw) acc += q.y;
+    if (i + 2 < nw) acc += q.z;
+    if (i + 3 < nw) acc += q.w;
+  }
+  return acc;
+}
+
 // ---- row addressing and the producer -------------------------------------------------
 
 struct RowMap {

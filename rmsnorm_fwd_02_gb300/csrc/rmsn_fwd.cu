@@ -10,13 +10,34 @@
 // into shared memory by bulk asynchronous copies (one producer thread, S-stage mbarrier
 // ring) and consumed by row groups whose threads own fixed 16-byte column vectors, so
 // every global access is a 16-byte coalesced vector and the weight stays in registers.
+//
+// Split-phase rows: phase A of row j reads the row, forms each warp's partial sum of
+// squares and arrives on the row's reduction mbarrier; phase B of row j-1 then waits on
+// that barrier (normally long complete), re-reads row j-1 from shared memory, and writes
+// y.  No warp ever blocks on the row it is still reducing, and the staged stage is
+// released per warp once phase B has read it.
+//
 // Precision: the sum of squares is accumulated in FP32 (BF16 squares are exact in FP32,
 // so only the additions round); the reciprocal square root is the correctly rounded
-// __frsqrt_rn, which keeps rstd within 1e-6 relative of the FP64 value.
+// __frsqrt_rn, which keeps rstd within 1e-6 relative of the FP64 value.  Arithmetic runs
+// on packed FP32 pairs (f32x2).
 #include "rmsn_common.cuh"
 #include "rmsn_launch.h"
 
 namespace rmsn {
+
+// h = BF16(x_in + residual) for one 16-byte vector.  The FP32 sum of two BF16 values is
+// exact unless their exponents differ by more than 16, and then the smaller one is far
+// below half a BF16 ulp of the larger: either way the rounding gives BF16_RNE of the
+// exact sum.
+__device__ __forceinline__ uint4 residual_sum8(const uint4& u, const uint4& q) {
+  uint4 r;
+  r.x = f2_to_bf2(f2_add(bf2_to_f2(u.x), bf2_to_f2(q.x)));
+  r.y = f2_to_bf2(f2_add(bf2_to_f2(u.y), bf2_to_f2(q.y)));
+  r.z = f2_to_bf2(f2_add(bf2_to_f2(u.z), bf2_to_f2(q.z)));
+  r.w = f2_to_bf2(f2_add(bf2_to_f2(u.w), bf2_to_f2(q.w)));
+  return r;
+}
 
 // At most 256 consumers (G*NTg) + the producer warp; two CTAs an SM.
 template <int VPT, bool kFp32W, bool kRes>
@@ -26,13 +47,16 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   const int H = a.map.H;
   const int NV = H >> 3;
   const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
+  const SmemLayout L = smem_layout(S, NT, G, H);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * stage_elems * 2);
-  uint64_t* empty = full + S;
-  float* red = reinterpret_cast<float*>(empty + S);  // [2][G][32]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * G * 32);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kRedBufs][G]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kRedBufs][G][32]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
 
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
@@ -44,8 +68,9 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(G));
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NW));  // one arrival per warp
     }
+    for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -84,6 +109,7 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
+  const int wg = lt >> 5, lane = lt & 31;
   f2 wv[VPT][4];
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
@@ -91,74 +117,72 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
     if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
   }
   const float hf = static_cast<float>(H);  // exact for H < 2^24
+  const int32_t ng = (r1 - r0 > g) ? (r1 - r0 - g + G - 1) / G : 0;  // rows of this group
 
-  for (int32_t j = 0; j < nstage; ++j) {
-    const int32_t row = r0 + j * G + g;
-    if (row >= r1) break;
-    const int s = j % S;
-    mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                      kErrConsumerWait);
-    const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
-    const size_t out_row = static_cast<size_t>(row) * H;
-
-    uint4 hv[VPT];
-    f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);  // two chains, fixed combine order
+  for (int32_t j = 0; j <= ng; ++j) {
+    // ---- phase A, row j: sum of squares (and h in the residual form) ----
+    if (j < ng) {
+      const int32_t row = r0 + j * G + g;
+      const int s = j % S;
+      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                        kErrConsumerWait);
+      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);  // two chains, fixed combine order
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = lt + v * NTg;
-      if (c < NV) {
-        uint4 u = lds128(xs + c * 8);
-        if constexpr (kRes) {
-          // The FP32 sum of two BF16 values is exact unless their exponents differ by
-          // more than 16, and then the smaller one is far below half a BF16 ulp of the
-          // larger: either way the rounding below gives BF16_RNE of the exact sum.
-          const uint4 q = lds128(xs + static_cast<size_t>(G) * H + c * 8);
-          u.x = f2_to_bf2(f2_add(bf2_to_f2(u.x), bf2_to_f2(q.x)));
-          u.y = f2_to_bf2(f2_add(bf2_to_f2(u.y), bf2_to_f2(q.y)));
-          u.z = f2_to_bf2(f2_add(bf2_to_f2(u.z), bf2_to_f2(q.z)));
-          u.w = f2_to_bf2(f2_add(bf2_to_f2(u.w), bf2_to_f2(q.w)));
-          stg128(a.h + out_row + c * 8, u);
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          uint4 u = lds128(xs + c * 8);
+          if constexpr (kRes) {
+            u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
+            stg128(a.h + static_cast<size_t>(row) * H + c * 8, u);
+          }
+          const f2 e0 = bf2_to_f2(u.x), e1 = bf2_to_f2(u.y);
+          const f2 e2 = bf2_to_f2(u.z), e3 = bf2_to_f2(u.w);
+          ss0 = f2_fma(e0, e0, ss0);
+          ss1 = f2_fma(e1, e1, ss1);
+          ss0 = f2_fma(e2, e2, ss0);
+          ss1 = f2_fma(e3, e3, ss1);
         }
-        hv[v] = u;
-        const f2 e0 = bf2_to_f2(u.x), e1 = bf2_to_f2(u.y);
-        const f2 e2 = bf2_to_f2(u.z), e3 = bf2_to_f2(u.w);
-        ss0 = f2_fma(e0, e0, ss0);
-        ss1 = f2_fma(e1, e1, ss1);
-        ss0 = f2_fma(e2, e2, ss0);
-        ss1 = f2_fma(e3, e3, ss1);
-      } else {
-        hv[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const f2 sp = f2_add(ss0, ss1);
+      const float ss = warp_allsum(f2_lo(sp) + f2_hi(sp));
+      if (lane == 0) {
+        slots[((j % kRedBufs) * G + g) * 32 + wg] = ss;
+        mbar_arrive(&redb[(j % kRedBufs) * G + g]);
       }
     }
-    const f2 sp = f2_add(ss0, ss1);
-    float ss = warp_allsum(f2_lo(sp) + f2_hi(sp));
-    if (NTg > 32) {
-      float* slot = red + ((j & 1) * G + g) * 32;
-      if ((lt & 31) == 0) slot[lt >> 5] = ss;
-      named_bar_sync(1 + g, NTg);
-      ss = 0.f;
-      for (int i = 0; i < (NTg >> 5); ++i) ss += slot[i];  // fixed order
-    } else {
-      __syncwarp();
-    }
-    // every thread of the group has read its vectors of this stage: release the slot
-    if (lt == 0) mbar_arrive(&empty[s]);
-
-    const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
-    const f2 rs2 = f2_splat(rs);
+    // ---- phase B, row j-1: rstd, y ----
+    if (j >= 1) {
+      const int32_t jj = j - 1;
+      const int32_t row = r0 + jj * G + g;
+      const int s = jj % S;
+      const int rb = (jj % kRedBufs) * G + g;
+      mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag,
+                        a.err, kErrConsumerWait);
+      const float ss = slot_sum(slots + rb * 32, NW);
+      const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
+      const f2 rs2 = f2_splat(rs);
+      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      const size_t out_row = static_cast<size_t>(row) * H;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      const int c = lt + v * NTg;
-      if (c < NV) {
-        uint4 o;
-        o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].x), rs2), wv[v][0]));
-        o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].y), rs2), wv[v][1]));
-        o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].z), rs2), wv[v][2]));
-        o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].w), rs2), wv[v][3]));
-        stg128(a.y + out_row + c * 8, o);
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          uint4 u = lds128(xs + c * 8);
+          if constexpr (kRes) u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
+          uint4 o;
+          o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.x), rs2), wv[v][0]));
+          o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.y), rs2), wv[v][1]));
+          o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.z), rs2), wv[v][2]));
+          o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.w), rs2), wv[v][3]));
+          stg128(a.y + out_row + c * 8, o);
+        }
       }
+      if (lt == 0) a.rstd[row] = rs;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
     }
-    if (lt == 0) a.rstd[row] = rs;
   }
 }
 

@@ -14,6 +14,41 @@ constexpr int kMaxThreads = kMaxConsumerThreads + kProducerThreads;
 constexpr int kFinishCols = 32;            // dw columns per finishing CTA
 constexpr int kFinishSlices = 8;           // partition slices per finishing CTA
 
+// Shared-memory carve-up of a row kernel (byte offsets), used by the kernels and by the
+// host's size computation alike.
+//   ring   [stages][tensors][groups][H] BF16 staged rows
+//   full, empty   [stages] mbarriers (staged bytes landed / stage released)
+//   redb   [kRedBufs][groups] mbarriers: a row's per-warp reduction partials are written
+//   slots  [kRedBufs][groups][32] FP32 per-warp reduction partials
+//   abort  CTA abort flag of the bounded waits
+//
+// Row j's reduction uses buffer j % kRedBufs.  A warp writes buffer j in phase A(j) after
+// finishing B(j-2), which needed every warp's A(j-2), which each warp issues after its
+// own B(j-4): so every reader of buffer j-4 is done, and four buffers never race.  The
+// same ordering keeps each redb barrier within one phase of its waiters.
+constexpr int kRedBufs = 4;
+struct SmemLayout {
+  size_t full, empty, redb, slots, abort_flag, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int groups, int H) {
+  SmemLayout L;
+  size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
+  L.full = off;
+  off += 8 * static_cast<size_t>(stages);
+  L.empty = off;
+  off += 8 * static_cast<size_t>(stages);
+  L.redb = off;
+  off += 8 * kRedBufs * static_cast<size_t>(groups);
+  off = (off + 127) & ~static_cast<size_t>(127);
+  L.slots = off;
+  off += 4 * kRedBufs * 32 * static_cast<size_t>(groups);
+  L.abort_flag = off;
+  off += 16;
+  L.total = off;
+  return L;
+}
+
 // Launch shape of a row kernel, a function of H (and of the mode for P).
 struct Shape {
   int vpt;       // 16-byte column vectors per consumer thread (1 or 2)
@@ -23,6 +58,7 @@ struct Shape {
   int tensors;   // BF16 tensors staged per row
   int threads;   // groups * ntg + producer warp
   size_t smem;   // dynamic shared memory bytes
+  bool wide;     // more than 288 threads: built for one CTA an SM
 };
 
 struct RowMapArgs {
@@ -73,8 +109,11 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaSt
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
 // CTAs per SM the backward row kernel is built to keep resident (its launch bounds'
-// minimum), a compile-time property: 2 for one-vector threads, else 1.
-constexpr int bwd_design_blocks_per_sm(int vpt) { return vpt == 1 ? 2 : 1; }
+// minimum), a compile-time property of the shape class: 2 for CTAs of at most 288
+// threads with 1 or 2 vectors a thread, else 1.
+constexpr int bwd_design_blocks_per_sm(int vpt, bool wide) {
+  return (vpt <= 2 && !wide) ? 2 : 1;
+}
 
 // Resident CTAs per SM of the chosen row kernel (cached per device).
 int fwd_blocks_per_sm(const Shape& s, bool fp32w);

@@ -4,8 +4,12 @@ case, run the FP64 oracle on the same bytes, and compare under the gates.
 Gates (the op's stated accuracy, flashinfer PR #8827 description and Measurement; the
 1-ulp and 1e-6 bounds are this build's tighter targets):
   y, dx   within 1 BF16 ulp of the FP64 result rounded to BF16 (ordinal distance <= 1);
-          dx may also sit within the FP32 evaluation error of its two cancelling terms,
-          2^-20 * r * (|g_j| + |xhat_j * c|), where g - xhat*c nearly cancels
+          where g - xhat*c nearly cancels, dx may instead sit within the FP32 error of
+          computing it, E_j = r*(2^-20*(|g_j| + |xhat_j*c|) + 2^-18*|xhat_j|*S) with
+          S = mean_k |g_k*xhat_k| (the first term: the few roundings of g, xhat, the fma
+          and the scaling; the second: the FP32 row reduction that forms c, whose error
+          scales with the sum of |terms|), plus 2^-23*|dh_j| when dh is added and half a
+          BF16 ulp for the final rounding
   rstd    |rstd - rstd64| <= 1e-6 * rstd64
   h       bit-exact (one rounding of an exact sum)
   dw      |dw - dw64| <= 1e-4 + 1e-4 * |dw64| for every element
@@ -106,23 +110,31 @@ def check_rstd(rstd_gpu: np.ndarray, rstd64: np.ndarray):
 
 
 def check_bf16_1ulp(gpu_bits: np.ndarray, ref64: np.ndarray, what: str, extra_ok=None):
+    """Ordinal distance <= 1 from BF16_RNE(ref64); elements beyond it pass only if
+    |gpu - ref64| <= extra_ok + half a BF16 ulp of the GPU value.  Returns the largest
+    ordinal distance, the count that needed the second clause, and their worst ratio of
+    error to allowance."""
     ref_bits = oracle.round_bf16(ref64)
     d = np.abs(ordinal(gpu_bits.reshape(-1)) - ordinal(ref_bits.reshape(-1)))
     bad = d > 1
     n_extra = 0
+    worst = 0.0
     if extra_ok is not None and bad.any():
         gv = oracle.bf16_to_f64(gpu_bits.reshape(-1))
-        ok2 = np.abs(gv - ref64.reshape(-1)) <= extra_ok.reshape(-1)
+        err = np.abs(gv - ref64.reshape(-1))
+        allow = extra_ok.reshape(-1) + np.abs(gv) * 2.0**-8
+        ok2 = err <= allow
         n_extra = int((bad & ok2).sum())
+        worst = float((err[bad] / allow[bad]).max())
         bad = bad & ~ok2
     assert not bad.any(), (
-        f"{what}: {int(bad.sum())} elements beyond 1 BF16 ulp "
-        f"(max ordinal distance {int(d.max())})")
-    return int(d.max()) if d.size else 0, n_extra
+        f"{what}: {int(bad.sum())} elements beyond 1 BF16 ulp and the FP32 cancellation "
+        f"allowance (max ordinal distance {int(d.max())}, worst err/allowance {worst:.3f})")
+    return int(d.max()) if d.size else 0, n_extra, worst
 
 
-def dx_cancel_tol(x_bits, dy_bits, w, r, H):
-    """2^-20 * r * (|g| + |xhat*c|) per element: the FP32 evaluation error of g - xhat*c."""
+def dx_cancel_tol(x_bits, dy_bits, w, r, H, dh_bits=None):
+    """E_j of the module docstring: the FP32 error of evaluating dx_j, per element."""
     xv = oracle.bf16_to_f64(x_bits).reshape(-1, H)
     dyv = oracle.bf16_to_f64(dy_bits).reshape(-1, H)
     wv = oracle.bf16_to_f64(w) if w.dtype == np.uint16 else w.astype(np.float64)
@@ -130,7 +142,11 @@ def dx_cancel_tol(x_bits, dy_bits, w, r, H):
     xh = xv * rr
     g = dyv * wv
     c = (g * xh).mean(axis=1, keepdims=True)
-    return 2.0**-20 * rr * (np.abs(g) + np.abs(xh * c))
+    S = np.abs(g * xh).mean(axis=1, keepdims=True)
+    E = rr * (2.0**-20 * (np.abs(g) + np.abs(xh * c)) + 2.0**-18 * np.abs(xh) * S)
+    if dh_bits is not None:
+        E = E + 2.0**-23 * np.abs(oracle.bf16_to_f64(dh_bits).reshape(-1, H))
+    return E
 
 
 def check_dw(dw_gpu: np.ndarray, dw64: np.ndarray):
@@ -179,7 +195,7 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
     y64, _, h_bits = oracle.fwd(c.x, c.w, c.eps, c.T, c.nh, H, c.s_tok, c.s_head,
                                 residual=c.residual, rows=rows)
     yb = bits_of(y).reshape(R, H)
-    out["y_ulp"], _ = check_bf16_1ulp(yb if rows is None else yb[rows], y64, "y")
+    out["y_ulp"], _, _ = check_bf16_1ulp(yb if rows is None else yb[rows], y64, "y")
     if residual:
         hb = bits_of(h).reshape(R, H)
         assert np.array_equal(hb, h_all.reshape(R, H)), "h not bit-exact"
@@ -201,18 +217,21 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
                          dh=c.dh if with_dh else None, rows=rows)
     sel = np.arange(R) if rows is None else rows
     xrows = gather_rows(xs_bits, c, sel) if not residual else xs_bits.reshape(R, H)[sel]
-    tol = dx_cancel_tol(xrows, c.dy.reshape(R, H)[sel], c.w, r_in[sel], H)
+    tol = dx_cancel_tol(xrows, c.dy.reshape(R, H)[sel], c.w, r_in[sel], H,
+                        dh_bits=c.dh.reshape(R, H)[sel] if with_dh else None)
     dws = {}
     for det in modes:
         dx, dw = gpu_bwd(dc, xs_dev, s_tok, s_head, r_dev, det, with_dh=with_dh)
         torch.cuda.synchronize()
         dxb = bits_of(dx).reshape(R, H)
-        ulp, n_extra = check_bf16_1ulp(dxb[sel], dx64, f"dx (det={det})", extra_ok=tol)
+        ulp, n_extra, worst = check_bf16_1ulp(dxb[sel], dx64, f"dx (det={det})",
+                                              extra_ok=tol)
         ratio = check_dw(dw.cpu().numpy(), dw64)
         dws[det] = (dxb, dw.cpu().numpy())
         key = "det" if det else "nondet"
         out[f"dx_ulp_{key}"] = ulp
         out[f"dx_cancel_{key}"] = n_extra
+        out[f"dx_cancel_worst_{key}"] = worst
         out[f"dw_ratio_{key}"] = ratio
     if len(dws) == 2:
         # the two modes share the row pass: dx is bit-identical

@@ -117,9 +117,11 @@ def test_bwd_rejects_before_any_cuda_call(lib, kw, want):
 
 def test_deterministic_workspace_size_depends_on_shape_only(lib):
     f = lib.rmsnorm_train_bwd_workspace_bytes
-    # H = 4096: one row group of 2-vector threads, one CTA an SM -> at most 152 partials
+    # H = 4096: one row group of 2-vector threads, two CTAs an SM -> at most 304 partials
     # of 2*H floats; a CTA takes at least 4 stages (4 rows)
-    assert f(65536, 1, 4096, 1) == 152 * 2 * 4096 * 4
+    assert f(65536, 1, 4096, 1) == 304 * 2 * 4096 * 4
+    # H = 6144: 384 consumers, one CTA an SM -> at most 152
+    assert f(65536, 1, 6144, 1) == 152 * 2 * 6144 * 4
     assert f(1, 1, 4096, 1) == 1 * 2 * 4096 * 4
     assert f(65, 1, 4096, 1) == 17 * 2 * 4096 * 4
     # H = 256: 8 one-warp row groups (8 rows a stage), two CTAs an SM -> at most 304
