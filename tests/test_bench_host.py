@@ -1,0 +1,104 @@
+"""bench.py's host logic without a GPU: the byte model, the peak lookup, the traffic gate
+on the kernel-source hash, the clock-sample summary, the reference arm's JSON line, and
+the max-over-ranks timing reduction across two gloo ranks (the replicas' only
+collective, host-side)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_byte_model():
+    R, H = 65536, 4096
+    assert bench.fwd_bytes(R, H, 2) == 4 * R * H + 4 * R + 2 * H
+    assert bench.bwd_bytes(R, H, 4) == 6 * R * H + 4 * R + 4 * H + 4 * H
+
+
+def test_peak_fallback_when_no_measured_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 7000.0}))
+    assert bench.measured_peak() == (7000.0, "measured")
+
+
+def test_traffic_needs_matching_source_hash(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_for("k") is None
+    f.write_text(json.dumps({"k": {"source_hash": "stale", "dram_bytes_per_op": 1.0}}))
+    assert bench.traffic_for("k") is None
+    f.write_text(json.dumps({"k": {"source_hash": bench.kernel_source_hash(),
+                                   "dram_bytes_per_op": 123.0}}))
+    assert bench.traffic_for("k") == 123.0
+
+
+def test_clock_summary_filters_window_and_reasons():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.lines = [
+        (10.0, "2026/01/01 00:00:00.000, 0, 1000, 2070, 500, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        (20.0, "2026/01/01 00:00:00.000, 0, 2070, 2070, 900, 0x4, Not Active, Not Active, Not Active, Active"),
+        (20.2, "2026/01/01 00:00:00.000, 0, 2040, 2070, 950, 0x0, Not Active, Not Active, Not Active, Not Active"),
+    ]
+    out = s.summary(19.0, 21.0)
+    assert out["samples"] == 2 and out["sm_mhz"] == 2055.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_reference_arm_line(capsys):
+    bench.main(["--impl", "reference", "--T", "64", "--H", "256", "--steps", "3",
+                "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["higher_is_better"] is True
+
+
+_WORKER = r"""
+import os, sys
+sys.path.insert(0, {root!r})
+import bench
+ws, rank, _ = bench.dist_env()
+dist = bench.dist_init(ws)
+bench.barrier(dist)
+t = bench.reduce_max(10.0 + rank, dist)
+print("RESULT", rank, t, flush=True)
+"""
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_max_over_two_gloo_ranks(tmp_path):
+    script = tmp_path / "w.py"
+    script.write_text(_WORKER.format(root=ROOT))
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, WORLD_SIZE="2", RANK=str(rank), LOCAL_RANK=str(rank),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, str(script)], env=env,
+                                      stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
+                                      text=True))
+    outs = []
+    for p in procs:
+        try:
+            out, _ = p.communicate(timeout=120)
+        except subprocess.TimeoutExpired:
+            p.kill()
+            pytest.fail("gloo rank did not finish")
+        outs.append(out)
+        assert p.returncode == 0, out
+    vals = sorted(float(l.split()[2]) for o in outs for l in o.splitlines()
+                  if l.startswith("RESULT"))
+    assert vals == [11.0, 11.0]
