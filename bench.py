@@ -492,6 +492,7 @@ SWEEP = [
     ("plain", 16384, 4096, 1, None, False, False),
     ("plain", 65536, 4096, 1, None, False, False),
     ("stress", 32768, 1536, 1, None, True, False),
+    ("stress", 65536, 1536, 1, None, True, False),
     ("stress", 131072, 1536, 1, None, True, False),
     ("stress", 32768, 2048, 1, None, True, False),
     ("stress", 131072, 2048, 1, None, True, False),
@@ -500,6 +501,7 @@ SWEEP = [
     ("residual", 30720, 6144, 1, None, False, True),
     ("residual", 65536, 6144, 1, None, False, True),
     ("heads24of32", 4096, 256, 24, 32, True, False),
+    ("heads24of32", 16384, 256, 24, 32, True, False),
     ("heads24of32", 65536, 256, 24, 32, True, False),
     ("heads4", 65536, 256, 4, None, True, False),
 ]
@@ -539,6 +541,8 @@ def run_sweep(args):
         return statistics.median(out)
 
     for label, T, H, nh, bh, w32, res in SWEEP:
+        if args.sweep_filter and args.sweep_filter != f"{label}_{T}_{H}":
+            continue
         c = synth.make_case(0, T, H, nh=nh, buf_heads=bh, w_fp32=w32, residual=res, dh=res)
         R = c.R
         wbytes = 4 if w32 else 2
@@ -607,6 +611,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="time each op on every workload family (one line each) instead")
     ap.add_argument("--sweep-reps", type=int, default=30)
+    ap.add_argument("--sweep-filter", default="",
+                    help="only the sweep entry LABEL_T_H (e.g. stress_131072_1536)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -19,8 +19,11 @@ __device__ unsigned g_err_word = 0u;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kRingTarget = 96 * 1024;  // shared-memory ring bytes per CTA (target)
-constexpr int kMaxStages = 8;
+// Shared-memory ring bytes per CTA (target): kernels built for two CTAs an SM take 96 KB
+// each; "wide" kernels, one CTA an SM, take twice that.
+constexpr size_t kRingTarget = 96 * 1024;
+constexpr size_t kRingTargetWide = 192 * 1024;
+constexpr int kMaxStages = 12;
 // Deterministic backward: at most kDetSMs x (the CTAs an SM the kernel is built to keep
 // resident) dw partials -- a function of the shape only, so the same on every device
 // whatever its SM count.  152 is GB300's SM count: there the partition is one wave.
@@ -41,7 +44,7 @@ uint64_t key(int dev, const void* fn, uint64_t extra) {
 }
 
 size_t shared_bytes(const Shape& s, int H) {
-  return smem_layout(s.stages, s.tensors, s.groups, H).total;
+  return smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0).total;
 }
 
 // Column vectors per thread, from the instantiated set `allowed` (descending): the
@@ -60,15 +63,22 @@ Shape make_shape(int H, int tensors, int vpt) {
   const int nv = H / 8;
   s.vpt = vpt;
   const int per = (nv + s.vpt - 1) / s.vpt;
-  s.ntg = ((per + 31) / 32) * 32;
+  if (per <= 8) {
+    s.ntg = 8;  // sub-warp groups: four rows a warp
+  } else if (per <= 16) {
+    s.ntg = 16;  // two rows a warp
+  } else {
+    s.ntg = ((per + 31) / 32) * 32;
+  }
   s.groups = s.ntg >= 256 ? 1 : 256 / s.ntg;
-  if (s.groups > 8) s.groups = 8;
+  // groups that reduce through shared memory use named barriers 1..8
+  if (s.ntg >= 32 && s.groups > 8) s.groups = 8;
   s.tensors = tensors;
-  const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
-  int st = static_cast<int>(kRingTarget / stage_bytes);
-  s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
   s.threads = s.groups * s.ntg + kProducerThreads;
   s.wide = s.threads > 288 || s.vpt == 4;
+  const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
+  int st = static_cast<int>((s.wide ? kRingTargetWide : kRingTarget) / stage_bytes);
+  s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
   s.smem = shared_bytes(s, H);
   return s;
 }
@@ -136,11 +146,15 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
 // spread over many elements.  Backward: 2 vectors a thread up to H = 6144 (registers
 // hold x_hat, g, w and the dw sum/compensation of 16 columns), 4 above.
 Shape fwd_shape(int H, bool residual) {
-  return make_shape(H, residual ? 2 : 1, pick_vpt(H / 8, {4, 3, 2, 1}));
+  const int nv = H / 8;
+  // narrow rows: 4 vectors a lane in 8- or 16-lane groups
+  const int vpt = nv <= 64 ? (nv >= 4 ? 4 : 1) : pick_vpt(nv, {4, 3, 2, 1});
+  return make_shape(H, residual ? 2 : 1, vpt);
 }
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
-  const int vpt = nv <= 32 ? 1 : (nv <= 768 ? 2 : 4);
+  // narrow rows: 2 vectors a lane in 8- or 16-lane groups
+  const int vpt = nv <= 768 ? (nv >= 2 ? 2 : 1) : 4;
   return make_shape(H, with_dh ? 3 : 2, vpt);
 }
 

@@ -38,7 +38,7 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
 }
 
 // Launch bounds per shape class: up to 256 consumers + the producer warp, two CTAs an
-// SM (VPT 1 or 2, H <= 4096); "wide" VPT=2 rows of H 4104..6144 with up to 384 consumers,
+// SM (VPT 1 or 2, H <= 4096; narrow rows in 8- or 16-lane sub-warp groups); "wide" VPT=2 rows of H 4104..6144 with up to 384 consumers,
 // one CTA an SM; VPT=4 (H up to 8192) with 256 consumers, one CTA an SM.
 template <int VPT, bool kWide>
 constexpr int bwd_max_threads() { return (kWide && VPT == 2) ? 416 : 288; }
@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
   const int G = a.groups, NTg = a.ntg, S = a.stages;
   const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
-  const SmemLayout L = smem_layout(S, NT, G, H);
+  const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
+  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -74,9 +75,10 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(G * NW));  // one arrival per warp
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
     }
-    for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
+    if (red_smem)
+      for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
   // the dw contributions.  Registers hold only w and the dw state across rows.
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
-  const int wg = lt >> 5, lane = lt & 31;
+  const int wg = lt >> 5, lane = tid & 31;
   f2 wv[VPT][4];
   f2 acc[VPT][4], cmp[VPT][4];
 #pragma unroll
@@ -131,41 +133,53 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
     }
   }
   const float inv_h = 1.0f / static_cast<float>(H);
-  const int32_t ng = (r1 - r0 > g) ? (r1 - r0 - g + G - 1) / G : 0;  // rows of this group
+  // Rows of this warp's first group: every lane of a warp runs the same iterations (the
+  // shuffles need them all); groups past the chunk's end skip the row work.
+  const int g0 = red_smem ? g : (tid & ~31) / NTg;
+  const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
-  float rs_prev = 0.f;  // rstd of row j-1 (loaded during phase A of row j-1)
+  float rs_prev = 0.f;   // rstd of row j-1 (loaded during phase A of row j-1)
+  float dot_carry = 0.f; // sub-warp groups: row j-1's sum of (dy*w)*x
   for (int32_t j = 0; j <= ng; ++j) {
-    float rs_new = 0.f;
+    float rs_new = 0.f, dot_new = 0.f;
     // ---- phase A, row j: partial of sum (dy*w)*x ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
-      rs_new = __ldg(a.rstd + row);  // consumed one iteration later
+      const bool valid = row < r1;
+      if (valid) rs_new = __ldg(a.rstd + row);  // consumed one iteration later
       const int s = j % S;
       mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
                         kErrConsumerWait);
       const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
       f2 dot0 = f2_splat(0.f), dot1 = f2_splat(0.f);
+      if (valid) {
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = lt + v * NTg;
-        if (c < NV) {
-          const uint4 xv = lds128(st + c * 8);
-          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            const uint4 xv = lds128(st + c * 8);
+            const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wv[v][q]);
-            if (q & 1)
-              dot1 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot1);
-            else
-              dot0 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot0);
+            for (int q = 0; q < 4; ++q) {
+              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wv[v][q]);
+              if (q & 1)
+                dot1 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot1);
+              else
+                dot0 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot0);
+            }
           }
         }
       }
       const f2 dsum = f2_add(dot0, dot1);
-      const float dot = warp_allsum(f2_lo(dsum) + f2_hi(dsum));
-      if (lane == 0) {
-        slots[((j % kRedBufs) * G + g) * 32 + wg] = dot;
-        mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+      const float part = f2_lo(dsum) + f2_hi(dsum);
+      if (red_smem) {
+        const float dot = warp_allsum(part);
+        if (lane == 0) {
+          slots[((j % kRedBufs) * G + g) * 32 + wg] = dot;
+          mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+        }
+      } else {
+        dot_new = subwarp_allsum(part, NTg);
       }
     }
     // ---- phase B, row j-1: dx and the dw contributions ----
@@ -173,53 +187,61 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
       const int32_t jj = j - 1;
       const int32_t row = r0 + jj * G + g;
       const int s = jj % S;
-      const int rb = (jj % kRedBufs) * G + g;
-      const float rs = rs_prev;
-      // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
-      // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
-      // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
-      const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
-      const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi), rl2 = f2_splat(__fsub_rn(rs, rs_hi));
-      mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag,
-                        a.err, kErrConsumerWait);
-      // c = (1/H) sum g*xhat = (rstd/H) sum (dy*w)*x
-      const f2 nc2 = f2_splat(-(slot_sum(slots + rb * 32, NW) * (rs * inv_h)));
-      const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
-      const size_t out_row = static_cast<size_t>(row) * H;
+      float dot = dot_carry;
+      if (red_smem) {
+        const int rb = (jj % kRedBufs) * G + g;
+        mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag,
+                          a.err, kErrConsumerWait);
+        dot = slot_sum(slots + rb * 32, NW);
+      }
+      if (row < r1) {
+        const float rs = rs_prev;
+        // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
+        // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
+        // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
+        const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
+        const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi);
+        const f2 rl2 = f2_splat(__fsub_rn(rs, rs_hi));
+        // c = (1/H) sum g*xhat = (rstd/H) sum (dy*w)*x
+        const f2 nc2 = f2_splat(-(dot * (rs * inv_h)));
+        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+        const size_t out_row = static_cast<size_t>(row) * H;
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = lt + v * NTg;
-        if (c < NV) {
-          const uint4 xv = lds128(st + c * 8);
-          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
-          uint4 hv = make_uint4(0u, 0u, 0u, 0u);
-          if constexpr (kDh) hv = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
-          uint32_t o[4];
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            const uint4 xv = lds128(st + c * 8);
+            const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+            uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (kDh) hv = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+            uint32_t o[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const f2 x2 = bf2_to_f2(u4_get(xv, q));
-            const f2 d2 = bf2_to_f2(u4_get(dv, q));
-            const f2 xh = f2_mul(x2, rs2);
-            const f2 gw = f2_mul(d2, wv[v][q]);
-            f2 d = f2_mul(f2_fma(xh, nc2, gw), rs2);  // (g - xhat*c) * rstd
-            if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
-            o[q] = f2_to_bf2(d);
-            // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
-            // compensation term, which also collects dy*x*rs_lo
-            const f2 dyx = f2_mul(d2, x2);
-            const f2 p = f2_mul(dyx, rh2);
-            const f2 t = f2_add(acc[v][q], p);
-            const f2 e = f2_add(f2_sub(acc[v][q], t), p);
-            cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
-            acc[v][q] = t;
+            for (int q = 0; q < 4; ++q) {
+              const f2 x2 = bf2_to_f2(u4_get(xv, q));
+              const f2 d2 = bf2_to_f2(u4_get(dv, q));
+              const f2 xh = f2_mul(x2, rs2);
+              const f2 gw = f2_mul(d2, wv[v][q]);
+              f2 d = f2_mul(f2_fma(xh, nc2, gw), rs2);  // (g - xhat*c) * rstd
+              if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
+              o[q] = f2_to_bf2(d);
+              // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
+              // compensation term, which also collects dy*x*rs_lo
+              const f2 dyx = f2_mul(d2, x2);
+              const f2 p = f2_mul(dyx, rh2);
+              const f2 t = f2_add(acc[v][q], p);
+              const f2 e = f2_add(f2_sub(acc[v][q], t), p);
+              cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
+              acc[v][q] = t;
+            }
+            stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
           }
-          stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
     }
     rs_prev = rs_new;
+    dot_carry = dot_new;
   }
 
   // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----

@@ -49,14 +49,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// One attempt to wait for phase `parity` of `bar`.  The thread is suspended until the
+// phase completes or a suspend-time hint of ~10 ms runs out, so waiting threads do not
+// spin and steal issue slots from the working warps of their SM sub-partition.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(10000000u)
       : "memory");
   return ok != 0;
 }
@@ -69,11 +72,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   volatile int* abort_flag,
                                                   unsigned* err_word, unsigned errbit) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
     if (*abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > kWaitLimitNs) {
       atomicOr(err_word, errbit);
       *abort_flag = 1;
       return false;
@@ -252,6 +255,13 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& u, int q) {
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over an aligned group of `ntg` lanes (ntg = 8 or 16) by butterfly; every lane of
+// the group gets the same bits.
+__device__ __forceinline__ float subwarp_allsum(float v, int ntg) {
+  for (int o = ntg >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 

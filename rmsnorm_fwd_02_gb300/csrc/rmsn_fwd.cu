@@ -39,7 +39,8 @@ __device__ __forceinline__ uint4 residual_sum8(const uint4& u, const uint4& q) {
   return r;
 }
 
-// At most 256 consumers (G*NTg) + the producer warp; two CTAs an SM.
+// At most 256 consumers (G*NTg) + the producer warp; two CTAs an SM.  Narrow rows use
+// sub-warp groups of 8 or 16 lanes (several rows a warp, reduced by shuffles alone).
 template <int VPT, bool kFp32W, bool kRes>
 __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -49,7 +50,8 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   const int G = a.groups, NTg = a.ntg, S = a.stages;
   const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
-  const SmemLayout L = smem_layout(S, NT, G, H);
+  const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
+  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -68,9 +70,10 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(G * NW));  // one arrival per warp
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
     }
-    for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
+    if (red_smem)
+      for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
-  const int wg = lt >> 5, lane = lt & 31;
+  const int wg = lt >> 5, lane = tid & 31;
   f2 wv[VPT][4];
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
@@ -117,9 +120,14 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
     if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
   }
   const float hf = static_cast<float>(H);  // exact for H < 2^24
-  const int32_t ng = (r1 - r0 > g) ? (r1 - r0 - g + G - 1) / G : 0;  // rows of this group
+  // Rows of this warp's first group: every lane of a warp runs the same iterations (the
+  // shuffles need them all); groups past the chunk's end skip the row work.
+  const int g0 = red_smem ? g : (tid & ~31) / NTg;
+  const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
+  float ss_carry = 0.f;  // sub-warp groups: row j-1's sum of squares
   for (int32_t j = 0; j <= ng; ++j) {
+    float ss_new = 0.f;
     // ---- phase A, row j: sum of squares (and h in the residual form) ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
@@ -128,28 +136,35 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
                         kErrConsumerWait);
       const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
       f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);  // two chains, fixed combine order
+      if (row < r1) {
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = lt + v * NTg;
-        if (c < NV) {
-          uint4 u = lds128(xs + c * 8);
-          if constexpr (kRes) {
-            u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
-            stg128(a.h + static_cast<size_t>(row) * H + c * 8, u);
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            uint4 u = lds128(xs + c * 8);
+            if constexpr (kRes) {
+              u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
+              stg128(a.h + static_cast<size_t>(row) * H + c * 8, u);
+            }
+            const f2 e0 = bf2_to_f2(u.x), e1 = bf2_to_f2(u.y);
+            const f2 e2 = bf2_to_f2(u.z), e3 = bf2_to_f2(u.w);
+            ss0 = f2_fma(e0, e0, ss0);
+            ss1 = f2_fma(e1, e1, ss1);
+            ss0 = f2_fma(e2, e2, ss0);
+            ss1 = f2_fma(e3, e3, ss1);
           }
-          const f2 e0 = bf2_to_f2(u.x), e1 = bf2_to_f2(u.y);
-          const f2 e2 = bf2_to_f2(u.z), e3 = bf2_to_f2(u.w);
-          ss0 = f2_fma(e0, e0, ss0);
-          ss1 = f2_fma(e1, e1, ss1);
-          ss0 = f2_fma(e2, e2, ss0);
-          ss1 = f2_fma(e3, e3, ss1);
         }
       }
       const f2 sp = f2_add(ss0, ss1);
-      const float ss = warp_allsum(f2_lo(sp) + f2_hi(sp));
-      if (lane == 0) {
-        slots[((j % kRedBufs) * G + g) * 32 + wg] = ss;
-        mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+      const float part = f2_lo(sp) + f2_hi(sp);
+      if (red_smem) {
+        const float ss = warp_allsum(part);
+        if (lane == 0) {
+          slots[((j % kRedBufs) * G + g) * 32 + wg] = ss;
+          mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+        }
+      } else {
+        ss_new = subwarp_allsum(part, NTg);
       }
     }
     // ---- phase B, row j-1: rstd, y ----
@@ -157,32 +172,39 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
       const int32_t jj = j - 1;
       const int32_t row = r0 + jj * G + g;
       const int s = jj % S;
-      const int rb = (jj % kRedBufs) * G + g;
-      mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag,
-                        a.err, kErrConsumerWait);
-      const float ss = slot_sum(slots + rb * 32, NW);
-      const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
-      const f2 rs2 = f2_splat(rs);
-      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
-      const size_t out_row = static_cast<size_t>(row) * H;
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = lt + v * NTg;
-        if (c < NV) {
-          uint4 u = lds128(xs + c * 8);
-          if constexpr (kRes) u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
-          uint4 o;
-          o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.x), rs2), wv[v][0]));
-          o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.y), rs2), wv[v][1]));
-          o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.z), rs2), wv[v][2]));
-          o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.w), rs2), wv[v][3]));
-          stg128(a.y + out_row + c * 8, o);
-        }
+      float ss = ss_carry;
+      if (red_smem) {
+        const int rb = (jj % kRedBufs) * G + g;
+        mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag,
+                          a.err, kErrConsumerWait);
+        ss = slot_sum(slots + rb * 32, NW);
       }
-      if (lt == 0) a.rstd[row] = rs;
+      if (row < r1) {
+        const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
+        const f2 rs2 = f2_splat(rs);
+        const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+        const size_t out_row = static_cast<size_t>(row) * H;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            uint4 u = lds128(xs + c * 8);
+            if constexpr (kRes)
+              u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
+            uint4 o;
+            o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.x), rs2), wv[v][0]));
+            o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.y), rs2), wv[v][1]));
+            o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.z), rs2), wv[v][2]));
+            o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.w), rs2), wv[v][3]));
+            stg128(a.y + out_row + c * 8, o);
+          }
+        }
+        if (lt == 0) a.rstd[row] = rs;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
     }
+    ss_carry = ss_new;
   }
 }
 

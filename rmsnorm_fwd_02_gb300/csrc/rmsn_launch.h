@@ -31,7 +31,10 @@ struct SmemLayout {
   size_t full, empty, redb, slots, abort_flag, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int groups, int H) {
+// `red_groups` is the number of row groups that reduce through shared memory: all of them
+// when a group spans whole warps, none when groups are sub-warp (shuffles only).
+__host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int groups, int H,
+                                                  int red_groups) {
   SmemLayout L;
   size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
   L.full = off;
@@ -39,10 +42,10 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int g
   L.empty = off;
   off += 8 * static_cast<size_t>(stages);
   L.redb = off;
-  off += 8 * kRedBufs * static_cast<size_t>(groups);
+  off += 8 * kRedBufs * static_cast<size_t>(red_groups);
   off = (off + 127) & ~static_cast<size_t>(127);
   L.slots = off;
-  off += 4 * kRedBufs * 32 * static_cast<size_t>(groups);
+  off += 4 * kRedBufs * 32 * static_cast<size_t>(red_groups);
   L.abort_flag = off;
   off += 16;
   L.total = off;
@@ -52,7 +55,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int g
 // Launch shape of a row kernel, a function of H (and of the mode for P).
 struct Shape {
   int vpt;       // 16-byte column vectors per consumer thread (1 or 2)
-  int ntg;       // threads per row group (a multiple of 32)
+  int ntg;       // threads per row group: 8 or 16 (sub-warp) or a multiple of 32
   int groups;    // row groups per CTA = rows per stage
   int stages;    // depth of the shared-memory ring
   int tensors;   // BF16 tensors staged per row
