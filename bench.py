@@ -508,8 +508,10 @@ SWEEP = [
 
 
 def run_sweep(args):
-    """Times each op of each workload: `reps` launches, each after an L2 flush (a 512 MiB
-    memset outside the events), CUDA events on the launch stream, median."""
+    """Times each op of each workload: `reps` launches, each after an L2 flush outside the
+    events, CUDA events on the launch stream, median.  The flush READS a 512 MiB buffer,
+    so L2 is cold but clean: a write-based flush would leave dirty lines whose write-back
+    lands inside the next timed kernel."""
     import torch
     from rmsnorm_fwd_02_gb300 import _native as N
     from rmsnorm_fwd_02_gb300 import synth
@@ -519,7 +521,7 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     lib = N.lib()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peak()
 
     def dbf(bits):
@@ -530,7 +532,7 @@ def run_sweep(args):
         for _ in range(3):
             fn()
         for _ in range(reps):
-            flush.zero_()
+            flush.sum()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)

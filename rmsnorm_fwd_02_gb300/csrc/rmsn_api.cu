@@ -8,7 +8,7 @@
 #include <mutex>
 #include <unordered_map>
 
-#include "../../include/rmsnorm_train.h"
+#include "rmsnorm_train.h"  // include/ (on the include path)
 #include "rmsn_launch.h"
 
 namespace rmsn {
@@ -58,7 +58,7 @@ int pick_vpt(int nv, std::initializer_list<int> allowed) {
   return 1;
 }
 
-Shape make_shape(int H, int tensors, int vpt) {
+Shape make_shape(int H, int tensors, int vpt, bool bwd) {
   Shape s{};
   const int nv = H / 8;
   s.vpt = vpt;
@@ -75,7 +75,9 @@ Shape make_shape(int H, int tensors, int vpt) {
   if (s.ntg >= 32 && s.groups > 8) s.groups = 8;
   s.tensors = tensors;
   s.threads = s.groups * s.ntg + kProducerThreads;
-  s.wide = s.threads > 288 || s.vpt == 4;
+  // backward kernels past 288 threads or with 4-vector threads are built for one CTA an
+  // SM; every forward kernel is built for two
+  s.wide = bwd && (s.threads > 288 || s.vpt == 4);
   const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
   int st = static_cast<int>((s.wide ? kRingTargetWide : kRingTarget) / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
@@ -149,13 +151,13 @@ Shape fwd_shape(int H, bool residual) {
   const int nv = H / 8;
   // narrow rows: 4 vectors a lane in 8- or 16-lane groups
   const int vpt = nv <= 64 ? (nv >= 4 ? 4 : 1) : pick_vpt(nv, {4, 3, 2, 1});
-  return make_shape(H, residual ? 2 : 1, vpt);
+  return make_shape(H, residual ? 2 : 1, vpt, false);
 }
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
   // narrow rows: 2 vectors a lane in 8- or 16-lane groups
   const int vpt = nv <= 768 ? (nv >= 2 ? 2 : 1) : 4;
-  return make_shape(H, with_dh ? 3 : 2, vpt);
+  return make_shape(H, with_dh ? 3 : 2, vpt, true);
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem) {
