@@ -280,31 +280,43 @@ __device__ __forceinline__ float slot_sum(const float* slot, int nw) {
 
 // ---- row addressing and the producer -------------------------------------------------
 
+// Row r = (token t, head h) = (r / nh, r % nh) starts at element t*s_tok + h*s_head.
 struct RowMap {
   int32_t nh;
   int32_t H;
   int64_t s_tok;
   int64_t s_head;
-  __device__ __forceinline__ int64_t offset(int32_t r) const {
-    int32_t t = r / nh;
-    int32_t h = r - t * nh;
-    return static_cast<int64_t>(t) * s_tok + static_cast<int64_t>(h) * s_head;
-  }
 };
 
 // Copies rows [ra, rb) of a BF16 tensor into consecutive H-element slots at `dst`,
-// merging rows that are adjacent in memory into one bulk copy.
+// merging rows that are adjacent in memory into one bulk copy.  The (token, head) walk is
+// incremental: one division per call, none per row (a single producer thread issues
+// every copy of its CTA, so its per-row cost bounds the CTA's row rate).
 __device__ __forceinline__ void copy_rows(__nv_bfloat16* dst, const __nv_bfloat16* src,
                                           const RowMap& m, int32_t ra, int32_t rb,
                                           uint64_t* bar, uint64_t pol) {
+  int32_t t = ra / m.nh;
+  int32_t h = ra - t * m.nh;
+  int64_t off = static_cast<int64_t>(t) * m.s_tok + static_cast<int64_t>(h) * m.s_head;
   int32_t r = ra;
   while (r < rb) {
-    int64_t off = m.offset(r);
-    int32_t n = 1;
-    while (r + n < rb && m.offset(r + n) == off + static_cast<int64_t>(n) * m.H) ++n;
-    bulk_g2s(dst + static_cast<int64_t>(r - ra) * m.H, src + off,
+    const int64_t run_off = off;
+    int32_t n = 0;
+    int64_t next = off;
+    do {  // extend the run while the next row starts where this one ends
+      ++n;
+      if (++h == m.nh) {
+        h = 0;
+        ++t;
+        next = static_cast<int64_t>(t) * m.s_tok;
+      } else {
+        next += m.s_head;
+      }
+    } while (r + n < rb && next == run_off + static_cast<int64_t>(n) * m.H);
+    bulk_g2s(dst + static_cast<int64_t>(r - ra) * m.H, src + run_off,
              static_cast<uint32_t>(n) * static_cast<uint32_t>(m.H) * 2u, bar, pol);
     r += n;
+    off = next;
   }
 }
 
