@@ -31,7 +31,7 @@
  *    passed as void*; NULL = the legacy default stream) and is asynchronous.
  *  - Alignment: every tensor pointer 16-byte aligned; H a multiple of 8; s_tok and
  *    s_head multiples of 8 elements (each row is a 16-byte-aligned run).
- *  - Limits: 8 <= H <= 16384, T >= 0, nh >= 1, T*nh < 2^31.
+ *  - Limits: 8 <= H <= 8192, T >= 0, nh >= 1, T*nh < 2^31.
  *  - Outputs must not overlap inputs.
  *  - Errors: argument checks happen before anything is enqueued and return a nonzero
  *    status without touching memory; RMSN_ERR_CUDA reports a failed launch (the CUDA
@@ -49,10 +49,11 @@ extern "C" {
 
 #define RMSN_OK 0
 #define RMSN_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, stride or dtype */
-#define RMSN_ERR_UNSUPPORTED 2 /* H outside [8, 16384] or T*nh too large */
+#define RMSN_ERR_UNSUPPORTED 2 /* H above 8192 or T*nh too large */
 #define RMSN_ERR_WORKSPACE 3   /* workspace missing or smaller than required */
 #define RMSN_ERR_CUDA 4        /* a CUDA runtime call or launch failed */
 #define RMSN_ERR_DEVICE 5      /* current device is not compute capability 10.3 */
+#define RMSN_ERR_SCRATCH_LIMIT 6 /* rmsnorm_train_bwd_noalloc: shape exceeds its scratch */
 
 #define RMSN_W_BF16 0 /* w is BF16 [H] */
 #define RMSN_W_FP32 1 /* w is FP32 [H] */
@@ -108,6 +109,29 @@ int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float
                       void* workspace, size_t workspace_bytes,
                       int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head,
                       int deterministic, void* stream);
+
+/*
+ * Backward for callers that cannot allocate device memory where they call it -- e.g. a
+ * plugin's enqueue callback in a runtime that forbids allocation there, or a host with no
+ * device allocator to provide a workspace.  (The pages have no counterpart: this entry
+ * point exists for such callers only.)  Same arguments, results and modes as
+ * rmsnorm_train_bwd minus the workspace: the dw partials live in a 16 MiB array of device
+ * memory built into the library, which each device that loads the library holds until
+ * the process exits.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device looks up that array's device address (a runtime call,
+ *    no allocation); make that first call before capturing a stream into a graph.
+ *  - Every call on a device shares the array; calls that may overlap on the GPU (e.g. on
+ *    two unordered streams) race on it and must be serialized by the caller.  No initial
+ *    contents are needed.
+ *  - Returns RMSN_ERR_SCRATCH_LIMIT, with nothing enqueued, when the shape needs more than
+ *    16 MiB of partials (rmsnorm_train_bwd_workspace_bytes() > 16 MiB); every shape up to
+ *    H = 8192 fits on a 152-SM GB300 in both modes.
+ */
+int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, const float* rstd,
+                              const void* w, int w_dtype, void* dx, float* dw,
+                              int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head,
+                              int deterministic, void* stream);
 
 /* Static string naming a status code (never NULL). */
 const char* rmsnorm_train_status_str(int status);

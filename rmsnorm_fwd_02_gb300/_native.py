@@ -28,6 +28,8 @@ SIGNATURES = {
     "rmsnorm_train_bwd_workspace_bytes": (_size, [_i64, _i32, _i32, _int]),
     "rmsnorm_train_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _size, _i64,
                                  _i32, _i32, _i64, _i64, _int, _vp]),
+    "rmsnorm_train_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _i64, _i32,
+                                         _i32, _i64, _i64, _int, _vp]),
     "rmsnorm_train_status_str": (C.c_char_p, [_int]),
     "rmsnorm_train_device_error": (_int, [C.POINTER(C.c_uint), _int]),
 }
@@ -100,6 +102,15 @@ def rmsnorm_train_bwd(x, dy, dh, rstd, w, w_dtype, dx, dw, workspace, workspace_
                                  H, s_tok, s_head, int(deterministic), _stream(stream))
     if st != RMSN_OK:
         raise RmsnError("rmsnorm_train_bwd", st)
+
+
+def rmsnorm_train_bwd_noalloc(x, dy, dh, rstd, w, w_dtype, dx, dw, T, nh, H, s_tok, s_head,
+                              deterministic, stream=None):
+    st = lib().rmsnorm_train_bwd_noalloc(_ptr(x), _ptr(dy), _ptr(dh), _ptr(rstd), _ptr(w),
+                                         w_dtype, _ptr(dx), _ptr(dw), T, nh, H, s_tok, s_head,
+                                         int(deterministic), _stream(stream))
+    if st != RMSN_OK:
+        raise RmsnError("rmsnorm_train_bwd_noalloc", st)
 
 
 def rmsnorm_train_status_str(status):

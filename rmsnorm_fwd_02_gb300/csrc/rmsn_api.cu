@@ -225,6 +225,8 @@ const char* rmsnorm_train_status_str(int status) {
     case RMSN_ERR_WORKSPACE: return "workspace missing or too small";
     case RMSN_ERR_CUDA: return "CUDA runtime error";
     case RMSN_ERR_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case RMSN_ERR_SCRATCH_LIMIT:
+      return "shape needs more than the 16 MiB built-in scratch of rmsnorm_train_bwd_noalloc";
     default: return "unknown status";
   }
 }
@@ -367,3 +369,58 @@ int rmsnorm_train_device_error(unsigned int* flags, int reset) {
 }
 
 }  // extern "C"
+
+// ---- backward without caller-provided workspace ----------------------------------------
+//
+// Some callers cannot allocate device memory where they call the backward: a plugin's
+// enqueue callback inside an inference or training runtime that forbids allocation
+// there, or a host program with no device allocator of its own to hand out a workspace.
+// For them, rmsnorm_train_bwd_noalloc keeps the dw partials in the static array below,
+// which every device that loads this library holds until the process exits.  The array
+// needs no initial contents: every call writes each partial it later reads.  All calls
+// on a device share it, so two calls that overlap on the GPU (different streams, no
+// ordering between them) race on it.
+
+namespace rmsn {
+
+constexpr size_t kNoAllocScratchBytes = size_t{16} << 20;  // 16 MiB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+namespace {
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (current).  Host code must not use
+// the symbol itself as a pointer: on the host it names a stand-in, not device memory.
+int noalloc_scratch(int dev, float** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return RMSN_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return RMSN_OK;
+}
+}  // namespace
+
+}  // namespace rmsn
+
+extern "C" int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh,
+                                         const float* rstd, const void* w, int w_dtype,
+                                         void* dx, float* dw, int64_t T, int32_t nh,
+                                         int32_t H, int64_t s_tok, int64_t s_head,
+                                         int deterministic, void* stream) {
+  int st = check_view(T, nh, H, s_tok, s_head, w_dtype);
+  if (st != RMSN_OK) return st;
+  if (deterministic != 0 && deterministic != 1) return RMSN_ERR_INVALID_ARG;
+  int dev = 0;
+  if ((st = current_device(&dev)) != RMSN_OK) return st;
+  if ((st = device_setup(dev)) != RMSN_OK) return st;
+  const size_t need = rmsnorm_train_bwd_workspace_bytes(T, nh, H, deterministic);
+  if (need > kNoAllocScratchBytes) return RMSN_ERR_SCRATCH_LIMIT;
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(dev, &scratch)) != RMSN_OK) return st;
+  return rmsnorm_train_bwd(x, dy, dh, rstd, w, w_dtype, dx, dw, scratch, kNoAllocScratchBytes,
+                           T, nh, H, s_tok, s_head, deterministic, stream);
+}
