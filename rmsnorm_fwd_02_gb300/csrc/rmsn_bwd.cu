@@ -301,7 +301,9 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
 
 // dw[col] = sum over k = 0..P-1 of (hi_k + lo_k), in a fixed order: slice i of the
 // kFinishSlices slices takes k in [i*P/slices, (i+1)*P/slices) in increasing k, then the
-// slice sums are added in slice order.  TwoSum carries the error terms throughout.
+// slice sums are combined by a pairwise tree in slice order (i with i + stride, stride
+// halving).  TwoSum carries the error terms throughout.  Each thread walks only ~P/32
+// partials with four loads in flight, so the kernel is a short tail.
 __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
     rmsn_dw_finish_kernel(const float* __restrict__ part, float* __restrict__ dw, int P, int H) {
   __shared__ float sh[kFinishSlices][kFinishCols];
@@ -315,26 +317,42 @@ __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
   if (col < H) {
     const int ka = (sl * P) / kFinishSlices;
     const int kb = ((sl + 1) * P) / kFinishSlices;
-    for (int kk = ka; kk < kb; ++kk) {
-      const float hi = part[static_cast<size_t>(kk) * 2 * H + col];
-      const float lo = part[static_cast<size_t>(kk) * 2 * H + H + col];
+    const float* p = part + static_cast<size_t>(ka) * 2 * H + col;
+    int kk = ka;
+    for (; kk + 4 <= kb; kk += 4, p += static_cast<size_t>(8) * H) {
+      float hi[4], lo[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        hi[u] = p[static_cast<size_t>(2 * u) * H];
+        lo[u] = p[static_cast<size_t>(2 * u + 1) * H];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float err;
+        s = two_sum(s, hi[u], err);
+        e = __fadd_rn(e, __fadd_rn(err, lo[u]));
+      }
+    }
+    for (; kk < kb; ++kk, p += static_cast<size_t>(2) * H) {
       float err;
-      s = two_sum(s, hi, err);
-      e = __fadd_rn(e, __fadd_rn(err, lo));
+      s = two_sum(s, p[0], err);
+      e = __fadd_rn(e, __fadd_rn(err, p[H]));
     }
   }
   sh[sl][cl] = s;
   se[sl][cl] = e;
   __syncthreads();
-  if (sl == 0 && col < H) {
-    float S = sh[0][cl], E = se[0][cl];
-    for (int i = 1; i < kFinishSlices; ++i) {
+#pragma unroll
+  for (int stride = kFinishSlices / 2; stride > 0; stride >>= 1) {
+    if (sl < stride) {
       float err;
-      S = two_sum(S, sh[i][cl], err);
-      E = __fadd_rn(E, __fadd_rn(err, se[i][cl]));
+      const float S = two_sum(sh[sl][cl], sh[sl + stride][cl], err);
+      se[sl][cl] = __fadd_rn(__fadd_rn(se[sl][cl], se[sl + stride][cl]), err);
+      sh[sl][cl] = S;
     }
-    dw[col] = __fadd_rn(S, E);
+    __syncthreads();
   }
+  if (sl == 0 && col < H) dw[col] = __fadd_rn(sh[0][cl], se[0][cl]);
 }
 
 template <int VPT, bool kWide, bool kFp32W, bool kDh>

@@ -11,11 +11,11 @@
 // ring) and consumed by row groups whose threads own fixed 16-byte column vectors, so
 // every global access is a 16-byte coalesced vector and the weight stays in registers.
 //
-// Split-phase rows: phase A of row j reads the row, forms each warp's partial sum of
-// squares and arrives on the row's reduction mbarrier; phase B of row j-1 then waits on
-// that barrier (normally long complete), re-reads row j-1 from shared memory, and writes
-// y.  No warp ever blocks on the row it is still reducing, and the staged stage is
-// released per warp once phase B has read it.
+// Split-phase rows: phase A of row j reads the row and forms each thread's partial sum
+// of squares; phase B of row j-1 re-reads row j-1 from shared memory into registers,
+// releases the stage, waits for row j-1's reduction (published one iteration earlier, so
+// normally complete) and writes y; then row j's warp partials are published.  No warp
+// ever blocks on the row it is still reducing.
 //
 // Precision: the sum of squares is accumulated in FP32 (BF16 squares are exact in FP32,
 // so only the additions round); the reciprocal square root is the correctly rounded
@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
 
   float ss_carry = 0.f;  // sub-warp groups: row j-1's sum of squares
   for (int32_t j = 0; j <= ng; ++j) {
-    float ss_new = 0.f;
-    // ---- phase A, row j: sum of squares (and h in the residual form) ----
+    float part = 0.f;
+    // ---- phase A, row j: this thread's partial sum of squares (and h, residual form) ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
       const int s = j % S;
@@ -156,22 +156,32 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
         }
       }
       const f2 sp = f2_add(ss0, ss1);
-      const float part = f2_lo(sp) + f2_hi(sp);
-      if (red_smem) {
-        const float ss = warp_allsum(part);
-        if (lane == 0) {
-          slots[((j % kRedBufs) * G + g) * 32 + wg] = ss;
-          mbar_arrive(&redb[(j % kRedBufs) * G + g]);
-        }
-      } else {
-        ss_new = subwarp_allsum(part, NTg);
-      }
+      part = f2_lo(sp) + f2_hi(sp);
     }
     // ---- phase B, row j-1: rstd, y ----
+    // Its staged vectors go to registers first and the stage is released at once; then
+    // the row's reduction result is awaited (normally long complete), and row j's warp
+    // reduction runs inside B's arithmetic, where its shuffle chain overlaps B's math.
+    float red_j = 0.f;
     if (j >= 1) {
       const int32_t jj = j - 1;
       const int32_t row = r0 + jj * G + g;
       const int s = jj % S;
+      const bool valid = row < r1;
+      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      uint4 hv[VPT];
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        hv[v] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid && c < NV) {
+          hv[v] = lds128(xs + c * 8);
+          if constexpr (kRes)
+            hv[v] = residual_sum8(hv[v], lds128(xs + static_cast<size_t>(G) * H + c * 8));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp has its vectors of the stage
       float ss = ss_carry;
       if (red_smem) {
         const int rb = (jj % kRedBufs) * G + g;
@@ -179,32 +189,34 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
                           a.err, kErrConsumerWait);
         ss = slot_sum(slots + rb * 32, NW);
       }
-      if (row < r1) {
+      if (j < ng) red_j = red_smem ? warp_allsum(part) : subwarp_allsum(part, NTg);
+      if (valid) {
         const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
         const f2 rs2 = f2_splat(rs);
-        const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
         const size_t out_row = static_cast<size_t>(row) * H;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
           if (c < NV) {
-            uint4 u = lds128(xs + c * 8);
-            if constexpr (kRes)
-              u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
             uint4 o;
-            o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.x), rs2), wv[v][0]));
-            o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.y), rs2), wv[v][1]));
-            o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.z), rs2), wv[v][2]));
-            o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(u.w), rs2), wv[v][3]));
+            o.x = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].x), rs2), wv[v][0]));
+            o.y = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].y), rs2), wv[v][1]));
+            o.z = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].z), rs2), wv[v][2]));
+            o.w = f2_to_bf2(f2_mul(f2_mul(bf2_to_f2(hv[v].w), rs2), wv[v][3]));
             stg128(a.y + out_row + c * 8, o);
           }
         }
         if (lt == 0) a.rstd[row] = rs;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+    } else if (j < ng) {
+      red_j = red_smem ? warp_allsum(part) : subwarp_allsum(part, NTg);
     }
-    ss_carry = ss_new;
+    // ---- publish row j's reduction ----
+    if (j < ng && red_smem && lane == 0) {
+      slots[((j % kRedBufs) * G + g) * 32 + wg] = red_j;
+      mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+    }
+    ss_carry = red_j;
   }
 }
 

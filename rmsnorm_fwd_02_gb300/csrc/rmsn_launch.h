@@ -12,7 +12,7 @@ constexpr int kProducerThreads = 32;       // one warp; lane 0 issues the bulk c
 constexpr int kMaxConsumerThreads = 512;   // G * NTg
 constexpr int kMaxThreads = kMaxConsumerThreads + kProducerThreads;
 constexpr int kFinishCols = 32;            // dw columns per finishing CTA
-constexpr int kFinishSlices = 8;           // partition slices per finishing CTA
+constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 
 // Shared-memory carve-up of a row kernel (byte offsets), used by the kernels and by the
 // host's size computation alike.
