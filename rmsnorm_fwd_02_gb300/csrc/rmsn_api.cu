@@ -23,6 +23,7 @@ constexpr int kMaxDevices = 64;
 // each; "wide" kernels, one CTA an SM, take twice that.
 constexpr size_t kRingTarget = 96 * 1024;
 constexpr size_t kRingTargetWide = 192 * 1024;
+constexpr size_t kRingTargetSmall = 64 * 1024;
 constexpr int kMaxStages = 12;
 // Deterministic backward: at most kDetSMs x (the CTAs an SM the kernel is built to keep
 // resident) dw partials -- a function of the shape only, so the same on every device
@@ -70,16 +71,31 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd) {
   } else {
     s.ntg = ((per + 31) / 32) * 32;
   }
-  s.groups = s.ntg >= 256 ? 1 : 256 / s.ntg;
+  const bool multi = bwd && vpt == 2 && s.ntg >= 32 && s.ntg <= 256;
+  if (multi) {
+    s.groups = 512 / s.ntg;  // one CTA an SM, several rows in flight
+  } else {
+    s.groups = s.ntg >= 256 ? 1 : 256 / s.ntg;
+  }
   // groups that reduce through shared memory use named barriers 1..8
   if (s.ntg >= 32 && s.groups > 8) s.groups = 8;
   s.tensors = tensors;
   s.threads = s.groups * s.ntg + kProducerThreads;
-  // backward kernels past 288 threads or with 4-vector threads are built for one CTA an
-  // SM; every forward kernel is built for two
-  s.wide = bwd && (s.threads > 288 || s.vpt == 4);
+  if (!bwd)
+    s.cls = 0;
+  else if (multi)
+    s.cls = kBwdMulti;
+  else if (s.vpt == 4 || s.threads > 288)
+    s.cls = kBwdWide;
+  else
+    s.cls = kBwdNarrow;
   const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
-  int st = static_cast<int>((s.wide ? kRingTargetWide : kRingTarget) / stage_bytes);
+  // backward kernels built for one CTA an SM take the wide ring; forward CTAs of at most
+  // 6 warps take a 64 KB ring so that three share an SM (18 warps) when that still
+  // leaves four or more stages; the rest take 96 KB (two CTAs an SM)
+  size_t target = (bwd && s.cls != kBwdNarrow) ? kRingTargetWide : kRingTarget;
+  if (!bwd && s.threads <= 192 && kRingTargetSmall / stage_bytes >= 4) target = kRingTargetSmall;
+  int st = static_cast<int>(target / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
   s.smem = shared_bytes(s, H);
   return s;
@@ -132,7 +148,7 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
   if (want < 1) want = 1;
   int64_t cap;
   if (det) {
-    cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.vpt, s.wide);
+    cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.cls);
   } else {
     const int occ = bwd_blocks_per_sm(s, fp32w);
     cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);

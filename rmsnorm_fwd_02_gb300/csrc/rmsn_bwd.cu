@@ -37,16 +37,16 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
   return s;
 }
 
-// Launch bounds per shape class: up to 256 consumers + the producer warp, two CTAs an
-// SM (VPT 1 or 2, H <= 4096; narrow rows in 8- or 16-lane sub-warp groups); "wide" VPT=2 rows of H 4104..6144 with up to 384 consumers,
-// one CTA an SM; VPT=4 (H up to 8192) with 256 consumers, one CTA an SM.
-template <int VPT, bool kWide>
-constexpr int bwd_max_threads() { return (kWide && VPT == 2) ? 416 : 288; }
-template <int VPT, bool kWide>
-constexpr int bwd_min_blocks() { return bwd_design_blocks_per_sm(VPT, kWide); }
+// Launch bounds per shape class (see rmsn_launch.h): narrow CTAs of up to 288 threads,
+// two an SM; multi-group CTAs of up to 544 threads and wide CTAs (416 threads with
+// 2-vector threads, 288 with 4-vector threads), one an SM.
+template <int VPT, int kCls>
+constexpr int bwd_max_threads() {
+  return kCls == kBwdMulti ? 544 : (kCls == kBwdWide && VPT == 2 ? 416 : 288);
+}
 
-template <int VPT, bool kWide, bool kFp32W, bool kDh>
-__global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<VPT, kWide>())
+template <int VPT, int kCls, bool kFp32W, bool kDh>
+__global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_blocks_per_sm(kCls))
     rmsn_bwd_rows_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
@@ -203,7 +203,9 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
         const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi);
         const f2 rl2 = f2_splat(__fsub_rn(rs, rs_hi));
         // c = (1/H) sum g*xhat = (rstd/H) sum (dy*w)*x
-        const f2 nc2 = f2_splat(-(dot * (rs * inv_h)));
+        // dx = rstd*(g - x*(c*rstd)): xhat*c as one product of x, so the cancelling pair
+        // is a single fma; c*rstd is on the scale of dx, so no new overflow or underflow
+        const f2 ncr2 = f2_splat(-(dot * (rs * inv_h)) * rs);
         const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
         const size_t out_row = static_cast<size_t>(row) * H;
 #pragma unroll
@@ -219,9 +221,8 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kWide>(), bwd_min_blocks<
             for (int q = 0; q < 4; ++q) {
               const f2 x2 = bf2_to_f2(u4_get(xv, q));
               const f2 d2 = bf2_to_f2(u4_get(dv, q));
-              const f2 xh = f2_mul(x2, rs2);
               const f2 gw = f2_mul(d2, wv[v][q]);
-              f2 d = f2_mul(f2_fma(xh, nc2, gw), rs2);  // (g - xhat*c) * rstd
+              f2 d = f2_mul(f2_fma(x2, ncr2, gw), rs2);  // (g - xhat*c) * rstd
               if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
               o[q] = f2_to_bf2(d);
               // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
@@ -355,22 +356,26 @@ __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
   if (sl == 0 && col < H) dw[col] = __fadd_rn(sh[0][cl], se[0][cl]);
 }
 
-template <int VPT, bool kWide, bool kFp32W, bool kDh>
+template <int VPT, int kCls, bool kFp32W, bool kDh>
 static const void* bwd_kernel_ptr() {
-  return reinterpret_cast<const void*>(&rmsn_bwd_rows_kernel<VPT, kWide, kFp32W, kDh>);
+  return reinterpret_cast<const void*>(&rmsn_bwd_rows_kernel<VPT, kCls, kFp32W, kDh>);
 }
 
-template <int VPT, bool kWide>
+template <int VPT, int kCls>
 static const void* pick_bwd_v(bool fp32w, bool dh) {
   if (fp32w)
-    return dh ? bwd_kernel_ptr<VPT, kWide, true, true>() : bwd_kernel_ptr<VPT, kWide, true, false>();
-  return dh ? bwd_kernel_ptr<VPT, kWide, false, true>() : bwd_kernel_ptr<VPT, kWide, false, false>();
+    return dh ? bwd_kernel_ptr<VPT, kCls, true, true>() : bwd_kernel_ptr<VPT, kCls, true, false>();
+  return dh ? bwd_kernel_ptr<VPT, kCls, false, true>() : bwd_kernel_ptr<VPT, kCls, false, false>();
 }
 
 static const void* pick_bwd(const Shape& s, bool fp32w, bool dh) {
-  if (s.vpt == 1) return pick_bwd_v<1, false>(fp32w, dh);
-  if (s.vpt == 2) return s.wide ? pick_bwd_v<2, true>(fp32w, dh) : pick_bwd_v<2, false>(fp32w, dh);
-  return pick_bwd_v<4, true>(fp32w, dh);
+  if (s.vpt == 1) return pick_bwd_v<1, kBwdNarrow>(fp32w, dh);
+  if (s.vpt == 2) {
+    if (s.cls == kBwdMulti) return pick_bwd_v<2, kBwdMulti>(fp32w, dh);
+    if (s.cls == kBwdWide) return pick_bwd_v<2, kBwdWide>(fp32w, dh);
+    return pick_bwd_v<2, kBwdNarrow>(fp32w, dh);
+  }
+  return pick_bwd_v<4, kBwdWide>(fp32w, dh);
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem);

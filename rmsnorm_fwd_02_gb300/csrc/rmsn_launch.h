@@ -61,7 +61,7 @@ struct Shape {
   int tensors;   // BF16 tensors staged per row
   int threads;   // groups * ntg + producer warp
   size_t smem;   // dynamic shared memory bytes
-  bool wide;     // more than 288 threads: built for one CTA an SM
+  int cls;       // backward shape class (kBwdNarrow / kBwdMulti / kBwdWide); forward: 0
 };
 
 struct RowMapArgs {
@@ -111,12 +111,17 @@ cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
+// Backward shape classes, each its own kernel build:
+//  kBwdNarrow  up to 288 threads, two CTAs an SM: one-vector threads and sub-warp groups
+//  kBwdMulti   2-vector threads in row groups of 32..256 threads, up to 8 groups (544
+//              threads), one CTA an SM: several rows in flight per CTA
+//  kBwdWide    one row group of more than 256 threads (2-vector, H 4104..6144) or
+//              4-vector threads (H above 6144), one CTA an SM
+enum { kBwdNarrow = 0, kBwdMulti = 1, kBwdWide = 2 };
+
 // CTAs per SM the backward row kernel is built to keep resident (its launch bounds'
-// minimum), a compile-time property of the shape class: 2 for CTAs of at most 288
-// threads with 1 or 2 vectors a thread, else 1.
-constexpr int bwd_design_blocks_per_sm(int vpt, bool wide) {
-  return (vpt <= 2 && !wide) ? 2 : 1;
-}
+// minimum), a compile-time property of the shape class.
+constexpr int bwd_design_blocks_per_sm(int cls) { return cls == kBwdNarrow ? 2 : 1; }
 
 // Resident CTAs per SM of the chosen row kernel (cached per device).
 int fwd_blocks_per_sm(const Shape& s, bool fp32w);

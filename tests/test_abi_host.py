@@ -117,13 +117,13 @@ def test_bwd_rejects_before_any_cuda_call(lib, kw, want):
 
 def test_deterministic_workspace_size_depends_on_shape_only(lib):
     f = lib.rmsnorm_train_bwd_workspace_bytes
-    # H = 4096: one row group of 2-vector threads, two CTAs an SM -> at most 304 partials
-    # of 2*H floats; a CTA takes at least 4 stages (4 rows)
-    assert f(65536, 1, 4096, 1) == 304 * 2 * 4096 * 4
+    # H = 4096: two row groups of 2-vector threads in one CTA an SM -> at most 152
+    # partials of 2*H floats; a CTA takes at least 4 stages (8 rows)
+    assert f(65536, 1, 4096, 1) == 152 * 2 * 4096 * 4
+    assert f(1, 1, 4096, 1) == 1 * 2 * 4096 * 4
+    assert f(65, 1, 4096, 1) == 9 * 2 * 4096 * 4
     # H = 6144: 384 consumers, one CTA an SM -> at most 152
     assert f(65536, 1, 6144, 1) == 152 * 2 * 6144 * 4
-    assert f(1, 1, 4096, 1) == 1 * 2 * 4096 * 4
-    assert f(65, 1, 4096, 1) == 17 * 2 * 4096 * 4
     # H = 256: 16 two-row-a-warp groups (16 rows a stage), two CTAs an SM -> at most 304
     assert f(64, 1, 256, 1) == 1 * 2 * 256 * 4
     assert f(65, 1, 256, 1) == 2 * 2 * 256 * 4

@@ -8,6 +8,7 @@ residual form at H=6144; per-head views [T,24,256] strided and [T,4,256] contigu
 Ragged tails and empty/one-row cases come from the T values themselves (T=1, 65, 96)
 and from extra widths below.  Gates are documented in tests/parity.py.
 """
+import numpy as np
 import pytest
 
 from rmsnorm_fwd_02_gb300 import synth
@@ -66,4 +67,15 @@ def test_per_head_strided_other_strides():
     # head stride != H and a token stride that is not a multiple of the heads' span
     c = synth.make_case(5, 37, 256, nh=3, buf_heads=5, w_fp32=True, label="heads3of5")
     c.s_head = 2 * 256          # heads 0, 2, 4 of the 5-head buffer
+    parity.run_case(c)
+
+
+@pytest.mark.parametrize("scale", [2.0**40, 2.0**-40])
+@pytest.mark.parametrize("H", [768, 4096])
+def test_extreme_row_scales(H, scale):
+    # 5 % of the rows scaled by 2^40 or 2^-40 (rstd near 2^-40 or 2^40; eps small enough
+    # not to mask the tiny rows): every intermediate of dx and dw must stay in range
+    c = synth.make_case(11, 257, H, outlier_frac=0.05, outlier_scale=scale,
+                        label=f"scale{scale:g}_H{H}")
+    c.eps = float(np.float32(1e-30))
     parity.run_case(c)
