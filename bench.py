@@ -509,7 +509,7 @@ SWEEP = [
 
 def run_sweep(args):
     """Times each op of each workload: `reps` launches, each after an L2 flush outside the
-    events, CUDA events on the launch stream, median.  The flush READS a 512 MiB buffer,
+    events, CUDA events on the launch stream, trimmed mean.  The flush READS a 512 MiB buffer,
     so L2 is cold but clean: a write-based flush would leave dirty lines whose write-back
     lands inside the next timed kernel."""
     import torch
@@ -540,7 +540,11 @@ def run_sweep(args):
             b.record(stream)
             torch.cuda.synchronize()
             out.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(out)
+        # the event clock ticks in steps of about 2 us on this part: a median would be one
+        # of those steps, the mean of the middle 80 % resolves below it
+        out.sort()
+        cut = len(out) // 10
+        return statistics.fmean(out[cut:len(out) - cut])
 
     for label, T, H, nh, bh, w32, res in SWEEP:
         if args.sweep_filter and args.sweep_filter != f"{label}_{T}_{H}":

@@ -133,14 +133,40 @@ int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, con
                               int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head,
                               int deterministic, void* stream);
 
+/*
+ * The launch plan the library uses for one op at width H: for tests and diagnostics.
+ * No device access; the result depends on H and op only.
+ *   op     RMSN_PLAN_FWD, RMSN_PLAN_FWD_RESIDUAL, RMSN_PLAN_BWD or RMSN_PLAN_BWD_DH
+ *   out    host array receiving min(n_out, RMSN_PLAN_FIELDS) values, in this order:
+ *            [0] 16-byte column vectors (8 columns) per consumer thread
+ *            [1] threads per row group (8 or 16: sub-warp groups; else whole warps)
+ *            [2] row groups per CTA (= rows per ring stage)
+ *            [3] ring stages
+ *            [4] threads per CTA (the row groups + one producer warp)
+ *            [5] dynamic shared memory bytes per CTA
+ *            [6] shape class (forward: 0 two CTAs an SM, 1 one CTA an SM; backward:
+ *                0 narrow, 1 several row groups, 2 wide)
+ *            [7] most threads a CTA of that class's kernel build may have
+ *            [8] CTAs per SM that class's kernel build is made for
+ * Returns RMSN_OK; RMSN_ERR_INVALID_ARG for an unknown op, out == NULL, n_out < 0 or H
+ * not a positive multiple of 8; RMSN_ERR_UNSUPPORTED for H above 8192.
+ */
+#define RMSN_PLAN_FWD 0
+#define RMSN_PLAN_FWD_RESIDUAL 1
+#define RMSN_PLAN_BWD 2
+#define RMSN_PLAN_BWD_DH 3
+#define RMSN_PLAN_FIELDS 9
+int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out);
+
 /* Static string naming a status code (never NULL). */
 const char* rmsnorm_train_status_str(int status);
 
 /*
  * Reads (and, if reset != 0, clears) the library's device-side error word on the current
  * device into *flags (host pointer).  Nonzero means a kernel gave up on a bounded wait
- * (bit 0: a consumer waited too long for staged data; bit 1: the staging producer waited
- * too long for a free buffer); that call's outputs are then unspecified.  This entry point
+ * (bit 0: a consumer waited too long for staged data or for a row's reduction; bit 1:
+ * the staging producer waited too long for a free buffer); that call's outputs are then
+ * unspecified.  This entry point
  * SYNCHRONIZES the device; it is meant for tests and diagnostics, not the hot path.
  */
 int rmsnorm_train_device_error(unsigned int* flags, int reset);

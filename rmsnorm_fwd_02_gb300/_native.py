@@ -32,7 +32,12 @@ SIGNATURES = {
                                          _i32, _i64, _i64, _int, _vp]),
     "rmsnorm_train_status_str": (C.c_char_p, [_int]),
     "rmsnorm_train_device_error": (_int, [C.POINTER(C.c_uint), _int]),
+    "rmsnorm_train_launch_plan": (_int, [_i32, _int, C.POINTER(C.c_int64), _int]),
 }
+
+PLAN_FWD, PLAN_FWD_RESIDUAL, PLAN_BWD, PLAN_BWD_DH = 0, 1, 2, 3
+PLAN_FIELDS = ("vpt", "group_threads", "groups", "stages", "threads", "smem", "cls",
+               "class_max_threads", "class_blocks_per_sm")
 
 _lib = None
 
@@ -123,3 +128,12 @@ def rmsnorm_train_device_error(reset=True):
     if st != RMSN_OK:
         raise RmsnError("rmsnorm_train_device_error", st)
     return int(flags.value)
+
+
+def rmsnorm_train_launch_plan(H, op):
+    """The library's launch plan for one op (PLAN_*) at width H, as a dict."""
+    out = (C.c_int64 * len(PLAN_FIELDS))()
+    st = lib().rmsnorm_train_launch_plan(H, op, out, len(PLAN_FIELDS))
+    if st != RMSN_OK:
+        raise RmsnError("rmsnorm_train_launch_plan", st)
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))

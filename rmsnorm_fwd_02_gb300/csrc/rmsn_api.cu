@@ -24,6 +24,10 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kRingTarget = 96 * 1024;
 constexpr size_t kRingTargetWide = 192 * 1024;
 constexpr size_t kRingTargetSmall = 64 * 1024;
+// Forward rows whose group has at least this many threads run one CTA an SM (kFwdSolo).
+constexpr int kFwdSoloMinGroup = 64;
+// Largest row group of the backward's multi-group class (a multiple of 32, <= 480 / 2).
+constexpr int kMultiMaxGroup = 240;
 constexpr int kMaxStages = 12;
 // Deterministic backward: at most kDetSMs x (the CTAs an SM the kernel is built to keep
 // resident) dw partials -- a function of the shape only, so the same on every device
@@ -44,8 +48,9 @@ uint64_t key(int dev, const void* fn, uint64_t extra) {
   return h;
 }
 
-size_t shared_bytes(const Shape& s, int H) {
-  return smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0).total;
+size_t shared_bytes(const Shape& s, int H, bool bwd) {
+  return smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0,
+                     bwd ? s.groups : 0).total;
 }
 
 // Column vectors per thread, from the instantiated set `allowed` (descending): the
@@ -71,33 +76,38 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd) {
   } else {
     s.ntg = ((per + 31) / 32) * 32;
   }
-  const bool multi = bwd && vpt == 2 && s.ntg >= 32 && s.ntg <= 256;
-  if (multi) {
-    s.groups = 512 / s.ntg;  // one CTA an SM, several rows in flight
+  if (bwd) {
+    if ((vpt == 2 || vpt == 3) && s.ntg >= 32 && s.ntg <= kMultiMaxGroup)
+      s.cls = kBwdMulti;
+    else if (vpt >= 2 && s.ntg >= 32)
+      s.cls = kBwdWide;
+    else
+      s.cls = kBwdNarrow;
   } else {
-    s.groups = s.ntg >= 256 ? 1 : 256 / s.ntg;
+    // rows of more than 256 threads exceed the two-CTA build: always one CTA an SM
+    s.cls = (vpt >= 2 && (s.ntg >= kFwdSoloMinGroup || s.ntg > 256)) ? kFwdSolo : kFwdPair;
   }
-  // groups that reduce through shared memory use named barriers 1..8
-  if (s.ntg >= 32 && s.groups > 8) s.groups = 8;
+  // one-CTA-an-SM classes with several row groups fill 512 (forward) or 480 (backward)
+  // consumers, the rest 256
+  int budget = kMaxConsumerThreads / 2;
+  if (!bwd && s.cls == kFwdSolo) budget = kMaxConsumerThreads;
+  if (bwd && s.cls == kBwdMulti) budget = kMultiConsumers;
+  s.groups = s.ntg >= budget ? 1 : budget / s.ntg;
+  // whole-warp groups: at most 16 (their reduction slots in shared memory)
+  if (s.ntg >= 32 && s.groups > 16) s.groups = 16;
   s.tensors = tensors;
   s.threads = s.groups * s.ntg + kProducerThreads;
-  if (!bwd)
-    s.cls = 0;
-  else if (multi)
-    s.cls = kBwdMulti;
-  else if (s.vpt == 4 || s.threads > 288)
-    s.cls = kBwdWide;
-  else
-    s.cls = kBwdNarrow;
   const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
-  // backward kernels built for one CTA an SM take the wide ring; forward CTAs of at most
-  // 6 warps take a 64 KB ring so that three share an SM (18 warps) when that still
-  // leaves four or more stages; the rest take 96 KB (two CTAs an SM)
-  size_t target = (bwd && s.cls != kBwdNarrow) ? kRingTargetWide : kRingTarget;
-  if (!bwd && s.threads <= 192 && kRingTargetSmall / stage_bytes >= 4) target = kRingTargetSmall;
+  // kernels built for one CTA an SM take the wide ring; forward CTAs of at most 6 warps
+  // take a 64 KB ring so that three share an SM when that still leaves four or more
+  // stages; the rest take 96 KB (two CTAs an SM)
+  const bool one_cta = bwd ? s.cls != kBwdNarrow : s.cls == kFwdSolo;
+  size_t target = one_cta ? kRingTargetWide : kRingTarget;
+  if (!bwd && !one_cta && s.threads <= 192 && kRingTargetSmall / stage_bytes >= 4)
+    target = kRingTargetSmall;
   int st = static_cast<int>(target / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
-  s.smem = shared_bytes(s, H);
+  s.smem = shared_bytes(s, H, bwd);
   return s;
 }
 
@@ -166,13 +176,27 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
 Shape fwd_shape(int H, bool residual) {
   const int nv = H / 8;
   // narrow rows: 4 vectors a lane in 8- or 16-lane groups
-  const int vpt = nv <= 64 ? (nv >= 4 ? 4 : 1) : pick_vpt(nv, {4, 3, 2, 1});
+  int vpt = nv <= 64 ? (nv >= 4 ? 4 : 1) : pick_vpt(nv, {4, 3, 2, 1});
+  // one-vector threads only while a row needs at most 256 of them (the two-CTA build);
+  // past that, ragged 4-vector rows
+  if (vpt == 1 && nv > 256) vpt = 4;
   return make_shape(H, residual ? 2 : 1, vpt, false);
 }
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
-  // narrow rows: 2 vectors a lane in 8- or 16-lane groups
-  const int vpt = nv <= 768 ? (nv >= 2 ? 2 : 1) : 4;
+  // narrow rows: 2 vectors a lane in 8- or 16-lane groups; rows that 240 threads cover
+  // with 2 or 3 vectors each: several row groups in one CTA (kBwdMulti); wider rows:
+  // one group of 2-vector threads, or of 4-vector threads past H = 6144 (kBwdWide)
+  auto group = [nv](int v) { return ((nv + v - 1) / v + 31) / 32 * 32; };
+  int vpt;
+  if (nv < 2)
+    vpt = 1;
+  else if (group(2) <= kMultiMaxGroup)
+    vpt = 2;
+  else if (group(3) <= kMultiMaxGroup)
+    vpt = 3;
+  else
+    vpt = nv <= 768 ? 2 : 4;
   return make_shape(H, with_dh ? 3 : 2, vpt, true);
 }
 
@@ -365,6 +389,21 @@ int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float
   }
   if (launch_dw_finish(static_cast<const float*>(workspace), dw, P, H, stream_) != cudaSuccess)
     return RMSN_ERR_CUDA;
+  return RMSN_OK;
+}
+
+int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out) {
+  if (!out || n_out < 0 || op < RMSN_PLAN_FWD || op > RMSN_PLAN_BWD_DH) return RMSN_ERR_INVALID_ARG;
+  if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
+  if (H > kMaxH) return RMSN_ERR_UNSUPPORTED;
+  const bool bwd = op >= RMSN_PLAN_BWD;
+  const Shape s = bwd ? bwd_shape(H, op == RMSN_PLAN_BWD_DH)
+                      : fwd_shape(H, op == RMSN_PLAN_FWD_RESIDUAL);
+  const int64_t v[RMSN_PLAN_FIELDS] = {
+      s.vpt, s.ntg, s.groups, s.stages, s.threads, static_cast<int64_t>(s.smem), s.cls,
+      bwd ? bwd_max_threads(s.cls, s.vpt) : fwd_max_threads(s.cls),
+      bwd ? bwd_design_blocks_per_sm(s.cls) : fwd_design_blocks_per_sm(s.cls)};
+  for (int i = 0; i < n_out && i < RMSN_PLAN_FIELDS; ++i) out[i] = v[i];
   return RMSN_OK;
 }
 

@@ -37,32 +37,32 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
   return s;
 }
 
-// Launch bounds per shape class (see rmsn_launch.h): narrow CTAs of up to 288 threads,
-// two an SM; multi-group CTAs of up to 544 threads and wide CTAs (416 threads with
-// 2-vector threads, 288 with 4-vector threads), one an SM.
-template <int VPT, int kCls>
-constexpr int bwd_max_threads() {
-  return kCls == kBwdMulti ? 544 : (kCls == kBwdWide && VPT == 2 ? 416 : 288);
-}
-
+// Launch bounds per shape class (rmsn_launch.h): narrow CTAs of up to 256 consumers, two
+// an SM; multi-group CTAs of up to 480 consumers and wide CTAs (384 consumers with
+// 2-vector threads, 256 with 4-vector threads), one an SM; each + the producer warp.
 template <int VPT, int kCls, bool kFp32W, bool kDh>
-__global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_blocks_per_sm(kCls))
+__global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_per_sm(kCls))
     rmsn_bwd_rows_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
+  // rstd staged with its rows and read from shared memory in phase B (else each consumer
+  // would load its row's rstd from global memory in phase A, one iteration ahead)
+  constexpr bool kStageRs = true;
   const int H = a.map.H;
   const int NV = H >> 3;
   const int G = a.groups, NTg = a.ntg, S = a.stages;
   const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
   const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
-  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0);
+  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0, G);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
   uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kRedBufs][G]
   float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kRedBufs][G][32]
+  float* rs_ring = reinterpret_cast<float*>(smem + L.rs);        // [S][RSP] staged rstd
+  const int RSP = rs_stride(G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
 
   const int tid = threadIdx.x;
@@ -89,8 +89,10 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_block
   if (tid >= ncons) {  // ---- producer warp ----
     if (tid == ncons) {
       const uint64_t pol = l2_evict_first_policy();
+      const bool rs_bulk = (reinterpret_cast<uintptr_t>(a.rstd) & 15u) == 0;
       const RowMap m{a.map.nh, H, a.map.s_tok, a.map.s_head};
-      for (int32_t j = 0; j < nstage; ++j) {
+      int32_t j = 0;
+      for (; j < nstage; ++j) {
         const int s = j % S;
         if (j >= S &&
             !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
@@ -98,7 +100,22 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_block
           break;
         const int32_t ra = r0 + j * G;
         const int32_t rb = min(ra + G, r1);
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u * NT);
+        // The stage's rstd values travel with it, so no consumer waits on a global load:
+        // the whole 16-byte blocks of rstd covering rows [ra, rb) by one bulk copy (slot
+        // index r - a4), and rows past the last whole block of the array -- or every row,
+        // when rstd is not 16-byte aligned -- by 4-byte async copies that the same
+        // barrier tracks (one extra pending arrival, taken before the arrival below).
+        const int32_t a4 = ra & ~3;
+        const int32_t b4 = !kStageRs ? a4 : (rs_bulk ? min((rb + 3) & ~3, a.R & ~3) : a4);
+        float* rsd = rs_ring + s * RSP;
+        if (kStageRs && rb > b4) {
+          for (int32_t r = max(ra, b4); r < rb; ++r) cp_async_4(rsd + (r - a4), a.rstd + r);
+          cp_async_mbar_arrive(&full[s]);
+        }
+        const uint32_t rs_bytes = static_cast<uint32_t>(b4 - a4) * 4u;
+        mbar_arrive_expect_tx(&full[s],
+                              static_cast<uint32_t>(rb - ra) * H * 2u * NT + rs_bytes);
+        if (rs_bytes) bulk_g2s(rsd, a.rstd + a4, rs_bytes, &full[s], pol);
         __nv_bfloat16* dst = ring + s * stage_elems;
         if (a.contig)
           copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
@@ -107,6 +124,7 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_block
         copy_rows_contig(dst + G * H, a.dy, H, ra, rb, &full[s], pol);
         if constexpr (kDh) copy_rows_contig(dst + 2 * G * H, a.dh, H, ra, rb, &full[s], pol);
       }
+      mbar_drain(full, S, j);
     }
     return;
   }
@@ -138,15 +156,15 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_block
   const int g0 = red_smem ? g : (tid & ~31) / NTg;
   const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
-  float rs_prev = 0.f;   // rstd of row j-1 (loaded during phase A of row j-1)
   float dot_carry = 0.f; // sub-warp groups: row j-1's sum of (dy*w)*x
+  float rs_carry = 0.f;  // multi-group build: row j-1's rstd, loaded in phase A(j-1)
   for (int32_t j = 0; j <= ng; ++j) {
-    float rs_new = 0.f, dot_new = 0.f;
+    float dot_new = 0.f, rs_new = 0.f;
     // ---- phase A, row j: partial of sum (dy*w)*x ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
       const bool valid = row < r1;
-      if (valid) rs_new = __ldg(a.rstd + row);  // consumed one iteration later
+      if (!kStageRs && valid) rs_new = __ldg(a.rstd + row);
       const int s = j % S;
       mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
                         kErrConsumerWait);
@@ -195,7 +213,8 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_block
         dot = slot_sum(slots + rb * 32, NW);
       }
       if (row < r1) {
-        const float rs = rs_prev;
+        // this row's rstd, staged with the row (the stage is held until phase B ends)
+        const float rs = kStageRs ? rs_ring[s * RSP + (row - ((r0 + jj * G) & ~3))] : rs_carry;
         // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
         // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
         // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
@@ -241,8 +260,8 @@ __global__ void __launch_bounds__(bwd_max_threads<VPT, kCls>(), bwd_design_block
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
     }
-    rs_prev = rs_new;
     dot_carry = dot_new;
+    rs_carry = rs_new;
   }
 
   // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----
@@ -375,6 +394,7 @@ static const void* pick_bwd(const Shape& s, bool fp32w, bool dh) {
     if (s.cls == kBwdWide) return pick_bwd_v<2, kBwdWide>(fp32w, dh);
     return pick_bwd_v<2, kBwdNarrow>(fp32w, dh);
   }
+  if (s.vpt == 3) return pick_bwd_v<3, kBwdMulti>(fp32w, dh);
   return pick_bwd_v<4, kBwdWide>(fp32w, dh);
 }
 

@@ -7,7 +7,9 @@
 // (consumer releases).  Consumers are G row groups of NTg threads; group g takes row slot
 // g of every stage, and each thread owns the same VPT 16-byte column vectors of every row
 // it touches (column vector c = lt + v*NTg), so per-column state (the weight, the dw
-// partial sums) lives in registers for the whole chunk.
+// partial sums) lives in registers for the whole chunk.  The producer has a warp of its
+// own: issuing a stage's copies takes long enough that, done by a consumer warp, it would
+// sit on the slowest warp's path every stage.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -83,6 +85,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// The producer's last step: waits until the `issued` stages' copies have landed (the last
+// S of them; earlier ones were released by the consumers), so that no copy still writes
+// this CTA's shared memory once it exits -- also after an abort, whose flag it ignores.
+// Bounded by one kWaitLimitNs for the whole drain.
+__device__ __forceinline__ void mbar_drain(uint64_t* full, int S, int32_t issued) {
+  const unsigned long long t0 = global_ns();
+  for (int32_t j = issued > S ? issued - S : 0; j < issued; ++j) {
+    const uint32_t parity = static_cast<uint32_t>(j / S) & 1u;
+    while (!mbar_try_wait(&full[j % S], parity))
+      if (global_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -103,6 +118,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned).
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// Makes `bar` track this thread's earlier cp.async copies: adds one pending arrival to
+// the current phase now and performs that arrival once the copies have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
@@ -288,35 +316,38 @@ struct RowMap {
   int64_t s_head;
 };
 
-// Copies rows [ra, rb) of a BF16 tensor into consecutive H-element slots at `dst`,
-// merging rows that are adjacent in memory into one bulk copy.  The (token, head) walk is
-// incremental: one division per call, none per row (a single producer thread issues
-// every copy of its CTA, so its per-row cost bounds the CTA's row rate).
+// Copies rows [ra, rb) of a BF16 tensor into consecutive H-element slots at `dst`.  When
+// a token's heads are back to back (s_head == H) the rows of one token form one run and
+// take one bulk copy, so the walk costs one step per token touched, not per row (the
+// producer's time between a slot's release and the slot's copies adds to every stage's
+// turnaround).  Otherwise every row is its own copy.  One division per call.
 __device__ __forceinline__ void copy_rows(__nv_bfloat16* dst, const __nv_bfloat16* src,
                                           const RowMap& m, int32_t ra, int32_t rb,
                                           uint64_t* bar, uint64_t pol) {
   int32_t t = ra / m.nh;
   int32_t h = ra - t * m.nh;
-  int64_t off = static_cast<int64_t>(t) * m.s_tok + static_cast<int64_t>(h) * m.s_head;
-  int32_t r = ra;
-  while (r < rb) {
-    const int64_t run_off = off;
-    int32_t n = 0;
-    int64_t next = off;
-    do {  // extend the run while the next row starts where this one ends
-      ++n;
+  const uint32_t row_bytes = static_cast<uint32_t>(m.H) * 2u;
+  __nv_bfloat16* d = dst;
+  if (m.s_head == m.H) {
+    for (int32_t r = ra; r < rb; ++t, h = 0) {
+      const int32_t n = min(rb - r, m.nh - h);
+      bulk_g2s(d, src + static_cast<int64_t>(t) * m.s_tok + static_cast<int64_t>(h) * m.H,
+               static_cast<uint32_t>(n) * row_bytes, bar, pol);
+      d += static_cast<int64_t>(n) * m.H;
+      r += n;
+    }
+  } else {
+    int64_t off = static_cast<int64_t>(t) * m.s_tok + static_cast<int64_t>(h) * m.s_head;
+    for (int32_t r = ra; r < rb; ++r, d += m.H) {
+      bulk_g2s(d, src + off, row_bytes, bar, pol);
       if (++h == m.nh) {
         h = 0;
         ++t;
-        next = static_cast<int64_t>(t) * m.s_tok;
+        off = static_cast<int64_t>(t) * m.s_tok;
       } else {
-        next += m.s_head;
+        off += m.s_head;
       }
-    } while (r + n < rb && next == run_off + static_cast<int64_t>(n) * m.H);
-    bulk_g2s(dst + static_cast<int64_t>(r - ra) * m.H, src + run_off,
-             static_cast<uint32_t>(n) * static_cast<uint32_t>(m.H) * 2u, bar, pol);
-    r += n;
-    off = next;
+    }
   }
 }
 

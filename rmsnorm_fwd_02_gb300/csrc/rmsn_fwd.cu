@@ -39,10 +39,14 @@ __device__ __forceinline__ uint4 residual_sum8(const uint4& u, const uint4& q) {
   return r;
 }
 
-// At most 256 consumers (G*NTg) + the producer warp; two CTAs an SM.  Narrow rows use
-// sub-warp groups of 8 or 16 lanes (several rows a warp, reduced by shuffles alone).
-template <int VPT, bool kFp32W, bool kRes>
-__global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
+// Launch bounds per shape class (rmsn_launch.h): kFwdPair, at most 256 consumers (G*NTg)
+// + the producer warp, two CTAs an SM; kFwdSolo, at most 512 consumers + the producer
+// warp, one CTA an SM.
+// Narrow rows use sub-warp groups of 8 or 16 lanes (several rows a warp, reduced by
+// shuffles alone).
+template <int VPT, int kCls, bool kFp32W, bool kRes>
+__global__ void __launch_bounds__(fwd_max_threads(kCls), fwd_design_blocks_per_sm(kCls))
+    rmsn_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kRes ? 2 : 1;
   const int H = a.map.H;
@@ -51,7 +55,7 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
   const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
-  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0);
+  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0, 0);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -87,7 +91,8 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
     if (tid == ncons) {
       const uint64_t pol = l2_evict_first_policy();
       const RowMap m{a.map.nh, H, a.map.s_tok, a.map.s_head};
-      for (int32_t j = 0; j < nstage; ++j) {
+      int32_t j = 0;
+      for (; j < nstage; ++j) {
         const int s = j % S;
         if (j >= S &&
             !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
@@ -105,6 +110,7 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
           if constexpr (kRes) copy_rows(dst + G * H, a.res, m, ra, rb, &full[s], pol);
         }
       }
+      mbar_drain(full, S, j);
     }
     return;
   }
@@ -220,23 +226,32 @@ __global__ void __launch_bounds__(288, 2) rmsn_fwd_kernel(const FwdArgs a) {
   }
 }
 
-template <int VPT, bool kFp32W, bool kRes>
+template <int VPT, int kCls, bool kFp32W, bool kRes>
 static const void* fwd_kernel_ptr() {
-  return reinterpret_cast<const void*>(&rmsn_fwd_kernel<VPT, kFp32W, kRes>);
+  return reinterpret_cast<const void*>(&rmsn_fwd_kernel<VPT, kCls, kFp32W, kRes>);
 }
 
-template <int VPT>
+template <int VPT, int kCls>
 static const void* pick_fwd_v(bool fp32w, bool res) {
-  if (fp32w) return res ? fwd_kernel_ptr<VPT, true, true>() : fwd_kernel_ptr<VPT, true, false>();
-  return res ? fwd_kernel_ptr<VPT, false, true>() : fwd_kernel_ptr<VPT, false, false>();
+  if (fp32w)
+    return res ? fwd_kernel_ptr<VPT, kCls, true, true>() : fwd_kernel_ptr<VPT, kCls, true, false>();
+  return res ? fwd_kernel_ptr<VPT, kCls, false, true>() : fwd_kernel_ptr<VPT, kCls, false, false>();
 }
 
-static const void* pick_fwd(int vpt, bool fp32w, bool res) {
-  switch (vpt) {
-    case 1: return pick_fwd_v<1>(fp32w, res);
-    case 2: return pick_fwd_v<2>(fp32w, res);
-    case 3: return pick_fwd_v<3>(fp32w, res);
-    default: return pick_fwd_v<4>(fp32w, res);
+// kFwdSolo is built for 2..4 vectors a thread; 1-vector rows always take kFwdPair.
+static const void* pick_fwd(const Shape& s, bool fp32w, bool res) {
+  if (s.cls == kFwdSolo) {
+    switch (s.vpt) {
+      case 2: return pick_fwd_v<2, kFwdSolo>(fp32w, res);
+      case 3: return pick_fwd_v<3, kFwdSolo>(fp32w, res);
+      default: return pick_fwd_v<4, kFwdSolo>(fp32w, res);
+    }
+  }
+  switch (s.vpt) {
+    case 1: return pick_fwd_v<1, kFwdPair>(fp32w, res);
+    case 2: return pick_fwd_v<2, kFwdPair>(fp32w, res);
+    case 3: return pick_fwd_v<3, kFwdPair>(fp32w, res);
+    default: return pick_fwd_v<4, kFwdPair>(fp32w, res);
   }
 }
 
@@ -246,11 +261,11 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
                        void** args);                           // rmsn_api.cu
 
 int fwd_blocks_per_sm(const Shape& s, bool fp32w) {
-  return blocks_per_sm(pick_fwd(s.vpt, fp32w, s.tensors == 2), s.threads, s.smem);
+  return blocks_per_sm(pick_fwd(s, fp32w, s.tensors == 2), s.threads, s.smem);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st) {
-  const void* fn = pick_fwd(s.vpt, fp32w, a.res != nullptr);
+  const void* fn = pick_fwd(s, fp32w, a.res != nullptr);
   cudaError_t e = prepare_kernel(fn, s.smem);
   if (e != cudaSuccess) return e;
   FwdArgs copy = a;

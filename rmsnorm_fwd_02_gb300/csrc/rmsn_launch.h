@@ -10,7 +10,6 @@ namespace rmsn {
 constexpr int kMaxH = 8192;
 constexpr int kProducerThreads = 32;       // one warp; lane 0 issues the bulk copies
 constexpr int kMaxConsumerThreads = 512;   // G * NTg
-constexpr int kMaxThreads = kMaxConsumerThreads + kProducerThreads;
 constexpr int kFinishCols = 32;            // dw columns per finishing CTA
 constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 
@@ -20,6 +19,8 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 //   full, empty   [stages] mbarriers (staged bytes landed / stage released)
 //   redb   [kRedBufs][groups] mbarriers: a row's per-warp reduction partials are written
 //   slots  [kRedBufs][groups][32] FP32 per-warp reduction partials
+//   rs     [stages][rs_stride(rs_rows)] FP32: the staged rows' rstd (backward; forward:
+//          none), from the 16-byte block holding the stage's first row onwards
 //   abort  CTA abort flag of the bounded waits
 //
 // Row j's reduction uses buffer j % kRedBufs.  A warp writes buffer j in phase A(j) after
@@ -28,13 +29,18 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 // same ordering keeps each redb barrier within one phase of its waiters.
 constexpr int kRedBufs = 4;
 struct SmemLayout {
-  size_t full, empty, redb, slots, abort_flag, total;
+  size_t full, empty, redb, slots, rs, abort_flag, total;
 };
+
+// Floats per stage of the staged rstd: the stage's `rows` values start up to 3 floats
+// into their first 16-byte block, and a stage slot stays a whole number of blocks.
+__host__ __device__ constexpr int rs_stride(int rows) { return rows == 0 ? 0 : ((rows + 6) & ~3); }
 
 // `red_groups` is the number of row groups that reduce through shared memory: all of them
 // when a group spans whole warps, none when groups are sub-warp (shuffles only).
+// `rs_rows` is the number of rstd values staged with each stage (the backward's groups).
 __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int groups, int H,
-                                                  int red_groups) {
+                                                  int red_groups, int rs_rows) {
   SmemLayout L;
   size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
   L.full = off;
@@ -46,6 +52,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int g
   off = (off + 127) & ~static_cast<size_t>(127);
   L.slots = off;
   off += 4 * kRedBufs * 32 * static_cast<size_t>(red_groups);
+  L.rs = off;  // 128-byte aligned
+  off += 4 * static_cast<size_t>(stages) * rs_stride(rs_rows);
   L.abort_flag = off;
   off += 16;
   L.total = off;
@@ -54,14 +62,14 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int g
 
 // Launch shape of a row kernel, a function of H (and of the mode for P).
 struct Shape {
-  int vpt;       // 16-byte column vectors per consumer thread (1 or 2)
+  int vpt;       // 16-byte column vectors per consumer thread (1..4)
   int ntg;       // threads per row group: 8 or 16 (sub-warp) or a multiple of 32
   int groups;    // row groups per CTA = rows per stage
   int stages;    // depth of the shared-memory ring
   int tensors;   // BF16 tensors staged per row
   int threads;   // groups * ntg + producer warp
   size_t smem;   // dynamic shared memory bytes
-  int cls;       // backward shape class (kBwdNarrow / kBwdMulti / kBwdWide); forward: 0
+  int cls;       // shape class: kFwdPair / kFwdSolo, or kBwdNarrow / kBwdMulti / kBwdWide
 };
 
 struct RowMapArgs {
@@ -112,16 +120,39 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaSt
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
 // Backward shape classes, each its own kernel build:
-//  kBwdNarrow  up to 288 threads, two CTAs an SM: one-vector threads and sub-warp groups
-//  kBwdMulti   2-vector threads in row groups of 32..256 threads, up to 8 groups (544
-//              threads), one CTA an SM: several rows in flight per CTA
-//  kBwdWide    one row group of more than 256 threads (2-vector, H 4104..6144) or
+//  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector threads and sub-warp groups
+//  kBwdMulti   2- or 3-vector threads in row groups of 32..240 threads, as many groups as
+//              fit in 480 consumers, one CTA an SM: several rows in flight per CTA.  With
+//              the producer that is 16 warps, four a scheduler partition, which leaves
+//              128 registers a thread (17 warps would put five warps on one partition
+//              and cap every thread at 96, too few for the dw state without spills)
+//  kBwdWide    one row group of more than 240 threads (2-vector, H up to 6144) or
 //              4-vector threads (H above 6144), one CTA an SM
 enum { kBwdNarrow = 0, kBwdMulti = 1, kBwdWide = 2 };
+constexpr int kMultiConsumers = 480;
 
 // CTAs per SM the backward row kernel is built to keep resident (its launch bounds'
 // minimum), a compile-time property of the shape class.
 constexpr int bwd_design_blocks_per_sm(int cls) { return cls == kBwdNarrow ? 2 : 1; }
+
+// Threads a backward CTA of the class may have (its launch bounds' maximum).
+constexpr int bwd_max_threads(int cls, int vpt) {
+  return kProducerThreads +
+         (cls == kBwdMulti ? kMultiConsumers : (cls == kBwdWide && vpt == 2 ? 384 : 256));
+}
+
+// Forward shape classes:
+//  kFwdPair  up to 256 consumers + the producer warp, two CTAs an SM: sub-warp groups
+//            and rows of at most 32-thread groups
+//  kFwdSolo  up to 512 consumers + the producer warp, one CTA an SM: row groups of 64
+//            threads or more, as many as fit in 512 consumers (one when a row needs more
+//            than 256 threads)
+// Two CTAs an SM split its bandwidth unevenly (one of the pair finishes its equal share
+// first and the other then runs alone); one CTA holding the same number of rows in
+// flight avoids that, where a row group is large enough to keep the warps busy.
+enum { kFwdPair = 0, kFwdSolo = 1 };
+constexpr int fwd_design_blocks_per_sm(int cls) { return cls == kFwdPair ? 2 : 1; }
+constexpr int fwd_max_threads(int cls) { return kProducerThreads + (cls == kFwdPair ? 256 : 512); }
 
 // Resident CTAs per SM of the chosen row kernel (cached per device).
 int fwd_blocks_per_sm(const Shape& s, bool fp32w);

@@ -137,3 +137,51 @@ def test_deterministic_workspace_size_depends_on_shape_only(lib):
 def test_package_import_needs_no_gpu():
     import rmsnorm_fwd_02_gb300 as R
     assert callable(R.rmsnorm_fwd) and callable(R.rmsnorm_train)
+
+
+SMEM_PER_SM = 228 * 1024      # GB300 shared memory per SM, of which 1 KB per CTA is reserved
+SMEM_PER_CTA = 227 * 1024
+
+
+@pytest.mark.parametrize("op", [0, 1, 2, 3], ids=["fwd", "fwd_res", "bwd", "bwd_dh"])
+def test_launch_plan_fits_its_kernel_build_at_every_width(lib, op):
+    # Every supported width: the CTA fits the launch bounds of the kernel build it selects,
+    # the ring and barriers fit shared memory at the build's CTAs per SM, the row groups
+    # cover the row, and (backward) the ring can hold the end-of-kernel dw combine buffer.
+    from rmsnorm_fwd_02_gb300 import _native as N
+    tensors = {0: 1, 1: 2, 2: 2, 3: 3}[op]
+    for H in range(8, 8193, 8):
+        p = N.rmsnorm_train_launch_plan(H, op)
+        ctx = f"H={H} {p}"
+        assert p["threads"] == p["groups"] * p["group_threads"] + 32, ctx  # + producer warp
+        assert p["threads"] % 32 == 0, ctx
+        assert p["threads"] <= p["class_max_threads"], ctx
+        assert p["smem"] <= SMEM_PER_CTA, ctx
+        assert p["class_blocks_per_sm"] * (p["smem"] + 1024) <= SMEM_PER_SM, ctx
+        assert p["stages"] >= 2, ctx
+        assert p["group_threads"] * p["vpt"] * 8 >= H, ctx
+        assert p["group_threads"] in (8, 16) or p["group_threads"] % 32 == 0, ctx
+        if p["group_threads"] >= 32:
+            assert p["groups"] <= 16, ctx          # reduction slots
+        ring = p["stages"] * tensors * p["groups"] * H * 2
+        if op >= 2:
+            assert ring >= 8 * p["groups"] * H, ctx
+            assert p["vpt"] in (1, 2, 3, 4), ctx
+            if p["vpt"] == 3:
+                assert p["cls"] == 1, ctx      # 3-vector rows only in the multi-group build
+        else:
+            assert p["vpt"] in (1, 2, 3, 4), ctx
+            if p["cls"] == 1:
+                assert p["vpt"] >= 2, ctx      # the one-CTA forward is built for 2..4
+
+
+def test_launch_plan_rejects_bad_arguments(lib):
+    out = (C.c_int64 * 9)()
+    assert lib.rmsnorm_train_launch_plan(4096, 4, out, 9) == INVALID
+    assert lib.rmsnorm_train_launch_plan(4096, -1, out, 9) == INVALID
+    assert lib.rmsnorm_train_launch_plan(4100, 0, out, 9) == INVALID
+    assert lib.rmsnorm_train_launch_plan(0, 0, out, 9) == INVALID
+    assert lib.rmsnorm_train_launch_plan(8200, 0, out, 9) == UNSUPPORTED
+    assert lib.rmsnorm_train_launch_plan(4096, 0, None, 9) == INVALID
+    assert lib.rmsnorm_train_launch_plan(4096, 0, out, -1) == INVALID
+    assert lib.rmsnorm_train_launch_plan(4096, 0, out, 0) == OK

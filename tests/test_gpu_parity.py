@@ -57,9 +57,11 @@ def test_per_head_contiguous_4(T):
 
 
 @pytest.mark.parametrize("H,T", [(8, 3), (24, 33), (264, 17), (512, 130), (1000, 9),
-                                 (3072, 257), (6144, 2), (8192, 300)])
+                                 (2816, 65), (3072, 257), (5632, 33), (6144, 2), (7680, 19),
+                                 (8192, 300)])
 def test_other_widths_ragged(H, T):
-    # widths that leave lanes idle (H < 256, H/8 not a multiple of 32) and the largest H
+    # widths that leave lanes idle (H < 256, H/8 not a multiple of 32), rows whose exact
+    # split needs more than 256 threads (2816, 5632, 7680) and the largest H
     parity.run_case(synth.make_case(7, T, H, w_fp32=(H % 16 == 0), label=f"w{H}_T{T}"))
 
 
@@ -79,3 +81,28 @@ def test_extreme_row_scales(H, scale):
                         label=f"scale{scale:g}_H{H}")
     c.eps = float(np.float32(1e-30))
     parity.run_case(c)
+
+
+@pytest.mark.parametrize("H,T", [(4096, 67), (256, 1030)])
+def test_bwd_rstd_not_16_byte_aligned(H, T):
+    # rstd 4 bytes past a 16-byte boundary: the kernel stages it by 4-byte copies instead
+    # of whole 16-byte blocks; results are the aligned call's, bit for bit, and those are
+    # checked against the oracle
+    import torch
+    from rmsnorm_fwd_02_gb300 import _native as N
+    c = synth.make_case(3, T, H, w_fp32=True, label=f"rs_misaligned_H{H}")
+    parity.run_case(c, modes=(True,))
+    dc = parity.DeviceCase(c)
+    _, rstd, _ = parity.gpu_fwd(dc, False)
+    shifted = torch.empty(c.R + 4, dtype=torch.float32, device=parity.DEV)
+    shifted[1:c.R + 1] = rstd
+    rs_mis = shifted[1:c.R + 1]
+    assert rs_mis.data_ptr() % 16 == 4
+    outs = []
+    for r in (rstd, rs_mis):
+        dx, dw = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, r, True)
+        torch.cuda.synchronize()
+        outs.append((parity.bits_of(dx), dw.cpu().numpy()))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert N.rmsnorm_train_device_error(reset=True) == 0
