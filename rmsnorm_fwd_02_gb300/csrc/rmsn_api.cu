@@ -185,18 +185,24 @@ Shape fwd_shape(int H, bool residual) {
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
   // narrow rows: 2 vectors a lane in 8- or 16-lane groups; rows that 240 threads cover
-  // with 2 or 3 vectors each: several row groups in one CTA (kBwdMulti); wider rows:
-  // one group of 2-vector threads, or of 4-vector threads past H = 6144 (kBwdWide)
+  // with 2 or 3 vectors each: several row groups in one CTA (kBwdMulti), with the vector
+  // count that keeps the most threads busy on row data (measured: rows in flight decide
+  // this kernel's bandwidth); wider rows: one group of 2-vector threads, or of 4-vector
+  // threads past H = 6144 (kBwdWide)
   auto group = [nv](int v) { return ((nv + v - 1) / v + 31) / 32 * 32; };
+  auto busy = [&](int v) {  // threads with row data in a multi-group CTA, 0 if none fits
+    const int gt = group(v);
+    if (nv < 32 || gt > kMultiMaxGroup) return 0;
+    const int groups = kMultiConsumers / gt < 16 ? kMultiConsumers / gt : 16;
+    return groups * ((nv + v - 1) / v);
+  };
   int vpt;
   if (nv < 2)
     vpt = 1;
-  else if (group(2) <= kMultiMaxGroup)
-    vpt = 2;
-  else if (group(3) <= kMultiMaxGroup)
-    vpt = 3;
-  else
+  else if (busy(2) == 0 && busy(3) == 0)
     vpt = nv <= 768 ? 2 : 4;
+  else
+    vpt = busy(3) > busy(2) ? 3 : 2;
   return make_shape(H, with_dh ? 3 : 2, vpt, true);
 }
 
