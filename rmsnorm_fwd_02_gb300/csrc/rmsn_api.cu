@@ -50,7 +50,7 @@ uint64_t key(int dev, const void* fn, uint64_t extra) {
 
 size_t shared_bytes(const Shape& s, int H, bool bwd) {
   return smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0,
-                     bwd ? s.groups : 0).total;
+                     bwd ? s.groups : 0, bwd && bwd_w_in_smem(s.cls, s.vpt) ? H : 0).total;
 }
 
 // Column vectors per thread, from the instantiated set `allowed` (descending): the
@@ -64,7 +64,7 @@ int pick_vpt(int nv, std::initializer_list<int> allowed) {
   return 1;
 }
 
-Shape make_shape(int H, int tensors, int vpt, bool bwd) {
+Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true) {
   Shape s{};
   const int nv = H / 8;
   s.vpt = vpt;
@@ -77,7 +77,7 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd) {
     s.ntg = ((per + 31) / 32) * 32;
   }
   if (bwd) {
-    if ((vpt == 2 || vpt == 3) && s.ntg >= 32 && s.ntg <= kMultiMaxGroup)
+    if (allow_multi && vpt >= 2 && s.ntg >= 32 && s.ntg <= kMultiMaxGroup)
       s.cls = kBwdMulti;
     else if (vpt >= 2 && s.ntg >= 32)
       s.cls = kBwdWide;
@@ -196,14 +196,17 @@ Shape bwd_shape(int H, bool with_dh) {
     const int groups = kMultiConsumers / gt < 16 ? kMultiConsumers / gt : 16;
     return groups * ((nv + v - 1) / v);
   };
-  int vpt;
-  if (nv < 2)
-    vpt = 1;
-  else if (busy(2) == 0 && busy(3) == 0)
-    vpt = nv <= 768 ? 2 : 4;
-  else
-    vpt = busy(3) > busy(2) ? 3 : 2;
-  return make_shape(H, with_dh ? 3 : 2, vpt, true);
+  const int tensors = with_dh ? 3 : 2;
+  if (nv < 2) return make_shape(H, tensors, 1, true);
+  if (busy(2) > 0 || busy(3) > 0) return make_shape(H, tensors, busy(3) > busy(2) ? 3 : 2, true);
+  // past 3 x 240 vectors: 4-vector threads in two row groups of up to 240 (H up to 7680)
+  // while the ring still holds three stages of them (measured: with two stages the ring
+  // runs dry, and one wide group does better), else one wide group
+  if (busy(4) > 0) {
+    const Shape s = make_shape(H, tensors, 4, true);
+    if (s.stages >= 3) return s;
+  }
+  return make_shape(H, tensors, nv <= 768 ? 2 : 4, true, /*allow_multi=*/false);
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem) {
@@ -329,7 +332,9 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
     return 0;
   const int64_t R = T * static_cast<int64_t>(nh);
   if (R == 0) return 0;
-  const Shape s = bwd_shape(H, false);  // partial count does not depend on dh
+  // the launch shape (so the partial count) may differ with and without dh: one size
+  // serves both
+  const Shape s = bwd_shape(H, false);
   int dev = 0;
   if (!deterministic) {
     if (current_device(&dev) != RMSN_OK || device_setup(dev) != RMSN_OK) return 0;
@@ -337,7 +342,10 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
   // the partition count of the non-deterministic mode is the larger of the two weight
   // dtypes' occupancies, so one size serves both
   int P = bwd_partials(static_cast<int32_t>(R), s, deterministic != 0, dev, false);
-  if (!deterministic) {
+  if (deterministic) {
+    const int Pd = bwd_partials(static_cast<int32_t>(R), bwd_shape(H, true), true, dev, false);
+    if (Pd > P) P = Pd;
+  } else {
     int P2 = bwd_partials(static_cast<int32_t>(R), s, false, dev, true);
     if (P2 > P) P = P2;
     const Shape sd = bwd_shape(H, true);

@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const int NW = NTg >> 5;
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
   const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
-  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0, G);
+  constexpr bool kWSmem = bwd_w_in_smem(kCls, VPT);
+  const SmemLayout L = smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -138,18 +139,45 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
-  f2 wv[VPT][4];
+  f2 wv[kWSmem ? 1 : VPT][4];  // the weight of this thread's columns (registers)
   f2 acc[VPT][4], cmp[VPT][4];
+  float* wsm = reinterpret_cast<float*>(smem + L.w);  // or FP32 in shared memory
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
-    if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
+    if constexpr (!kWSmem) {
+      if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
+    }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       acc[v][q] = f2_splat(0.f);
       cmp[v][q] = f2_splat(0.f);
     }
   }
+  if constexpr (kWSmem) {
+    for (int c = tid; c < NV; c += ncons) {
+      f2 p[4];
+      load_w8_pairs<kFp32W>(a.w, c, p);
+      float4* d = reinterpret_cast<float4*>(wsm) + 2 * c;
+      d[0] = make_float4(f2_lo(p[0]), f2_hi(p[0]), f2_lo(p[1]), f2_hi(p[1]));
+      d[1] = make_float4(f2_lo(p[2]), f2_hi(p[2]), f2_lo(p[3]), f2_hi(p[3]));
+    }
+    named_bar_sync(14, ncons);
+  }
+  // this thread's weight pairs for column vector c (its v-th)
+  auto wvec = [&](int v, int c, f2 (&p)[4]) {
+    if constexpr (kWSmem) {
+      const float4 a4 = reinterpret_cast<const float4*>(wsm)[2 * c];
+      const float4 b4 = reinterpret_cast<const float4*>(wsm)[2 * c + 1];
+      p[0] = f2_make(a4.x, a4.y);
+      p[1] = f2_make(a4.z, a4.w);
+      p[2] = f2_make(b4.x, b4.y);
+      p[3] = f2_make(b4.z, b4.w);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) p[q] = wv[v][q];
+    }
+  };
   const float inv_h = 1.0f / static_cast<float>(H);
   // Rows of this warp's first group: every lane of a warp runs the same iterations (the
   // shuffles need them all); groups past the chunk's end skip the row work.
@@ -177,9 +205,11 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
           if (c < NV) {
             const uint4 xv = lds128(st + c * 8);
             const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+            f2 wl[4];
+            wvec(v, c, wl);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wv[v][q]);
+              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wl[q]);
               if (q & 1)
                 dot1 = f2_fma(gw, bf2_to_f2(u4_get(xv, q)), dot1);
               else
@@ -235,12 +265,14 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
             const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
             uint4 hv = make_uint4(0u, 0u, 0u, 0u);
             if constexpr (kDh) hv = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+            f2 wl[4];
+            wvec(v, c, wl);
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const f2 x2 = bf2_to_f2(u4_get(xv, q));
               const f2 d2 = bf2_to_f2(u4_get(dv, q));
-              const f2 gw = f2_mul(d2, wv[v][q]);
+              const f2 gw = f2_mul(d2, wl[q]);
               f2 d = f2_mul(f2_fma(x2, ncr2, gw), rs2);  // (g - xhat*c) * rstd
               if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
               o[q] = f2_to_bf2(d);
@@ -395,6 +427,7 @@ static const void* pick_bwd(const Shape& s, bool fp32w, bool dh) {
     return pick_bwd_v<2, kBwdNarrow>(fp32w, dh);
   }
   if (s.vpt == 3) return pick_bwd_v<3, kBwdMulti>(fp32w, dh);
+  if (s.cls == kBwdMulti) return pick_bwd_v<4, kBwdMulti>(fp32w, dh);
   return pick_bwd_v<4, kBwdWide>(fp32w, dh);
 }
 

@@ -21,6 +21,7 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 //   slots  [kRedBufs][groups][32] FP32 per-warp reduction partials
 //   rs     [stages][rs_stride(rs_rows)] FP32: the staged rows' rstd (backward; forward:
 //          none), from the 16-byte block holding the stage's first row onwards
+//   w      [w_floats] FP32 weight, for builds that keep it in shared memory
 //   abort  CTA abort flag of the bounded waits
 //
 // Row j's reduction uses buffer j % kRedBufs.  A warp writes buffer j in phase A(j) after
@@ -29,7 +30,7 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 // same ordering keeps each redb barrier within one phase of its waiters.
 constexpr int kRedBufs = 4;
 struct SmemLayout {
-  size_t full, empty, redb, slots, rs, abort_flag, total;
+  size_t full, empty, redb, slots, rs, w, abort_flag, total;
 };
 
 // Floats per stage of the staged rstd: the stage's `rows` values start up to 3 floats
@@ -40,7 +41,8 @@ __host__ __device__ constexpr int rs_stride(int rows) { return rows == 0 ? 0 : (
 // when a group spans whole warps, none when groups are sub-warp (shuffles only).
 // `rs_rows` is the number of rstd values staged with each stage (the backward's groups).
 __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int groups, int H,
-                                                  int red_groups, int rs_rows) {
+                                                  int red_groups, int rs_rows,
+                                                  int w_floats = 0) {
   SmemLayout L;
   size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
   L.full = off;
@@ -54,6 +56,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int g
   off += 4 * kRedBufs * 32 * static_cast<size_t>(red_groups);
   L.rs = off;  // 128-byte aligned
   off += 4 * static_cast<size_t>(stages) * rs_stride(rs_rows);
+  L.w = off;   // 16-byte aligned
+  off += 4 * static_cast<size_t>(w_floats);
   L.abort_flag = off;
   off += 16;
   L.total = off;
@@ -119,10 +123,15 @@ cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
+// Backward builds that keep the weight in shared memory (FP32, H floats) instead of
+// registers: 4-vector threads of the multi-group class.
+__host__ __device__ constexpr bool bwd_w_in_smem(int cls, int vpt) { return cls == 1 && vpt == 4; }
+
 // Backward shape classes, each its own kernel build:
 //  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector threads and sub-warp groups
-//  kBwdMulti   2- or 3-vector threads in row groups of 32..240 threads, as many groups as
-//              fit in 480 consumers, one CTA an SM: several rows in flight per CTA.  With
+//  kBwdMulti   2- to 4-vector threads in row groups of 32..240 threads, as many groups
+//              as fit in 480 consumers, one CTA an SM: several rows in flight per CTA
+//              (4-vector threads keep the weight in shared memory, not registers).  With
 //              the producer that is 16 warps, four a scheduler partition, which leaves
 //              128 registers a thread (17 warps would put five warps on one partition
 //              and cap every thread at 96, too few for the dw state without spills)

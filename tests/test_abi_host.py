@@ -185,3 +185,18 @@ def test_launch_plan_rejects_bad_arguments(lib):
     assert lib.rmsnorm_train_launch_plan(4096, 0, None, 9) == INVALID
     assert lib.rmsnorm_train_launch_plan(4096, 0, out, -1) == INVALID
     assert lib.rmsnorm_train_launch_plan(4096, 0, out, 0) == OK
+
+
+def test_deterministic_workspace_covers_both_dh_plans(lib):
+    # The backward's launch shape may differ with and without dh (the workspace query has
+    # no dh argument): the size must cover the larger deterministic partition, which is
+    # min(ceil(R / (groups * 4)), 152 * CTAs an SM) partials of 2*H floats.
+    from rmsnorm_fwd_02_gb300 import _native as N
+    for H in (256, 768, 1536, 4096, 5120, 5632, 6144, 7168, 8192):
+        for T in (1, 96, 700, 65536):
+            need = 0
+            for op in (2, 3):
+                p = N.rmsnorm_train_launch_plan(H, op)
+                P = min(-(-T // (p["groups"] * 4)), 152 * p["class_blocks_per_sm"])
+                need = max(need, P * 2 * H * 4)
+            assert lib.rmsnorm_train_bwd_workspace_bytes(T, 1, H, 1) == need, (H, T)
