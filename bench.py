@@ -508,10 +508,17 @@ SWEEP = [
 
 
 def run_sweep(args):
-    """Times each op of each workload: `reps` launches, each after an L2 flush outside the
-    events, CUDA events on the launch stream, trimmed mean.  The flush READS a 512 MiB buffer,
-    so L2 is cold but clean: a write-based flush would leave dirty lines whose write-back
-    lands inside the next timed kernel."""
+    """Times each op of each workload two ways, CUDA events on the launch stream:
+
+    isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
+              The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
+              flush would leave dirty lines whose write-back lands inside the next timed
+              kernel).  Includes the launch's ramp-up and tail and the gap before the first
+              CTA starts.
+    stream    `reps` launches back to back inside one event pair, rotating over copies of
+              the inputs and outputs so that every launch finds its inputs out of L2 (the
+              sets in between exceed twice the L2); time / launches.  This is the op as a
+              training step runs it, queued behind other work."""
     import torch
     from rmsnorm_fwd_02_gb300 import _native as N
     from rmsnorm_fwd_02_gb300 import synth
@@ -523,6 +530,7 @@ def run_sweep(args):
     lib = N.lib()
     flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peak()
+    l2_bytes = 129 << 20
 
     def dbf(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -530,13 +538,13 @@ def run_sweep(args):
     def timed(fn, reps):
         out = []
         for _ in range(3):
-            fn()
+            fn(0)
         for _ in range(reps):
             flush.sum()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            fn()
+            fn(0)
             b.record(stream)
             torch.cuda.synchronize()
             out.append(a.elapsed_time(b) * 1e3)
@@ -546,6 +554,20 @@ def run_sweep(args):
         cut = len(out) // 10
         return statistics.fmean(out[cut:len(out) - cut])
 
+    def timed_stream(fn, nsets, reps):
+        n = max(reps, 2 * nsets)
+        for i in range(nsets):
+            fn(i)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            fn(i % nsets)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / n
+
     for label, T, H, nh, bh, w32, res in SWEEP:
         if args.sweep_filter and args.sweep_filter != f"{label}_{T}_{H}":
             continue
@@ -553,24 +575,33 @@ def run_sweep(args):
         R = c.R
         wbytes = 4 if w32 else 2
         wd = 1 if w32 else 0
-        x, dy, w = dbf(c.x), dbf(c.dy), (torch.from_numpy(c.w).to(dev) if w32 else dbf(c.w))
-        rr = dbf(c.residual) if res else None
-        dh = dbf(c.dh) if res else None
-        y = torch.empty(R * H, dtype=torch.bfloat16, device=dev)
-        h = torch.empty_like(y) if res else None
-        dx = torch.empty_like(y)
-        rstd = torch.empty(R, dtype=torch.float32, device=dev)
-        dw = torch.empty(H, dtype=torch.float32, device=dev)
+        base = {"x": dbf(c.x), "dy": dbf(c.dy)}
+        if res:
+            base["rr"], base["dh"] = dbf(c.residual), dbf(c.dh)
+        w = torch.from_numpy(c.w).to(dev) if w32 else dbf(c.w)
+        set_bytes = sum(t.numel() * t.element_size() for t in base.values()) + 3 * R * H * 2
+        nsets = max(2, -(-2 * l2_bytes // set_bytes) + 1)
+        sets = []
+        for i in range(nsets):
+            st = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+            st["y"] = torch.empty(R * H, dtype=torch.bfloat16, device=dev)
+            st["h"] = torch.empty_like(st["y"]) if res else None
+            st["dx"] = torch.empty_like(st["y"])
+            st["rstd"] = torch.empty(R, dtype=torch.float32, device=dev)
+            st["dw"] = torch.empty(H, dtype=torch.float32, device=dev)
+            sets.append(st)
 
-        def fwd():
-            st = lib.rmsnorm_train_fwd(x.data_ptr(), rr.data_ptr() if res else None,
-                                       w.data_ptr(), wd, y.data_ptr(),
-                                       h.data_ptr() if res else None, rstd.data_ptr(), T, nh,
-                                       H, c.s_tok, c.s_head, 1e-6, sh)
+        def fwd(i):
+            q = sets[i]
+            st = lib.rmsnorm_train_fwd(q["x"].data_ptr(), q["rr"].data_ptr() if res else None,
+                                       w.data_ptr(), wd, q["y"].data_ptr(),
+                                       q["h"].data_ptr() if res else None,
+                                       q["rstd"].data_ptr(), T, nh, H, c.s_tok, c.s_head,
+                                       1e-6, sh)
             assert st == 0, st
 
-        fwd()
-        xs = h if res else x
+        for i in range(nsets):
+            fwd(i)
         s_tok, s_head = (nh * H, H) if res else (c.s_tok, c.s_head)
         rows = [("fwd", fwd, (8 if res else 4) * R * H + 4 * R + wbytes * H)]
         for det in (1, 0):
@@ -578,12 +609,15 @@ def run_sweep(args):
                 nws = N.rmsnorm_train_bwd_workspace_bytes(T, nh, H, det)
                 ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
 
-                def bwd(det=det, use_dh=use_dh, ws=ws, nws=nws):
-                    st = lib.rmsnorm_train_bwd(xs.data_ptr(), dy.data_ptr(),
-                                               dh.data_ptr() if use_dh else None,
-                                               rstd.data_ptr(), w.data_ptr(), wd,
-                                               dx.data_ptr(), dw.data_ptr(), ws.data_ptr(),
-                                               nws, T, nh, H, s_tok, s_head, det, sh)
+                def bwd(i, det=det, use_dh=use_dh, ws=ws, nws=nws):
+                    q = sets[i]
+                    xs = q["h"] if res else q["x"]
+                    st = lib.rmsnorm_train_bwd(xs.data_ptr(), q["dy"].data_ptr(),
+                                               q["dh"].data_ptr() if use_dh else None,
+                                               q["rstd"].data_ptr(), w.data_ptr(), wd,
+                                               q["dx"].data_ptr(), q["dw"].data_ptr(),
+                                               ws.data_ptr(), nws, T, nh, H, s_tok, s_head,
+                                               det, sh)
                     assert st == 0, st
 
                 name = ("bwd_det" if det else "bwd_nondet") + ("+dh" if use_dh else "")
@@ -591,13 +625,17 @@ def run_sweep(args):
                              + 4 * H))
         for name, fn, nbytes in rows:
             us = timed(fn, args.sweep_reps)
+            us_s = timed_stream(fn, nsets, args.sweep_reps)
             gbs = nbytes / (us * 1e-6) / 1e9
+            gbs_s = nbytes / (us_s * 1e-6) / 1e9
             print(json.dumps({"sweep": label, "op": name, "T": T, "H": H, "nh": nh,
                               "w": "fp32" if w32 else "bf16", "us": round(us, 2),
                               "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "stream_us": round(us_s, 2), "stream_GBps": round(gbs_s, 1),
+                              "stream_frac": round(gbs_s / peak, 4), "input_sets": nsets,
                               "peak": peak, "peak_kind": peak_kind,
                               "bytes": nbytes}), flush=True)
-        del x, dy, w, y, dx, rstd, dw, h, rr, dh
+        del sets, base, w
         torch.cuda.empty_cache()
     return 0
 

@@ -77,7 +77,7 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true)
     s.ntg = ((per + 31) / 32) * 32;
   }
   if (bwd) {
-    if (allow_multi && vpt >= 2 && s.ntg >= 32 && s.ntg <= kMultiMaxGroup)
+    if (allow_multi && vpt >= 2 && s.ntg <= kMultiMaxGroup)
       s.cls = kBwdMulti;
     else if (vpt >= 2 && s.ntg >= 32)
       s.cls = kBwdWide;
@@ -184,16 +184,19 @@ Shape fwd_shape(int H, bool residual) {
 }
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
-  // narrow rows: 2 vectors a lane in 8- or 16-lane groups; rows that 240 threads cover
-  // with 2 or 3 vectors each: several row groups in one CTA (kBwdMulti), with the vector
-  // count that keeps the most threads busy on row data (measured: rows in flight decide
-  // this kernel's bandwidth); wider rows: one group of 2-vector threads, or of 4-vector
-  // threads past H = 6144 (kBwdWide)
-  auto group = [nv](int v) { return ((nv + v - 1) / v + 31) / 32 * 32; };
+  // rows that 240 threads cover with 2 or 3 vectors each (narrow rows in 8- or 16-lane
+  // groups): several row groups in one CTA (kBwdMulti), with the vector count that keeps
+  // the most threads busy on row data (measured: rows in flight decide this kernel's
+  // bandwidth); wider rows: see below; H = 8: one-vector lanes, two CTAs an SM
+  // (kBwdNarrow)
+  auto group = [nv](int v) {  // threads a row group takes (8, 16 or whole warps)
+    const int per = (nv + v - 1) / v;
+    return per <= 8 ? 8 : (per <= 16 ? 16 : (per + 31) / 32 * 32);
+  };
   auto busy = [&](int v) {  // threads with row data in a multi-group CTA, 0 if none fits
     const int gt = group(v);
-    if (nv < 32 || gt > kMultiMaxGroup) return 0;
-    const int groups = kMultiConsumers / gt < 16 ? kMultiConsumers / gt : 16;
+    if (gt > kMultiMaxGroup) return 0;
+    const int groups = (gt < 32 || kMultiConsumers / gt < 16) ? kMultiConsumers / gt : 16;
     return groups * ((nv + v - 1) / v);
   };
   const int tensors = with_dh ? 3 : 2;

@@ -128,9 +128,10 @@ cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStr
 __host__ __device__ constexpr bool bwd_w_in_smem(int cls, int vpt) { return cls == 1 && vpt == 4; }
 
 // Backward shape classes, each its own kernel build:
-//  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector threads and sub-warp groups
-//  kBwdMulti   2- to 4-vector threads in row groups of 32..240 threads, as many groups
-//              as fit in 480 consumers, one CTA an SM: several rows in flight per CTA
+//  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector lanes (H = 8)
+//  kBwdMulti   2- to 4-vector threads in row groups of 8, 16 or 32..240 threads, as many
+//              groups as fit in 480 consumers (at most 16 whole-warp groups), one CTA an
+//              SM: several rows in flight per CTA
 //              (4-vector threads keep the weight in shared memory, not registers).  With
 //              the producer that is 16 warps, four a scheduler partition, which leaves
 //              128 registers a thread (17 warps would put five warps on one partition

@@ -124,10 +124,10 @@ def test_deterministic_workspace_size_depends_on_shape_only(lib):
     assert f(65, 1, 4096, 1) == 9 * 2 * 4096 * 4
     # H = 6144: 384 consumers, one CTA an SM -> at most 152
     assert f(65536, 1, 6144, 1) == 152 * 2 * 6144 * 4
-    # H = 256: 16 two-row-a-warp groups (16 rows a stage), two CTAs an SM -> at most 304
+    # H = 256: 30 two-row-a-warp groups (30 rows a stage), one CTA an SM -> at most 152
     assert f(64, 1, 256, 1) == 1 * 2 * 256 * 4
-    assert f(65, 1, 256, 1) == 2 * 2 * 256 * 4
-    assert f(65536, 24, 256, 1) == 304 * 2 * 256 * 4
+    assert f(121, 1, 256, 1) == 2 * 2 * 256 * 4
+    assert f(65536, 24, 256, 1) == 152 * 2 * 256 * 4
     # H = 8192: 4-vector threads, one CTA an SM
     assert f(131072, 1, 8192, 1) == 152 * 2 * 8192 * 4
     assert f(0, 1, 4096, 1) == 0
