@@ -201,7 +201,17 @@ Shape bwd_shape(int H, bool with_dh) {
   };
   const int tensors = with_dh ? 3 : 2;
   if (nv < 2) return make_shape(H, tensors, 1, true);
-  if (busy(2) > 0 || busy(3) > 0) return make_shape(H, tensors, busy(3) > busy(2) ? 3 : 2, true);
+  if (busy(2) > 0 || busy(3) > 0) {
+    const int v = busy(3) > busy(2) ? 3 : 2;
+    // 4-vector threads (weight in shared memory) when they keep at least 5 % more threads
+    // busy and the ring still holds three stages (measured: H = 3072 and 4096 gain,
+    // H = 2048, 4 % more, loses a little)
+    if (20 * busy(4) >= 21 * busy(v)) {
+      const Shape s4 = make_shape(H, tensors, 4, true);
+      if (s4.stages >= 3) return s4;
+    }
+    return make_shape(H, tensors, v, true);
+  }
   // past 3 x 240 vectors: 4-vector threads in two row groups of up to 240 (H up to 7680)
   // while the ring still holds three stages of them (measured: with two stages the ring
   // runs dry, and one wide group does better), else one wide group

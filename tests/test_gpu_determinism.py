@@ -103,10 +103,18 @@ def test_workspace_too_small_is_rejected():
     dx = torch.empty(c.R * c.H, dtype=torch.bfloat16, device="cuda")
     dw = torch.empty(c.H, dtype=torch.float32, device="cuda")
     rstd = torch.ones(c.R, device="cuda")
-    with pytest.raises(N.RmsnError) as ei:
-        N.rmsnorm_train_bwd(dc.x, dc.dy, None, rstd, dc.w, N.RMSN_W_BF16, dx, dw, ws,
-                            need - 16, c.T, 1, c.H, c.H, c.H, True)
-    assert ei.value.status == 3
+    # the query covers both launch shapes (with and without dh); here the dh shape needs
+    # all of it, and any call needs more than 16 bytes
+    for dh, nbytes in ((dc.dy, need - 16), (None, 16)):
+        with pytest.raises(N.RmsnError) as ei:
+            N.rmsnorm_train_bwd(dc.x, dc.dy, dh, rstd, dc.w, N.RMSN_W_BF16, dx, dw, ws,
+                                nbytes, c.T, 1, c.H, c.H, c.H, True)
+        assert ei.value.status == 3
+    for dh in (dc.dy, None):   # the queried size is accepted either way
+        N.rmsnorm_train_bwd(dc.x, dc.dy, dh, rstd, dc.w, N.RMSN_W_BF16, dx, dw, ws, need,
+                            c.T, 1, c.H, c.H, c.H, True)
+    torch.cuda.synchronize()
+    assert N.rmsnorm_train_device_error(reset=True) == 0
 
 
 def test_autograd_wrapper_matches_direct_calls():
