@@ -158,17 +158,19 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     for (int c = tid; c < NV; c += ncons) {
       f2 p[4];
       load_w8_pairs<kFp32W>(a.w, c, p);
-      float4* d = reinterpret_cast<float4*>(wsm) + 2 * c;
-      d[0] = make_float4(f2_lo(p[0]), f2_hi(p[0]), f2_lo(p[1]), f2_hi(p[1]));
-      d[1] = make_float4(f2_lo(p[2]), f2_hi(p[2]), f2_lo(p[3]), f2_hi(p[3]));
+      // two planes of float4 (columns 0-3 and 4-7 of each vector), so that a warp's
+      // reads of one plane are contiguous and free of bank conflicts
+      float4* d = reinterpret_cast<float4*>(wsm);
+      d[c] = make_float4(f2_lo(p[0]), f2_hi(p[0]), f2_lo(p[1]), f2_hi(p[1]));
+      d[NV + c] = make_float4(f2_lo(p[2]), f2_hi(p[2]), f2_lo(p[3]), f2_hi(p[3]));
     }
     named_bar_sync(14, ncons);
   }
   // this thread's weight pairs for column vector c (its v-th)
   auto wvec = [&](int v, int c, f2 (&p)[4]) {
     if constexpr (kWSmem) {
-      const float4 a4 = reinterpret_cast<const float4*>(wsm)[2 * c];
-      const float4 b4 = reinterpret_cast<const float4*>(wsm)[2 * c + 1];
+      const float4 a4 = reinterpret_cast<const float4*>(wsm)[c];
+      const float4 b4 = reinterpret_cast<const float4*>(wsm)[NV + c];
       p[0] = f2_make(a4.x, a4.y);
       p[1] = f2_make(a4.z, a4.w);
       p[2] = f2_make(b4.x, b4.y);
