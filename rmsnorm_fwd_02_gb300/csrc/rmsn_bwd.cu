@@ -325,27 +325,35 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   // free once every consumer is past its loop: each stage was waited on (full) by every
   // group that had a row in it before that group finished.
   named_bar_sync(15, ncons);
-  float* cb = reinterpret_cast<float*>(smem);  // [G][2][H]
+  // cb: [G][2][H] (hi, lo), each H-slab stored as two planes of float4 (columns 0-3 and
+  // 4-7 of every vector) so that a warp's stores of one plane are contiguous
+  float* cb = reinterpret_cast<float*>(smem);
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
     if (c < NV) {
+      f2 hi[4], lo[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const f2 hi = f2_add(acc[v][q], cmp[v][q]);
-        const f2 lo = f2_sub(cmp[v][q], f2_sub(hi, acc[v][q]));
-        *reinterpret_cast<unsigned long long*>(cb + (2 * g) * H + c * 8 + 2 * q) = hi.v;
-        *reinterpret_cast<unsigned long long*>(cb + (2 * g + 1) * H + c * 8 + 2 * q) = lo.v;
+        hi[q] = f2_add(acc[v][q], cmp[v][q]);
+        lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
       }
+      ulonglong2* ph = reinterpret_cast<ulonglong2*>(cb + (2 * g) * H);
+      ulonglong2* pl = reinterpret_cast<ulonglong2*>(cb + (2 * g + 1) * H);
+      ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
+      ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
+      pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
+      pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
     }
   }
   named_bar_sync(15, ncons);
   for (int col = tid; col < H; col += ncons) {
+    const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
     float sacc = 0.f, e = 0.f;
     for (int gi = 0; gi < G; ++gi) {
       float err;
-      sacc = two_sum(sacc, cb[(2 * gi) * H + col], err);
-      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + col]));
+      sacc = two_sum(sacc, cb[(2 * gi) * H + at], err);
+      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + at]));
     }
     const float hi = __fadd_rn(sacc, e);
     part[col] = hi;
