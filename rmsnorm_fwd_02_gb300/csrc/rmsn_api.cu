@@ -184,29 +184,31 @@ Shape fwd_shape(int H, bool residual) {
 }
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
-  // rows that 240 threads cover with 2 or 3 vectors each (narrow rows in 8- or 16-lane
-  // groups): several row groups in one CTA (kBwdMulti), with the vector count that keeps
-  // the most threads busy on row data (measured: rows in flight decide this kernel's
-  // bandwidth); wider rows: see below; H = 8: one-vector lanes, two CTAs an SM
-  // (kBwdNarrow)
+  // rows that 240 threads cover with 2 to 4 vectors each (narrow rows in 8- or 16-lane
+  // groups): several row groups in one CTA (kBwdMulti); wider rows: see below; H = 8:
+  // one-vector lanes, two CTAs an SM (kBwdNarrow)
   auto group = [nv](int v) {  // threads a row group takes (8, 16 or whole warps)
     const int per = (nv + v - 1) / v;
     return per <= 8 ? 8 : (per <= 16 ? 16 : (per + 31) / 32 * 32);
   };
-  auto busy = [&](int v) {  // threads with row data in a multi-group CTA, 0 if none fits
+  auto groups = [&](int v) {  // row groups of a multi-group CTA, 0 if a row does not fit
     const int gt = group(v);
     if (gt > kMultiMaxGroup) return 0;
-    const int groups = (gt < 32 || kMultiConsumers / gt < 16) ? kMultiConsumers / gt : 16;
-    return groups * ((nv + v - 1) / v);
+    return (gt < 32 || kMultiConsumers / gt < 16) ? kMultiConsumers / gt : 16;
   };
+  auto busy = [&](int v) { return groups(v) * ((nv + v - 1) / v); };  // threads with data
   const int tensors = with_dh ? 3 : 2;
   if (nv < 2) return make_shape(H, tensors, 1, true);
-  if (busy(2) > 0 || busy(3) > 0) {
-    const int v = busy(3) > busy(2) ? 3 : 2;
-    // 4-vector threads (weight in shared memory) when they keep at least 5 % more threads
-    // busy and the ring still holds three stages (measured: H = 3072 and 4096 gain,
-    // H = 2048, 4 % more, loses a little)
-    if (20 * busy(4) >= 21 * busy(v)) {
+  if (groups(2) > 0 || groups(3) > 0) {
+    // the vector count with the most rows in flight, then the most threads busy with row
+    // data (measured: rows in flight decide this kernel's bandwidth -- H = 1536 gains 7 %
+    // with 7 two-warp rows over 5 three-warp rows); 4-vector threads (weight in shared
+    // memory) only while the ring still holds three stages of them
+    auto better = [&](int u, int v) {
+      return groups(u) != groups(v) ? groups(u) > groups(v) : busy(u) > busy(v);
+    };
+    const int v = better(3, 2) ? 3 : 2;
+    if (groups(4) > 0 && better(4, v)) {
       const Shape s4 = make_shape(H, tensors, 4, true);
       if (s4.stages >= 3) return s4;
     }
