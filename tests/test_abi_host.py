@@ -117,16 +117,17 @@ def test_bwd_rejects_before_any_cuda_call(lib, kw, want):
 
 def test_deterministic_workspace_size_depends_on_shape_only(lib):
     f = lib.rmsnorm_train_bwd_workspace_bytes
-    # H = 4096: two row groups of 2-vector threads in one CTA an SM -> at most 152
-    # partials of 2*H floats; a CTA takes at least 4 stages (8 rows)
+    # H = 4096: one CTA an SM -> at most 152 partials of 2*H floats; a CTA takes at least
+    # one stage (3 rows without dh, 2 with: the larger need, 2 rows, sets the size)
     assert f(65536, 1, 4096, 1) == 152 * 2 * 4096 * 4
     assert f(1, 1, 4096, 1) == 1 * 2 * 4096 * 4
-    assert f(65, 1, 4096, 1) == 9 * 2 * 4096 * 4
+    assert f(65, 1, 4096, 1) == 33 * 2 * 4096 * 4
     # H = 6144: 384 consumers, one CTA an SM -> at most 152
     assert f(65536, 1, 6144, 1) == 152 * 2 * 6144 * 4
-    # H = 256: 30 two-row-a-warp groups (30 rows a stage), one CTA an SM -> at most 152
-    assert f(64, 1, 256, 1) == 1 * 2 * 256 * 4
-    assert f(121, 1, 256, 1) == 2 * 2 * 256 * 4
+    # H = 256: 60 eight-lane groups without dh, 30 sixteen-lane groups with (30 rows a
+    # stage), one CTA an SM -> at most 152
+    assert f(30, 1, 256, 1) == 1 * 2 * 256 * 4
+    assert f(31, 1, 256, 1) == 2 * 2 * 256 * 4
     assert f(65536, 24, 256, 1) == 152 * 2 * 256 * 4
     # H = 8192: 4-vector threads, one CTA an SM
     assert f(131072, 1, 8192, 1) == 152 * 2 * 8192 * 4
@@ -190,13 +191,14 @@ def test_launch_plan_rejects_bad_arguments(lib):
 def test_deterministic_workspace_covers_both_dh_plans(lib):
     # The backward's launch shape may differ with and without dh (the workspace query has
     # no dh argument): the size must cover the larger deterministic partition, which is
-    # min(ceil(R / (groups * 4)), 152 * CTAs an SM) partials of 2*H floats.
+    # min(ceil(R / groups), 152 * CTAs an SM) partials of 2*H floats (a CTA takes at least
+    # one stage of rows).
     from rmsnorm_fwd_02_gb300 import _native as N
     for H in (256, 768, 1536, 4096, 5120, 5632, 6144, 7168, 8192):
         for T in (1, 96, 700, 65536):
             need = 0
             for op in (2, 3):
                 p = N.rmsnorm_train_launch_plan(H, op)
-                P = min(-(-T // (p["groups"] * 4)), 152 * p["class_blocks_per_sm"])
+                P = min(-(-T // p["groups"]), 152 * p["class_blocks_per_sm"])
                 need = max(need, P * 2 * H * 4)
             assert lib.rmsnorm_train_bwd_workspace_bytes(T, 1, H, 1) == need, (H, T)
