@@ -508,7 +508,9 @@ SWEEP = [
 
 
 def run_sweep(args):
-    """Times each op of each workload two ways, CUDA events on the launch stream:
+    """Times each op of each workload (forward; backward in both modes, with and without dh
+    in the residual form; the checkpointed step 2xfwd+bwd = forward, forward recompute,
+    deterministic backward) two ways, CUDA events on the launch stream:
 
     isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
               The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
@@ -621,8 +623,16 @@ def run_sweep(args):
                     assert st == 0, st
 
                 name = ("bwd_det" if det else "bwd_nondet") + ("+dh" if use_dh else "")
-                rows.append((name, bwd, (8 if use_dh else 6) * R * H + 4 * R + wbytes * H
-                             + 4 * H))
+                bwd_bytes_ = (8 if use_dh else 6) * R * H + 4 * R + wbytes * H + 4 * H
+                rows.append((name, bwd, bwd_bytes_))
+                if det and not use_dh:
+                    # the checkpointed step: forward, forward recompute, backward
+                    def ckpt(i, bwd=bwd):
+                        fwd(i)
+                        fwd(i)
+                        bwd(i)
+
+                    rows.append(("2xfwd+bwd_det", ckpt, 2 * rows[0][2] + bwd_bytes_))
         for name, fn, nbytes in rows:
             us = timed(fn, args.sweep_reps)
             us_s = timed_stream(fn, nsets, args.sweep_reps)

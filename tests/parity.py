@@ -173,10 +173,22 @@ def report(rec: dict):
             f.write(json.dumps(rec) + "\n")
 
 
-def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=False):
+def eager_fp32_dw(xs_dev, dy_dev, r_dev, c, s_tok, s_head):
+    """dw the plain FP32 way (torch on the GPU: x*rstd, times dy, summed over rows by
+    torch's reduction): the pages' FP32 eager reference, whose worst dw error a kernel's
+    must not exceed."""
+    R, H = c.R, c.H
+    x = torch.as_strided(xs_dev, (c.T, c.nh, H), (s_tok, s_head, 1)).reshape(R, H).float()
+    xhat = x * r_dev.view(R, 1)
+    return (dy_dev.view(R, H).float() * xhat).sum(dim=0)
+
+
+def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=False,
+             check_eager=False):
     """Forward + backward of `case` on the GPU against the oracle.  Rows beyond
     `full_rows_limit` elements are sampled for y / h / dx; rstd and dw are checked in
-    full.  Returns a dict of the worst figures."""
+    full.  With check_eager, each mode's worst dw error must also be at most the FP32
+    eager reference's.  Returns a dict of the worst figures."""
     c = case
     R, H = c.R, c.H
     residual = c.residual is not None
@@ -219,6 +231,11 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
     xrows = gather_rows(xs_bits, c, sel) if not residual else xs_bits.reshape(R, H)[sel]
     tol = dx_cancel_tol(xrows, c.dy.reshape(R, H)[sel], c.w, r_in[sel], H,
                         dh_bits=c.dh.reshape(R, H)[sel] if with_dh else None)
+    eager_err = None
+    if check_eager:
+        dw_e = eager_fp32_dw(xs_dev, dc.dy, r_dev, c, s_tok, s_head).cpu().numpy()
+        eager_err = float(np.abs(dw_e.astype(np.float64) - dw64).max())
+        out["dw_eager_fp32_max_err"] = eager_err
     dws = {}
     for det in modes:
         dx, dw = gpu_bwd(dc, xs_dev, s_tok, s_head, r_dev, det, with_dh=with_dh)
@@ -229,6 +246,11 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
         ratio = check_dw(dw.cpu().numpy(), dw64)
         dws[det] = (dxb, dw.cpu().numpy())
         key = "det" if det else "nondet"
+        if eager_err is not None:
+            err = float(np.abs(dw.cpu().numpy().astype(np.float64) - dw64).max())
+            out[f"dw_max_err_{key}"] = err
+            assert err <= eager_err, (
+                f"dw worst error {err:.3e} above the FP32 eager reference's {eager_err:.3e}")
         out[f"dx_ulp_{key}"] = ulp
         out[f"dx_cancel_{key}"] = n_extra
         out[f"dx_cancel_worst_{key}"] = worst

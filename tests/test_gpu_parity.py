@@ -33,7 +33,9 @@ def test_dw_stress(T, H):
     # the stress family is specified for deterministic=False; the largest T also runs
     # the deterministic mode
     modes = (False, True) if T == synth.STRESS_T[-1] else (False,)
-    parity.run_case(synth.stress(T, H), modes=modes)
+    # the pages' acceptance also asks that the worst dw error stay at or below the FP32
+    # eager reference's: checked at the two largest T
+    parity.run_case(synth.stress(T, H), modes=modes, check_eager=T >= synth.STRESS_T[-2])
 
 
 @pytest.mark.parametrize("T", synth.RES_T)
