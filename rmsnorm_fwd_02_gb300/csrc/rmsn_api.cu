@@ -4,7 +4,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <initializer_list>
 #include <mutex>
 #include <unordered_map>
 
@@ -55,17 +54,6 @@ size_t shared_bytes(const Shape& s, int H, bool bwd) {
                      bwd ? s.groups : 0, bwd && bwd_w_in_smem(s.cls, s.vpt) ? H : 0).total;
 }
 
-// Column vectors per thread, from the instantiated set `allowed` (descending): the
-// largest whose row of NV vectors splits into whole warps, else the largest that fills
-// at least one warp.
-int pick_vpt(int nv, std::initializer_list<int> allowed) {
-  for (int v : allowed)
-    if (nv % (32 * v) == 0) return v;
-  for (int v : allowed)
-    if (nv >= 32 * v) return v;
-  return 1;
-}
-
 Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true) {
   Shape s{};
   const int nv = H / 8;
@@ -86,13 +74,15 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true)
     else
       s.cls = kBwdNarrow;
   } else {
-    // rows of more than 256 threads exceed the two-CTA build: always one CTA an SM
-    s.cls = (vpt >= 2 && (s.ntg >= kFwdSoloMinGroup || s.ntg > 256)) ? kFwdSolo : kFwdPair;
+    // one-warp rows of up to 4 vectors a thread: two CTAs an SM (measured 2-5 % ahead of
+    // one CTA of 16 such rows at H = 768 and 1024); larger row groups and the 6-vector
+    // build: one CTA an SM
+    s.cls = (vpt == 6 || (vpt >= 2 && s.ntg >= kFwdSoloMinGroup)) ? kFwdSolo : kFwdPair;
   }
   // one-CTA-an-SM classes with several row groups fill 512 (forward) or 480 (backward)
   // consumers, the rest 256
   int budget = kMaxConsumerThreads / 2;
-  if (!bwd && s.cls == kFwdSolo) budget = kMaxConsumerThreads;
+  if (!bwd && s.cls == kFwdSolo) budget = fwd_solo_consumers(vpt);
   if (bwd && s.cls == kBwdMulti) budget = kMultiConsumers;
   s.groups = s.ntg >= budget ? 1 : budget / s.ntg;
   // whole-warp groups: at most 16 (their reduction slots in shared memory)
@@ -177,13 +167,42 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
 // hold x_hat, g, w and the dw sum/compensation of 16 columns), 4 above.
 Shape fwd_shape(int H, bool residual) {
   const int nv = H / 8;
-  // narrow rows: 4 vectors a lane in 8- or 16-lane groups
-  int vpt = nv <= 64 ? (nv >= 4 ? 4 : 1) : pick_vpt(nv, {4, 3, 2, 1});
-  // one-vector threads only while a row needs at most 256 of them (the two-CTA build);
-  // past that, ragged 4-vector rows
-  if (vpt == 1 && nv > 256) vpt = 4;
-  return make_shape(H, residual ? 2 : 1, vpt, false);
+  const int tensors = residual ? 2 : 1;
+  // narrow rows (H <= 512): 4 vectors a lane in 8- or 16-lane groups, two CTAs an SM
+  if (nv <= 64) return make_shape(H, tensors, nv >= 4 ? 4 : 1, false);
+  // wider rows: whole-warp row groups.  Rows of 2-4 vectors a thread run 512 consumers
+  // (they fit 96 registers); rows of 6 vectors a thread, 480 (16 warps, 128 registers).
+  // The 6-vector build is taken when it puts a quarter more rows in flight (measured:
+  // H = 1536 as 15 one-warp rows 0.67 -> 0.82 of peak against 8 two-warp rows; H = 3072
+  // 7 rows against 5 gains 3 %; H = 4096 5 rows against 4 loses 2 %); otherwise the
+  // vector count with the most rows in flight, then the most threads busy.  Every choice
+  // keeps three ring stages when it can.
+  auto group = [nv](int v) { return ((nv + v - 1) / v + 31) / 32 * 32; };
+  auto groups = [&](int v) {
+    const int gt = group(v), budget = fwd_solo_consumers(v);
+    const int g = gt > budget ? 0 : budget / gt;
+    return g > 16 ? 16 : g;
+  };
+  auto busy = [&](int v) { return groups(v) * ((nv + v - 1) / v); };
+  auto better = [&](int u, int v) {  // u beats v (v == 0: nothing yet)
+    if (v == 0) return true;
+    if ((u == 6) != (v == 6)) {
+      const int g6 = groups(u == 6 ? u : v), g4 = groups(u == 6 ? v : u);
+      const bool six = 4 * g6 > 5 * g4;
+      return u == 6 ? six : !six;
+    }
+    return groups(u) > groups(v) || (groups(u) == groups(v) && busy(u) > busy(v));
+  };
+  Shape best{}, any{};
+  for (int v : {2, 3, 4, 6}) {
+    if (groups(v) == 0) continue;
+    const Shape s = make_shape(H, tensors, v, false);
+    if (better(v, any.vpt)) any = s;
+    if (s.stages >= 3 && better(v, best.vpt)) best = s;
+  }
+  return best.vpt != 0 ? best : any;
 }
+
 Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
   // rows that 240 threads cover with 2 to 4 vectors each (narrow rows in 8- or 16-lane
@@ -432,7 +451,7 @@ int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out) {
                       : fwd_shape(H, op == RMSN_PLAN_FWD_RESIDUAL);
   const int64_t v[RMSN_PLAN_FIELDS] = {
       s.vpt, s.ntg, s.groups, s.stages, s.threads, static_cast<int64_t>(s.smem), s.cls,
-      bwd ? bwd_max_threads(s.cls, s.vpt) : fwd_max_threads(s.cls),
+      bwd ? bwd_max_threads(s.cls, s.vpt) : fwd_max_threads(s.cls, s.vpt),
       bwd ? bwd_design_blocks_per_sm(s.cls) : fwd_design_blocks_per_sm(s.cls)};
   for (int i = 0; i < n_out && i < RMSN_PLAN_FIELDS; ++i) out[i] = v[i];
   return RMSN_OK;

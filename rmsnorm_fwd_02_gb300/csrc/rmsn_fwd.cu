@@ -40,12 +40,12 @@ __device__ __forceinline__ uint4 residual_sum8(const uint4& u, const uint4& q) {
 }
 
 // Launch bounds per shape class (rmsn_launch.h): kFwdPair, at most 256 consumers (G*NTg)
-// + the producer warp, two CTAs an SM; kFwdSolo, at most 512 consumers + the producer
-// warp, one CTA an SM.
+// + the producer warp, two CTAs an SM; kFwdSolo, at most 512 consumers (480 with 6
+// vectors a thread) + the producer warp, one CTA an SM.
 // Narrow rows use sub-warp groups of 8 or 16 lanes (several rows a warp, reduced by
 // shuffles alone).
 template <int VPT, int kCls, bool kFp32W, bool kRes>
-__global__ void __launch_bounds__(fwd_max_threads(kCls), fwd_design_blocks_per_sm(kCls))
+__global__ void __launch_bounds__(fwd_max_threads(kCls, VPT), fwd_design_blocks_per_sm(kCls))
     rmsn_fwd_kernel(const FwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kRes ? 2 : 1;
@@ -238,12 +238,13 @@ static const void* pick_fwd_v(bool fp32w, bool res) {
   return res ? fwd_kernel_ptr<VPT, kCls, false, true>() : fwd_kernel_ptr<VPT, kCls, false, false>();
 }
 
-// kFwdSolo is built for 2..4 vectors a thread; 1-vector rows always take kFwdPair.
+// kFwdSolo is built for 2, 3, 4 and 6 vectors a thread, kFwdPair for 1 to 4.
 static const void* pick_fwd(const Shape& s, bool fp32w, bool res) {
   if (s.cls == kFwdSolo) {
     switch (s.vpt) {
       case 2: return pick_fwd_v<2, kFwdSolo>(fp32w, res);
       case 3: return pick_fwd_v<3, kFwdSolo>(fp32w, res);
+      case 6: return pick_fwd_v<6, kFwdSolo>(fp32w, res);
       default: return pick_fwd_v<4, kFwdSolo>(fp32w, res);
     }
   }

@@ -154,15 +154,19 @@ constexpr int bwd_max_threads(int cls, int vpt) {
 // Forward shape classes:
 //  kFwdPair  up to 256 consumers + the producer warp, two CTAs an SM: sub-warp groups
 //            and rows of at most 32-thread groups
-//  kFwdSolo  up to 512 consumers + the producer warp, one CTA an SM: row groups of 64
-//            threads or more, as many as fit in 512 consumers (one when a row needs more
-//            than 256 threads)
+//  kFwdSolo  one CTA an SM, row groups of 64 or more threads (or one-warp rows of 6
+//            vectors a thread), as many as fit (at most 16): 512 consumers + the producer
+//            warp for 2-4 vectors a thread (17 warps, at most 96 registers, which these
+//            builds fit), 480 for 6 (16 warps, 128 registers)
 // Two CTAs an SM split its bandwidth unevenly (one of the pair finishes its equal share
 // first and the other then runs alone); one CTA holding the same number of rows in
 // flight avoids that, where a row group is large enough to keep the warps busy.
 enum { kFwdPair = 0, kFwdSolo = 1 };
+constexpr int fwd_solo_consumers(int vpt) { return vpt == 6 ? 480 : 512; }
 constexpr int fwd_design_blocks_per_sm(int cls) { return cls == kFwdPair ? 2 : 1; }
-constexpr int fwd_max_threads(int cls) { return kProducerThreads + (cls == kFwdPair ? 256 : 512); }
+constexpr int fwd_max_threads(int cls, int vpt) {
+  return kProducerThreads + (cls == kFwdPair ? 256 : fwd_solo_consumers(vpt));
+}
 
 // Resident CTAs per SM of the chosen row kernel (cached per device).
 int fwd_blocks_per_sm(const Shape& s, bool fp32w);

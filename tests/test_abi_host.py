@@ -171,9 +171,11 @@ def test_launch_plan_fits_its_kernel_build_at_every_width(lib, op):
             if p["vpt"] == 3:
                 assert p["cls"] == 1, ctx      # 3-vector rows only in the multi-group build
         else:
-            assert p["vpt"] in (1, 2, 3, 4), ctx
             if p["cls"] == 1:
-                assert p["vpt"] >= 2, ctx      # the one-CTA forward is built for 2..4
+                assert p["vpt"] in (2, 3, 4, 6), ctx   # the one-CTA forward's builds
+                assert p["group_threads"] % 32 == 0, ctx
+            else:
+                assert p["vpt"] in (1, 2, 3, 4), ctx   # the two-CTA forward's builds
 
 
 def test_launch_plan_rejects_bad_arguments(lib):

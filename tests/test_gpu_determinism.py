@@ -72,8 +72,13 @@ def test_residual_forward_equals_plain_on_h():
     p = synth.Case(T=c.T, nh=1, H=c.H, s_tok=c.H, s_head=c.H, x=_bits(h), dy=c.dy, w=c.w)
     dp = parity.DeviceCase(p)
     y2, rstd2, _ = parity.gpu_fwd(dp, False)
-    assert np.array_equal(_bits(y), _bits(y2))
-    assert torch.equal(rstd, rstd2)
+    # the statistics come from h: the two forms may split a row over threads differently
+    # (the residual form stages twice the bytes a row), so their FP32 sums of squares may
+    # round differently -- rstd within 2^-22 relative, y within 1 BF16 ulp
+    rel = ((rstd - rstd2).abs() / rstd2).max().item()
+    assert rel <= 2.0**-22, rel
+    d = np.abs(parity.ordinal(_bits(y)) - parity.ordinal(_bits(y2)))
+    assert d.max() <= 1
 
 
 def test_empty_input_zero_fills_dw():
