@@ -162,9 +162,9 @@ int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
 
 // ---- helpers used by the kernel translation units ------------------------------------
 
-// Forward: up to 4 vectors (32 columns) a thread, so per-row work (reductions, rstd) is
-// spread over many elements.  Backward: 2 vectors a thread up to H = 6144 (registers
-// hold x_hat, g, w and the dw sum/compensation of 16 columns), 4 above.
+// Launch shapes: a thread owns VPT 16-byte column vectors of every row its group takes;
+// each kernel's vector count and row-group layout follow from H (and from the residual
+// form or dh), chosen for rows in flight within the kernel build's register budget.
 Shape fwd_shape(int H, bool residual) {
   const int nv = H / 8;
   const int tensors = residual ? 2 : 1;

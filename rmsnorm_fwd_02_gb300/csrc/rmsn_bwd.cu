@@ -45,9 +45,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     rmsn_bwd_rows_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
-  // rstd staged with its rows and read from shared memory in phase B (else each consumer
-  // would load its row's rstd from global memory in phase A, one iteration ahead)
-  constexpr bool kStageRs = true;
   const int H = a.map.H;
   const int NV = H >> 3;
   const int G = a.groups, NTg = a.ntg, S = a.stages;
@@ -107,9 +104,9 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
         // when rstd is not 16-byte aligned -- by 4-byte async copies that the same
         // barrier tracks (one extra pending arrival, taken before the arrival below).
         const int32_t a4 = ra & ~3;
-        const int32_t b4 = !kStageRs ? a4 : (rs_bulk ? min((rb + 3) & ~3, a.R & ~3) : a4);
+        const int32_t b4 = rs_bulk ? min((rb + 3) & ~3, a.R & ~3) : a4;
         float* rsd = rs_ring + s * RSP;
-        if (kStageRs && rb > b4) {
+        if (rb > b4) {
           for (int32_t r = max(ra, b4); r < rb; ++r) cp_async_4(rsd + (r - a4), a.rstd + r);
           cp_async_mbar_arrive(&full[s]);
         }
@@ -187,14 +184,12 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
   float dot_carry = 0.f; // sub-warp groups: row j-1's sum of (dy*w)*x
-  float rs_carry = 0.f;  // multi-group build: row j-1's rstd, loaded in phase A(j-1)
   for (int32_t j = 0; j <= ng; ++j) {
-    float dot_new = 0.f, rs_new = 0.f;
+    float dot_new = 0.f;
     // ---- phase A, row j: partial of sum (dy*w)*x ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
       const bool valid = row < r1;
-      if (!kStageRs && valid) rs_new = __ldg(a.rstd + row);
       const int s = j % S;
       mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
                         kErrConsumerWait);
@@ -246,7 +241,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       }
       if (row < r1) {
         // this row's rstd, staged with the row (the stage is held until phase B ends)
-        const float rs = kStageRs ? rs_ring[s * RSP + (row - ((r0 + jj * G) & ~3))] : rs_carry;
+        const float rs = rs_ring[s * RSP + (row - ((r0 + jj * G) & ~3))];
         // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
         // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
         // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
@@ -295,7 +290,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
     }
     dot_carry = dot_new;
-    rs_carry = rs_new;
   }
 
   // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----

@@ -123,10 +123,6 @@ cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
-// Backward builds that keep the weight in shared memory (FP32, H floats) instead of
-// registers: 4-vector threads of the multi-group class.
-__host__ __device__ constexpr bool bwd_w_in_smem(int cls, int vpt) { return cls == 1 && vpt == 4; }
-
 // Backward shape classes, each its own kernel build:
 //  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector lanes (H = 8)
 //  kBwdMulti   2- to 4-vector threads in row groups of 8, 16 or 32..240 threads, as many
@@ -140,6 +136,12 @@ __host__ __device__ constexpr bool bwd_w_in_smem(int cls, int vpt) { return cls 
 //              4-vector threads (H above 6144), one CTA an SM
 enum { kBwdNarrow = 0, kBwdMulti = 1, kBwdWide = 2 };
 constexpr int kMultiConsumers = 480;
+
+// Backward builds that keep the weight in shared memory (FP32, H floats) instead of
+// registers: 4-vector threads of the multi-group class.
+__host__ __device__ constexpr bool bwd_w_in_smem(int cls, int vpt) {
+  return cls == kBwdMulti && vpt == 4;
+}
 
 // CTAs per SM the backward row kernel is built to keep resident (its launch bounds'
 // minimum), a compile-time property of the shape class.
