@@ -125,7 +125,7 @@ STRESS_T = (65, 4096, 32768, 65536, 98304, 131072)
 def stress(T: int, H: int, seed: int = 0) -> Case:
     """dw-accuracy stress: 1 % of rows x16, FP32 weight."""
     return make_case(seed, T, H, w_fp32=True, outlier_frac=0.01,
-                     label=f"stress_T{T}_H{H}")
+                     label=f"stress_T{T}_H{H}" + (f"_seed{seed}" if seed else ""))
 
 
 RES_H = 6144
