@@ -5,7 +5,9 @@
 - both modes run the same forward and the same row pass: dx identical across modes.
 - per-head views equal the plain path on a gathered contiguous copy, bit for bit (y,
   rstd, dx; dw too in deterministic mode, where the partition depends on R and H only).
-- the residual form's y and rstd equal the plain forward run on its h.
+- the residual form's y and rstd equal the plain forward run on its h (to 2^-22 in rstd,
+  1 BF16 ulp in y: the two forms may split a row over threads differently).
+- a training step captured in a CUDA graph replays to the same bits as direct calls.
 """
 import numpy as np
 import pytest
@@ -136,3 +138,48 @@ def test_autograd_wrapper_matches_direct_calls():
     assert torch.equal(y, y0)
     assert torch.equal(x.grad, dx0)
     assert torch.equal(w.grad, dw0.to(w.dtype))
+
+
+@pytest.mark.parametrize("det", [True, False])
+def test_cuda_graph_replay_matches_direct_calls(det):
+    # forward + backward enqueued on a side stream under stream capture (the launches use
+    # programmatic dependent launch attributes) and replayed: the same bits as direct calls
+    c = synth.plain(8192)
+    dc = parity.DeviceCase(c)
+    R, H = c.R, c.H
+    nbytes = N.rmsnorm_train_bwd_workspace_bytes(c.T, 1, H, det)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    y = torch.empty(R * H, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.empty(R, dtype=torch.float32, device="cuda")
+    dx = torch.empty(R * H, dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty(H, dtype=torch.float32, device="cuda")
+
+    def step(stream):
+        N.rmsnorm_train_fwd(dc.x, None, dc.w, N.RMSN_W_BF16, y, None, rstd, c.T, 1, H, H, H,
+                            c.eps, stream=stream)
+        N.rmsnorm_train_bwd(dc.x, dc.dy, None, rstd, dc.w, N.RMSN_W_BF16, dx, dw, ws, nbytes,
+                            c.T, 1, H, H, H, det, stream=stream)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step(s.cuda_stream)   # warm-up: kernel attributes set outside the capture
+    torch.cuda.synchronize()
+    want = (_bits(y), rstd.cpu().numpy().copy(), _bits(dx), dw.cpu().numpy().copy())
+    for t in (y, dx):
+        t.zero_()
+    rstd.zero_()
+    dw.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(s.cuda_stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    got = (_bits(y), rstd.cpu().numpy(), _bits(dx), dw.cpu().numpy())
+    assert np.array_equal(want[0], got[0]) and np.array_equal(want[1], got[1])
+    assert np.array_equal(want[2], got[2])
+    if det:
+        assert np.array_equal(want[3], got[3])
+    else:
+        np.testing.assert_allclose(got[3], want[3], rtol=1e-6, atol=1e-6)
+    assert N.rmsnorm_train_device_error(reset=True) == 0
