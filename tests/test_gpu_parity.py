@@ -126,3 +126,13 @@ def test_dw_stress_other_seeds(H, seed):
     T = synth.STRESS_T[-1]
     r = parity.run_case(synth.stress(T, H, seed=seed), modes=(False,), check_eager=True)
     assert r["dw_ratio_nondet"] <= 1
+
+
+@pytest.mark.parametrize("H,T", [(256, 5000), (1536, 700), (3072, 401), (7168, 150),
+                                 (8192, 130)])
+def test_residual_form_and_dh_at_other_widths(H, T):
+    # the residual forward and the with-dh backward take their own launch plans (twice the
+    # staged bytes a row): check them at widths of each build
+    c = synth.make_case(19, T, H, residual=True, dh=True, label=f"resdh{H}_T{T}")
+    parity.run_case(c, with_dh=True)
+    parity.run_case(c)
