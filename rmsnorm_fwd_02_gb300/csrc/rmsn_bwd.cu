@@ -132,7 +132,9 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   // Split-phase rows: phase A of row j forms each warp's partial of sum_j (dy*w)*x and
   // arrives on the row's reduction mbarrier; phase B of row j-1 waits on that barrier
   // (normally long complete), re-reads row j-1 from shared memory, and produces dx and
-  // the dw contributions.  Registers hold only w and the dw state across rows.
+  // the dw contributions.  Across rows a thread keeps only its columns' dw state and
+  // weight in registers (the 4-vector multi-group build reads the weight from shared
+  // memory instead).
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
