@@ -582,7 +582,7 @@ def run_sweep(args):
             base["rr"], base["dh"] = dbf(c.residual), dbf(c.dh)
         w = torch.from_numpy(c.w).to(dev) if w32 else dbf(c.w)
         set_bytes = sum(t.numel() * t.element_size() for t in base.values()) + 3 * R * H * 2
-        nsets = max(2, -(-2 * l2_bytes // set_bytes) + 1)
+        nsets = 1 if args.sweep_once else max(2, -(-2 * l2_bytes // set_bytes) + 1)
         sets = []
         for i in range(nsets):
             st = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
@@ -602,7 +602,7 @@ def run_sweep(args):
                                        1e-6, sh)
             assert st == 0, st
 
-        for i in range(nsets):
+        for i in range(1 if args.sweep_once else nsets):
             fwd(i)
         s_tok, s_head = (nh * H, H) if res else (c.s_tok, c.s_head)
         rows = [("fwd", fwd, (8 if res else 4) * R * H + 4 * R + wbytes * H)]
@@ -633,6 +633,18 @@ def run_sweep(args):
                         bwd(i)
 
                     rows.append(("2xfwd+bwd_det", ckpt, 2 * rows[0][2] + bwd_bytes_))
+        if args.sweep_once:
+            torch.cuda.synchronize()
+            for name, fn, nbytes in rows:
+                if name.startswith("2x") or "nondet" in name or name == "fwd":
+                    continue   # the forward already ran once, for the backward's rstd
+                fn(0)
+                torch.cuda.synchronize()
+                print(json.dumps({"sweep": label, "op": name, "T": T, "H": H, "nh": nh,
+                                  "ran_once": True}), flush=True)
+            del sets, base, w
+            torch.cuda.empty_cache()
+            continue
         for name, fn, nbytes in rows:
             us = timed(fn, args.sweep_reps)
             us_s = timed_stream(fn, nsets, args.sweep_reps)
@@ -667,6 +679,9 @@ def main(argv=None):
     ap.add_argument("--sweep-reps", type=int, default=30)
     ap.add_argument("--sweep-filter", default="",
                     help="only the sweep entry LABEL_T_H (e.g. stress_131072_1536)")
+    ap.add_argument("--sweep-once", action="store_true",
+                    help="with --sweep: run each op of each selected workload once, untimed "
+                         "(one launch of each kernel, for a profiler)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
