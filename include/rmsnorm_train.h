@@ -78,10 +78,11 @@ int rmsnorm_train_fwd(const void* x, const void* residual, const void* w, int w_
                       float eps, void* stream);
 
 /*
- * Bytes of device workspace rmsnorm_train_bwd needs for this shape and mode (0 is never
- * returned for T*nh > 0).  For deterministic == 0 the size depends on the current device
- * (its SM count); for deterministic != 0 it depends on (T, nh, H) only.  Returns 0 on
- * invalid sizes.  Host-only computation apart from a device-attribute query.
+ * Bytes of device workspace rmsnorm_train_bwd needs for this shape and mode: 0 for
+ * T*nh <= 256 rows (done in one launch without a workspace) and for T*nh == 0.  For
+ * deterministic == 0 the size depends on the current device (its SM count); for
+ * deterministic != 0 it depends on (T, nh, H) only.  Returns 0 on invalid sizes.
+ * Host-only computation apart from a device-attribute query.
  */
 size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int deterministic);
 
@@ -102,6 +103,7 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
  *   dw         FP32 [H] out, overwritten (not accumulated); zero-filled when T*nh == 0
  *   workspace  device scratch of >= rmsnorm_train_bwd_workspace_bytes(...) bytes,
  *              16-byte aligned, no initial contents required; clobbered by the call
+ *              (may be NULL when that size is 0)
  *   deterministic  0 or 1 (see the top of this file)
  */
 int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float* rstd,

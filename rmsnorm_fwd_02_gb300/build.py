@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm_train.so")
-SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu"]
+SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_small.cu"]
 HEADERS = ["rmsn_common.cuh", "rmsn_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

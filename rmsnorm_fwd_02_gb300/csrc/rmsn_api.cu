@@ -367,7 +367,7 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
       RMSN_OK)
     return 0;
   const int64_t R = T * static_cast<int64_t>(nh);
-  if (R == 0) return 0;
+  if (R == 0 || bwd_is_small(R)) return 0;  // small inputs take the one-launch path
   // the launch shape (so the partial count) may differ with and without dh: one size
   // serves both
   const Shape s = bwd_shape(H, false);
@@ -412,6 +412,19 @@ int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float
   const cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
 
   const bool fp32w = (w_dtype == RMSN_W_FP32);
+  if (bwd_is_small(R)) {  // one launch, no workspace
+    BwdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dy = static_cast<const __nv_bfloat16*>(dy);
+    a.dh = static_cast<const __nv_bfloat16*>(dh);
+    a.rstd = rstd;
+    a.w = w;
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
+    a.R = static_cast<int32_t>(R);
+    a.err = g_err_ptr[dev];
+    return launch_bwd_small(a, dw, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
+  }
   const Shape s = bwd_shape(H, dh != nullptr);
   int P = 0;
   if (R > 0) {

@@ -123,6 +123,15 @@ cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
+// Small inputs (rmsn_small.cu): the whole backward in one launch of row tasks (dx) and
+// column tasks (dw over every row in a fixed order), no workspace, for R <= kSmallMaxRows.
+constexpr int kSmallThreads = 256;
+constexpr int kSmallColVecs = 4;                              // column vectors a column task
+constexpr int kSmallSlices = kSmallThreads / kSmallColVecs;   // row slices a column task
+constexpr int64_t kSmallMaxRows = 256;
+bool bwd_is_small(int64_t R);
+cudaError_t launch_bwd_small(const BwdArgs& a, float* dw, bool fp32w, cudaStream_t st);
+
 // Backward shape classes, each its own kernel build:
 //  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector lanes (H = 8)
 //  kBwdMulti   2- to 4-vector threads in row groups of 8, 16 or 32..240 threads, as many

@@ -103,7 +103,7 @@ def test_empty_input_zero_fills_dw():
 
 
 def test_workspace_too_small_is_rejected():
-    c = synth.plain(64)
+    c = synth.plain(300)      # above the one-launch (no workspace) size
     dc = parity.DeviceCase(c)
     need = N.rmsnorm_train_bwd_workspace_bytes(c.T, 1, c.H, True)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")

@@ -136,3 +136,11 @@ def test_residual_form_and_dh_at_other_widths(H, T):
     c = synth.make_case(19, T, H, residual=True, dh=True, label=f"resdh{H}_T{T}")
     parity.run_case(c, with_dh=True)
     parity.run_case(c)
+
+
+@pytest.mark.parametrize("H,T", [(4096, 256), (4096, 257), (256, 256), (256, 257), (8192, 200),
+                                 (8, 256)])
+def test_one_launch_backward_boundary(H, T):
+    # up to 256 rows the backward is one launch of row and column tasks; above, the staged
+    # row pass and the dw finish: both sides of the boundary, in both modes
+    parity.run_case(synth.make_case(17, T, H, w_fp32=(H == 8192), label=f"edge{H}_T{T}"))
