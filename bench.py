@@ -19,6 +19,9 @@ plus the dw finish), timed by events around it on its launch stream.
 
 With --gpus N under torchrun each rank runs an independent replica (the op has no
 exchange step); timings are max-reduced over ranks on the host (gloo).
+
+`--sweep` instead times every op of every workload family (isolated and back to back, one
+JSON line each); `--sweep --sweep-once` runs each op once, untimed, for a profiler.
 """
 from __future__ import annotations
 
