@@ -15,7 +15,8 @@ Gates (the op's stated accuracy, flashinfer PR #8827 description and Measurement
   dw      |dw - dw64| <= 1e-4 + 1e-4 * |dw64| for every element
 The backward is fed rstd = FP32(rstd64), the oracle's own correctly rounded forward rstd,
 so no oracle input ever comes from the CUDA path; the oracle's dx and dw use that same
-FP32 value widened to FP64.
+FP32 value widened to FP64 (the gate).  dw against the oracle at rstd64 itself, the other
+rstd form, is reported as dw_ratio_rstd64_*.
 """
 from __future__ import annotations
 
@@ -225,6 +226,9 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
     r_in = r32.astype(np.float64)
     r_dev = to_dev(r32)
     dw64 = oracle.bwd_dw(xs_bits, c.dy, r_in, c.T, c.nh, H, s_tok, s_head)
+    # the second rstd form: the FP64 rstd itself (reported, not gated -- the kernels are
+    # handed the FP32 rstd a forward returns)
+    dw64_exact = oracle.bwd_dw(xs_bits, c.dy, rstd64, c.T, c.nh, H, s_tok, s_head)
     dx64 = oracle.bwd_dx(xs_bits, c.dy, r_in, c.w, c.T, c.nh, H, s_tok, s_head,
                          dh=c.dh if with_dh else None, rows=rows)
     sel = np.arange(R) if rows is None else rows
@@ -246,6 +250,9 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
         ratio = check_dw(dw.cpu().numpy(), dw64)
         dws[det] = (dxb, dw.cpu().numpy())
         key = "det" if det else "nondet"
+        budget = DW_ATOL + DW_RTOL * np.abs(dw64_exact)
+        out[f"dw_ratio_rstd64_{key}"] = float(
+            (np.abs(dw.cpu().numpy().astype(np.float64) - dw64_exact) / budget).max())
         if eager_err is not None:
             err = float(np.abs(dw.cpu().numpy().astype(np.float64) - dw64).max())
             out[f"dw_max_err_{key}"] = err
