@@ -12,9 +12,9 @@
  *             dw_j = sum over all normalized rows of dy_j * xhat_j   (FP32)
  *
  * Two backward modes share one forward: deterministic != 0 gives bit-identical dw run to
- * run and across GPUs of any SM count (the row -> partial mapping depends on T, nh and H
- * only); deterministic == 0 may size its partition to the current GPU.  dx is the same in
- * both modes, bit for bit.
+ * run and across GPUs of any SM count (the row -> partial mapping depends on T, nh, H and
+ * whether dh is given, never on the GPU); deterministic == 0 may size its partition to
+ * the current GPU.  dx is the same in both modes, bit for bit.
  *
  * Rows and views (same PR, description: per-head views [T,24,256] strided and [T,4,256]
  * contiguous with a shared w[256]).  A normalized row is a pair (token t, head h),
@@ -29,7 +29,8 @@
  *  - Ownership: the caller owns every buffer, the workspace included.  The library never
  *    allocates, frees or synchronizes; all work is enqueued on `stream` (a cudaStream_t
  *    passed as void*; NULL = the legacy default stream) and is asynchronous.
- *  - Alignment: every tensor pointer 16-byte aligned; H a multiple of 8; s_tok and
+ *  - Alignment: every tensor pointer 16-byte aligned, except rstd (4-byte aligned; the
+ *    backward reads it fastest when it is 16-byte aligned); H a multiple of 8; s_tok and
  *    s_head multiples of 8 elements (each row is a 16-byte-aligned run).
  *  - Limits: 8 <= H <= 8192, T >= 0, nh >= 1, T*nh < 2^31.
  *  - Outputs must not overlap inputs.
