@@ -21,7 +21,9 @@ With --gpus N under torchrun each rank runs an independent replica (the op has n
 exchange step); timings are max-reduced over ranks on the host (gloo).
 
 `--sweep` instead times every op of every workload family (isolated and back to back, one
-JSON line each); `--sweep --sweep-once` runs each op once, untimed, for a profiler.
+JSON line each); `--sweep --sweep-once` runs each op once, untimed, for a profiler;
+`--sweep --sweep-layernorm` does the same for the LayerNorm ops on the shapes of the
+normalization tables.
 """
 from __future__ import annotations
 
@@ -58,8 +60,13 @@ def bwd_bytes(R: int, H: int, wbytes: int) -> int:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the RMSNorm kernel sources (the rmsn_* files): the key that ties a recorded
+    traffic figure to the kernels it was measured on.  The LayerNorm sources beside them
+    (ln_*) build into the same library but no RMSNorm launch runs their code."""
     h = hashlib.sha256()
     for fn in sorted(os.listdir(CSRC)):
+        if not fn.startswith("rmsn_"):
+            continue
         with open(os.path.join(CSRC, fn), "rb") as f:
             h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -510,35 +517,9 @@ SWEEP = [
 ]
 
 
-def run_sweep(args):
-    """Times each op of each workload (forward; backward in both modes, with and without dh
-    in the residual form; the checkpointed step 2xfwd+bwd = forward, forward recompute,
-    deterministic backward) two ways, CUDA events on the launch stream:
-
-    isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
-              The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
-              flush would leave dirty lines whose write-back lands inside the next timed
-              kernel).  Includes the launch's ramp-up and tail and the gap before the first
-              CTA starts.
-    stream    `reps` launches back to back inside one event pair, rotating over copies of
-              the inputs and outputs so that every launch finds its inputs out of L2 (the
-              sets in between exceed twice the L2); time / launches.  This is the op as a
-              training step runs it, queued behind other work."""
-    import torch
-    from rmsnorm_fwd_02_gb300 import _native as N
-    from rmsnorm_fwd_02_gb300 import synth
-
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    lib = N.lib()
-    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
-    peak, peak_kind = measured_peak()
-    l2_bytes = 129 << 20
-
-    def dbf(bits):
-        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+def _sweep_timers(torch, stream, flush):
+    """The sweep's two clocks (see run_sweep): isolated launches after a read-based L2
+    flush, and launches back to back over rotating input sets."""
 
     def timed(fn, reps):
         out = []
@@ -572,6 +553,41 @@ def run_sweep(args):
         b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / n
+
+    return timed, timed_stream
+
+
+def run_sweep(args):
+    """Times each op of each workload (forward; backward in both modes, with and without dh
+    in the residual form; the checkpointed step 2xfwd+bwd = forward, forward recompute,
+    deterministic backward) two ways, CUDA events on the launch stream:
+
+    isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
+              The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
+              flush would leave dirty lines whose write-back lands inside the next timed
+              kernel).  Includes the launch's ramp-up and tail and the gap before the first
+              CTA starts.
+    stream    `reps` launches back to back inside one event pair, rotating over copies of
+              the inputs and outputs so that every launch finds its inputs out of L2 (the
+              sets in between exceed twice the L2); time / launches.  This is the op as a
+              training step runs it, queued behind other work."""
+    import torch
+    from rmsnorm_fwd_02_gb300 import _native as N
+    from rmsnorm_fwd_02_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    lib = N.lib()
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
+    peak, peak_kind = measured_peak()
+    l2_bytes = 129 << 20
+
+    def dbf(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    timed, timed_stream = _sweep_timers(torch, stream, flush)
 
     for label, T, H, nh, bh, w32, res in SWEEP:
         if args.sweep_filter and args.sweep_filter != f"{label}_{T}_{H}":
@@ -665,6 +681,116 @@ def run_sweep(args):
     return 0
 
 
+# ---- LayerNorm sweep (the normalization tables' shapes: M rows of hidden_size, BF16) ------
+
+LN_SWEEP = [(M, H) for H in (3584, 4096, 8192) for M in (1024, 2048, 4096, 8192)] + [
+    (32768, 4096), (65536, 4096), (16384, 8192)]
+
+
+def ln_fwd_bytes(R: int, H: int, wbytes: int) -> int:
+    """x read, y written (BF16), mean and rstd written (FP32), w and b read."""
+    return 4 * R * H + 8 * R + 2 * wbytes * H
+
+
+def ln_bwd_bytes(R: int, H: int, wbytes: int) -> int:
+    """x, dy read and dx written (BF16), mean and rstd read, w read, dw and db written."""
+    return 6 * R * H + 8 * R + wbytes * H + 8 * H
+
+
+def run_ln_sweep(args):
+    """The LayerNorm forward and backward (both modes) on the normalization tables' shapes
+    (M in 1024..8192 at hidden 3584, 4096, 8192) and a few larger M, timed like run_sweep:
+    isolated (L2 flushed by a read) and back to back over rotating input sets."""
+    import torch
+    from rmsnorm_fwd_02_gb300 import _native as N
+    from rmsnorm_fwd_02_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    lib = N.lib()
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
+    peak, peak_kind = measured_peak()
+    l2_bytes = 129 << 20
+    timed, timed_stream = _sweep_timers(torch, stream, flush)
+
+    def dbf(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    for M, H in LN_SWEEP:
+        if args.sweep_filter and args.sweep_filter != f"layernorm_{M}_{H}":
+            continue
+        c = synth.make_ln_case(0, M, H)
+        wbytes = 4 if c.wb_fp32 else 2
+        wd = N.RMSN_W_FP32 if c.wb_fp32 else N.RMSN_W_BF16
+        w = torch.from_numpy(c.w).to(dev) if c.wb_fp32 else dbf(c.w)
+        b = torch.from_numpy(c.b).to(dev) if c.wb_fp32 else dbf(c.b)
+        base = {"x": dbf(c.x), "dy": dbf(c.dy)}
+        set_bytes = 4 * M * H * 2
+        nsets = 1 if args.sweep_once else max(2, -(-2 * l2_bytes // set_bytes) + 1)
+        sets = []
+        for i in range(nsets):
+            st = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+            st["y"] = torch.empty(M * H, dtype=torch.bfloat16, device=dev)
+            st["dx"] = torch.empty_like(st["y"])
+            st["mean"] = torch.empty(M, dtype=torch.float32, device=dev)
+            st["rstd"] = torch.empty(M, dtype=torch.float32, device=dev)
+            st["dw"] = torch.empty(H, dtype=torch.float32, device=dev)
+            st["db"] = torch.empty(H, dtype=torch.float32, device=dev)
+            sets.append(st)
+
+        def fwd(i):
+            q = sets[i]
+            st = lib.layernorm_train_fwd(q["x"].data_ptr(), w.data_ptr(), b.data_ptr(), wd,
+                                         q["y"].data_ptr(), q["mean"].data_ptr(),
+                                         q["rstd"].data_ptr(), M, H, c.eps, sh)
+            assert st == 0, st
+
+        for i in range(1 if args.sweep_once else nsets):
+            fwd(i)
+        rows = [("ln_fwd", fwd, ln_fwd_bytes(M, H, wbytes))]
+        for det in (1, 0):
+            nws = N.layernorm_train_bwd_workspace_bytes(M, H, det)
+            ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+
+            def bwd(i, det=det, ws=ws, nws=nws):
+                q = sets[i]
+                st = lib.layernorm_train_bwd(q["x"].data_ptr(), q["dy"].data_ptr(),
+                                             q["mean"].data_ptr(), q["rstd"].data_ptr(),
+                                             w.data_ptr(), wd, q["dx"].data_ptr(),
+                                             q["dw"].data_ptr(), q["db"].data_ptr(),
+                                             ws.data_ptr(), nws, M, H, det, sh)
+                assert st == 0, st
+
+            rows.append(("ln_bwd_det" if det else "ln_bwd_nondet", bwd,
+                         ln_bwd_bytes(M, H, wbytes)))
+        if args.sweep_once:
+            torch.cuda.synchronize()
+            rows[1][1](0)
+            torch.cuda.synchronize()
+            print(json.dumps({"sweep": "layernorm", "op": "ln_fwd+ln_bwd_det", "M": M, "H": H,
+                              "ran_once": True}), flush=True)
+            del sets, base, w, b
+            torch.cuda.empty_cache()
+            continue
+        for name, fn, nbytes in rows:
+            us = timed(fn, args.sweep_reps)
+            us_s = timed_stream(fn, nsets, args.sweep_reps)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            gbs_s = nbytes / (us_s * 1e-6) / 1e9
+            print(json.dumps({"sweep": "layernorm", "op": name, "M": M, "H": H,
+                              "w": "fp32" if c.wb_fp32 else "bf16", "us": round(us, 2),
+                              "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "stream_us": round(us_s, 2), "stream_GBps": round(gbs_s, 1),
+                              "stream_frac": round(gbs_s / peak, 4), "input_sets": nsets,
+                              "peak": peak, "peak_kind": peak_kind,
+                              "bytes": nbytes}), flush=True)
+        del sets, base, w, b
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -682,6 +808,9 @@ def main(argv=None):
     ap.add_argument("--sweep-reps", type=int, default=30)
     ap.add_argument("--sweep-filter", default="",
                     help="only the sweep entry LABEL_T_H (e.g. stress_131072_1536)")
+    ap.add_argument("--sweep-layernorm", action="store_true",
+                    help="with --sweep: the LayerNorm ops on the normalization tables' shapes "
+                         "(filter entries as layernorm_M_H)")
     ap.add_argument("--sweep-once", action="store_true",
                     help="with --sweep: run each op of each selected workload once, untimed "
                          "(one launch of each kernel, for a profiler)")
@@ -691,7 +820,7 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:
-        return run_sweep(args)
+        return run_ln_sweep(args) if args.sweep_layernorm else run_sweep(args)
     return run_ours(args)
 
 

@@ -1,4 +1,5 @@
-"""ctypes binding of ``librmsnorm_train.so`` with the C ABI's names.
+"""ctypes binding of ``librmsnorm_train.so`` with the C ABI's names (include/rmsnorm_train.h
+and include/layernorm_train.h).
 
 Argument marshalling only: tensors become device pointers, the current torch stream
 becomes the ``cudaStream_t``, sizes and strides are passed through, and a nonzero status
@@ -33,9 +34,17 @@ SIGNATURES = {
     "rmsnorm_train_status_str": (C.c_char_p, [_int]),
     "rmsnorm_train_device_error": (_int, [C.POINTER(C.c_uint), _int]),
     "rmsnorm_train_launch_plan": (_int, [_i32, _int, C.POINTER(C.c_int64), _int]),
+    # include/layernorm_train.h
+    "layernorm_train_fwd": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _i64, _i32, _f32, _vp]),
+    "layernorm_train_bwd_workspace_bytes": (_size, [_i64, _i32, _int]),
+    "layernorm_train_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _size,
+                                   _i64, _i32, _int, _vp]),
+    "layernorm_train_launch_plan": (_int, [_i32, _int, C.POINTER(C.c_int64), _int]),
+    "layernorm_train_device_error": (_int, [C.POINTER(C.c_uint), _int]),
 }
 
 PLAN_FWD, PLAN_FWD_RESIDUAL, PLAN_BWD, PLAN_BWD_DH = 0, 1, 2, 3
+LN_PLAN_FWD, LN_PLAN_BWD = 0, 1
 PLAN_FIELDS = ("vpt", "group_threads", "groups", "stages", "threads", "smem", "cls",
                "class_max_threads", "class_blocks_per_sm")
 
@@ -137,3 +146,42 @@ def rmsnorm_train_launch_plan(H, op):
     if st != RMSN_OK:
         raise RmsnError("rmsnorm_train_launch_plan", st)
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+# ---- LayerNorm (include/layernorm_train.h) ----------------------------------------------
+
+def layernorm_train_fwd(x, w, b, wb_dtype, y, mean, rstd, R, H, eps, stream=None):
+    st = lib().layernorm_train_fwd(_ptr(x), _ptr(w), _ptr(b), wb_dtype, _ptr(y), _ptr(mean),
+                                   _ptr(rstd), R, H, eps, _stream(stream))
+    if st != RMSN_OK:
+        raise RmsnError("layernorm_train_fwd", st)
+
+
+def layernorm_train_bwd_workspace_bytes(R, H, deterministic):
+    return int(lib().layernorm_train_bwd_workspace_bytes(R, H, int(deterministic)))
+
+
+def layernorm_train_bwd(x, dy, mean, rstd, w, wb_dtype, dx, dw, db, workspace, workspace_bytes,
+                        R, H, deterministic, stream=None):
+    st = lib().layernorm_train_bwd(_ptr(x), _ptr(dy), _ptr(mean), _ptr(rstd), _ptr(w), wb_dtype,
+                                   _ptr(dx), _ptr(dw), _ptr(db), _ptr(workspace),
+                                   workspace_bytes, R, H, int(deterministic), _stream(stream))
+    if st != RMSN_OK:
+        raise RmsnError("layernorm_train_bwd", st)
+
+
+def layernorm_train_launch_plan(H, op):
+    """The library's LayerNorm launch plan for op LN_PLAN_FWD / LN_PLAN_BWD, as a dict."""
+    out = (C.c_int64 * len(PLAN_FIELDS))()
+    st = lib().layernorm_train_launch_plan(H, op, out, len(PLAN_FIELDS))
+    if st != RMSN_OK:
+        raise RmsnError("layernorm_train_launch_plan", st)
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+def layernorm_train_device_error(reset=True):
+    flags = C.c_uint(0)
+    st = lib().layernorm_train_device_error(C.byref(flags), int(reset))
+    if st != RMSN_OK:
+        raise RmsnError("layernorm_train_device_error", st)
+    return int(flags.value)

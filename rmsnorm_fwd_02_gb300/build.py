@@ -18,8 +18,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm_train.so")
-SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_small.cu"]
-HEADERS = ["rmsn_common.cuh", "rmsn_launch.h"]
+SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_small.cu",
+           "ln_api.cu", "ln_fwd.cu", "ln_bwd.cu"]
+HEADERS = ["rmsn_common.cuh", "rmsn_launch.h", "ln_launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,7 +33,7 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files.append(os.path.join(ROOT, "include", "rmsnorm_train.h"))
+    files += [os.path.join(ROOT, "include", h) for h in ("rmsnorm_train.h", "layernorm_train.h")]
     return files
 
 

@@ -1,0 +1,491 @@
+// ln_bwd.cu -- LayerNorm training backward for sm_103a: the dx row pass fused with the dw
+// and db partial sums, and the fixed-order finish of both.
+//
+// Per row, with the forward's mean and rstd r (textbook LayerNorm gradient; the
+// normalization benchmarked beside RMSNorm in ROCm TransformerEngine PR #478's tables):
+//   d_j = x_j - mean,  xhat_j = d_j * r,  g_j = dy_j * w_j
+//   c1  = (1/H) sum_j g_j,   c2 = (1/H) sum_j g_j * xhat_j = (r/H) sum_j g_j * d_j
+//   dx_j = BF16(r * (g_j - c1 - xhat_j * c2))
+//   dw_j += dy_j * xhat_j,   db_j += dy_j          over every row of every CTA's chunk
+//
+// The two row sums (sum g, sum g*d) travel together through one reduction per row, so the
+// pipeline is the RMSNorm backward's: a producer warp stages x, dy and the rows' mean and
+// rstd; phase A of row j forms the partial sums; phase B of row j-1 writes dx and adds the
+// row to the thread's dw and db running sums.  Each running sum carries a Fast2Sum
+// compensation term, and a CTA writes its partial as an unevaluated (hi, lo) FP32 pair per
+// column; the finish adds the P pairs in a fixed order with TwoSum, so dw and db are
+// bit-reproducible for a fixed partition and dx does not depend on the partition at all.
+#include "ln_launch.h"
+#include "rmsn_common.cuh"
+
+namespace lnorm {
+
+using namespace rmsn;
+
+namespace {
+
+constexpr int kLnFinishCols = 32;
+constexpr int kLnFinishSlices = 32;
+
+// Knuth's TwoSum: s + err == a + b exactly, no ordering assumption.
+__device__ __forceinline__ float two_sum_ln(float a, float b, float& err) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float ap = __fsub_rn(s, bp);
+  err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+  return s;
+}
+
+// Running sum with a Fast2Sum compensation term: acc + cmp tracks the sum of every p.
+__device__ __forceinline__ void comp_add(f2& acc, f2& cmp, f2 p) {
+  const f2 t = f2_add(acc, p);
+  cmp = f2_add(cmp, f2_add(f2_sub(acc, t), p));
+  acc = t;
+}
+
+// The 8 weights of column vector c, kept as loaded (BF16: one uint4 of pairs).
+template <bool kFp32>
+struct W8;
+template <>
+struct W8<false> {
+  uint4 u;
+};
+template <>
+struct W8<true> {
+  float4 a, b;
+};
+
+template <bool kFp32>
+__device__ __forceinline__ void load_w8_raw(const void* p, int c, W8<kFp32>& out) {
+  if constexpr (kFp32) {
+    const float4* q = reinterpret_cast<const float4*>(p) + 2 * c;
+    out.a = __ldg(q);
+    out.b = __ldg(q + 1);
+  } else {
+    out.u = __ldg(reinterpret_cast<const uint4*>(p) + c);
+  }
+}
+
+template <bool kFp32>
+__device__ __forceinline__ f2 w_pair(const W8<kFp32>& p, int q) {
+  if constexpr (kFp32) {
+    return q == 0 ? f2_make(p.a.x, p.a.y)
+                  : (q == 1 ? f2_make(p.a.z, p.a.w)
+                            : (q == 2 ? f2_make(p.b.x, p.b.y) : f2_make(p.b.z, p.b.w)));
+  } else {
+    return bf2_to_f2(u4_get(p.u, q));
+  }
+}
+
+}  // namespace
+
+// Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdWide up to
+// 352; each + the producer warp, one CTA an SM.
+template <int VPT, int kCls, bool kFp32W>
+__global__ void __launch_bounds__(ln_max_threads(kCls), 1)
+    ln_bwd_rows_kernel(const LnBwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int H = a.H;
+  const int NV = H >> 3;
+  const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const int NW = NTg >> 5;
+  const size_t stage_elems = static_cast<size_t>(2) * G * H;  // x rows, then dy rows
+  const bool red_smem = NTg >= 32;
+  const LnSmem L = ln_smem_layout(S, 2, G, H, red_smem ? G : 0, G);
+
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kLnRedBufs][G]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kLnRedBufs][G][32]
+  float* stat = reinterpret_cast<float*>(smem + L.stat);         // [S][2][SP] mean, rstd
+  const int SP = ln_stat_stride(G);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+
+  const int tid = threadIdx.x;
+  const int ncons = G * NTg;
+  const int32_t k = blockIdx.x;
+  const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
+  const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
+  const int32_t nstage = (r1 - r0 + G - 1) / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
+    }
+    if (red_smem)
+      for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+
+  if (tid >= ncons) {  // ---- producer warp ----
+    if (tid == ncons) {
+      const uint64_t pol = l2_evict_first_policy();
+      const bool st_bulk = ((reinterpret_cast<uintptr_t>(a.mean) |
+                             reinterpret_cast<uintptr_t>(a.rstd)) & 15u) == 0;
+      int32_t j = 0;
+      for (; j < nstage; ++j) {
+        const int s = j % S;
+        if (j >= S &&
+            !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                               a.err, kErrProducerWait))
+          break;
+        const int32_t ra = r0 + j * G;
+        const int32_t rb = min(ra + G, r1);
+        // The stage's mean and rstd travel with it: the whole 16-byte blocks covering rows
+        // [ra, rb) by bulk copies (slot index r - a4), and rows past the arrays' last whole
+        // block -- or every row, when either array is not 16-byte aligned -- by 4-byte
+        // asynchronous copies that the same barrier tracks (one extra pending arrival,
+        // taken before the arrival below).
+        const int32_t a4 = ra & ~3;
+        const int32_t b4 = st_bulk ? min((rb + 3) & ~3, a.R & ~3) : a4;
+        float* md = stat + s * 2 * SP;
+        float* rd = md + SP;
+        if (rb > b4) {
+          for (int32_t r = max(ra, b4); r < rb; ++r) {
+            cp_async_4(md + (r - a4), a.mean + r);
+            cp_async_4(rd + (r - a4), a.rstd + r);
+          }
+          cp_async_mbar_arrive(&full[s]);
+        }
+        const uint32_t st_bytes = static_cast<uint32_t>(b4 - a4) * 4u;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 4u + 2u * st_bytes);
+        if (st_bytes) {
+          bulk_g2s(md, a.mean + a4, st_bytes, &full[s], pol);
+          bulk_g2s(rd, a.rstd + a4, st_bytes, &full[s], pol);
+        }
+        __nv_bfloat16* dst = ring + s * stage_elems;
+        copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
+        copy_rows_contig(dst + static_cast<size_t>(G) * H, a.dy, H, ra, rb, &full[s], pol);
+      }
+      mbar_drain(full, S, j);
+    }
+    return;
+  }
+
+  // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
+  const int g = tid / NTg;
+  const int lt = tid - g * NTg;
+  const int wg = lt >> 5, lane = tid & 31;
+  W8<kFp32W> wv[VPT];
+  f2 aw[VPT][4], cw[VPT][4], ab[VPT][4], cb[VPT][4];  // dw and db: sums, compensations
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if (c < NV) load_w8_raw<kFp32W>(a.w, c, wv[v]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      aw[v][q] = f2_splat(0.f);
+      cw[v][q] = f2_splat(0.f);
+      ab[v][q] = f2_splat(0.f);
+      cb[v][q] = f2_splat(0.f);
+    }
+  }
+  const float inv_h = 1.0f / static_cast<float>(H);
+  const int g0 = red_smem ? g : (tid & ~31) / NTg;
+  const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
+
+  float sg_carry = 0.f, sgd_carry = 0.f;  // sub-warp groups: row j-1's two sums
+  for (int32_t j = 0; j <= ng; ++j) {
+    float sg_new = 0.f, sgd_new = 0.f;
+    // ---- phase A, row j: partials of sum g and sum g*d ----
+    if (j < ng) {
+      const int32_t row = r0 + j * G + g;
+      const int s = j % S;
+      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                        kErrConsumerWait);
+      f2 ga = f2_splat(0.f), gb = f2_splat(0.f), da = f2_splat(0.f), db2 = f2_splat(0.f);
+      if (row < r1) {
+        const float mu = stat[s * 2 * SP + (row - ((r0 + j * G) & ~3))];
+        const f2 mu2 = f2_splat(mu);
+        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            const uint4 xv = lds128(st + c * 8);
+            const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), w_pair<kFp32W>(wv[v], q));
+              const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
+              if (q & 1) {
+                gb = f2_add(gb, gw);
+                db2 = f2_fma(gw, dd, db2);
+              } else {
+                ga = f2_add(ga, gw);
+                da = f2_fma(gw, dd, da);
+              }
+            }
+          }
+        }
+      }
+      const f2 gs = f2_add(ga, gb), ds = f2_add(da, db2);
+      const float pg = f2_lo(gs) + f2_hi(gs);
+      const float pgd = f2_lo(ds) + f2_hi(ds);
+      if (red_smem) {
+        const float wg_s = warp_allsum(pg);
+        const float wgd_s = warp_allsum(pgd);
+        if (lane == 0) {
+          const int rb = (j % kLnRedBufs) * G + g;
+          *reinterpret_cast<float2*>(slots + rb * 32 + 2 * wg) = make_float2(wg_s, wgd_s);
+          mbar_arrive(&redb[rb]);
+        }
+      } else {
+        sg_new = subwarp_allsum(pg, NTg);
+        sgd_new = subwarp_allsum(pgd, NTg);
+      }
+    }
+    // ---- phase B, row j-1: dx and the dw, db contributions ----
+    if (j >= 1) {
+      const int32_t jj = j - 1;
+      const int32_t row = r0 + jj * G + g;
+      const int s = jj % S;
+      float SG = sg_carry, SGD = sgd_carry;
+      if (red_smem) {
+        const int rb = (jj % kLnRedBufs) * G + g;
+        mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u, abort_flag,
+                          a.err, kErrConsumerWait);
+        const float* sl = slots + rb * 32;
+        SG = 0.f;
+        SGD = 0.f;
+        for (int i = 0; i < NW; ++i) {  // warp order: the same bits in every thread
+          const float2 p = *reinterpret_cast<const float2*>(sl + 2 * i);
+          SG += p.x;
+          SGD += p.y;
+        }
+      }
+      if (row < r1) {
+        const int base = (r0 + jj * G) & ~3;
+        const float mu = stat[s * 2 * SP + (row - base)];
+        const float rs = stat[s * 2 * SP + SP + (row - base)];
+        const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
+        const f2 c1 = f2_splat(SG * inv_h);
+        // xhat*c2 = d * (r^2 SGD / H): one product of d, so the cancelling terms meet in
+        // a single fma
+        const f2 ncr2 = f2_splat(-(SGD * (rs * inv_h)) * rs);
+        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+        const size_t out_row = static_cast<size_t>(row) * H;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            const uint4 xv = lds128(st + c * 8);
+            const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const f2 d2 = bf2_to_f2(u4_get(dv, q));
+              const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
+              const f2 gw = f2_mul(d2, w_pair<kFp32W>(wv[v], q));
+              const f2 t = f2_fma(dd, ncr2, f2_sub(gw, c1));  // g - c1 - xhat*c2, over r
+              o[q] = f2_to_bf2(f2_mul(t, rs2));
+              comp_add(aw[v][q], cw[v][q], f2_mul(f2_mul(d2, dd), rs2));  // dy * xhat
+              comp_add(ab[v][q], cb[v][q], d2);                            // dy
+            }
+            stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+    }
+    sg_carry = sg_new;
+    sgd_carry = sgd_new;
+  }
+
+  // ---- this CTA's partials: per column (hi, lo) with hi + lo == acc + cmp exactly ----
+  // part row 0 (hi) and row 1 (lo), each over dw's H columns then db's H columns
+  float* part = a.part + static_cast<size_t>(k) * 4 * H;
+  if (G == 1) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+#pragma unroll
+        for (int qty = 0; qty < 2; ++qty) {
+          f2 hi[4], lo[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2 acc = qty == 0 ? aw[v][q] : ab[v][q];
+            const f2 cmp = qty == 0 ? cw[v][q] : cb[v][q];
+            hi[q] = f2_add(acc, cmp);
+            lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
+          }
+          ulonglong2* ph = reinterpret_cast<ulonglong2*>(part + qty * H + c * 8);
+          ulonglong2* pl = reinterpret_cast<ulonglong2*>(part + 2 * H + qty * H + c * 8);
+          ph[0] = make_ulonglong2(hi[0].v, hi[1].v);
+          ph[1] = make_ulonglong2(hi[2].v, hi[3].v);
+          pl[0] = make_ulonglong2(lo[0].v, lo[1].v);
+          pl[1] = make_ulonglong2(lo[2].v, lo[3].v);
+        }
+      }
+    }
+    return;
+  }
+  // several row groups: combine them through shared memory in group order, dw then db.
+  // The ring is free once every consumer is past its loop: each stage was waited on (full)
+  // by every group that had a row in it, group 0 included, before that group finished.
+  named_bar_sync(15, ncons);
+  // cbuf: [G][2][H] (hi, lo), each H-slab as two planes of float4 (columns 0-3 and 4-7 of
+  // every vector) so that a warp's stores of one plane are contiguous
+  float* cbuf = reinterpret_cast<float*>(smem);
+#pragma unroll
+  for (int qty = 0; qty < 2; ++qty) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        f2 hi[4], lo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const f2 acc = qty == 0 ? aw[v][q] : ab[v][q];
+          const f2 cmp = qty == 0 ? cw[v][q] : cb[v][q];
+          hi[q] = f2_add(acc, cmp);
+          lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
+        }
+        ulonglong2* ph = reinterpret_cast<ulonglong2*>(cbuf + (2 * g) * H);
+        ulonglong2* pl = reinterpret_cast<ulonglong2*>(cbuf + (2 * g + 1) * H);
+        ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
+        ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
+        pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
+        pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
+      }
+    }
+    named_bar_sync(15, ncons);
+    for (int col = tid; col < H; col += ncons) {
+      const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
+      float sacc = 0.f, e = 0.f;
+      for (int gi = 0; gi < G; ++gi) {
+        float err;
+        sacc = two_sum_ln(sacc, cbuf[(2 * gi) * H + at], err);
+        e = __fadd_rn(e, __fadd_rn(err, cbuf[(2 * gi + 1) * H + at]));
+      }
+      const float hi = __fadd_rn(sacc, e);
+      part[qty * H + col] = hi;
+      part[2 * H + qty * H + col] = __fsub_rn(e, __fsub_rn(hi, sacc));
+    }
+    named_bar_sync(15, ncons);  // cbuf is rewritten by the next quantity
+  }
+}
+
+// dw[col] (col < H) and db[col - H] (col >= H) = sum over k = 0..P-1 of (hi_k + lo_k), in a
+// fixed order: slice i of the kLnFinishSlices slices takes k in [i*P/slices,
+// (i+1)*P/slices) in increasing k, then the slice sums combine by a pairwise tree in slice
+// order (i with i + stride, stride halving), TwoSum carrying the error terms throughout.
+__global__ void __launch_bounds__(kLnFinishCols* kLnFinishSlices)
+    ln_finish_kernel(const float* __restrict__ part, float* __restrict__ dw,
+                     float* __restrict__ db, int P, int H) {
+  __shared__ float sh[kLnFinishSlices][kLnFinishCols];
+  __shared__ float se[kLnFinishSlices][kLnFinishCols];
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+  const int cl = threadIdx.x % kLnFinishCols;
+  const int sl = threadIdx.x / kLnFinishCols;
+  const int col = blockIdx.x * kLnFinishCols + cl;
+  const int H2 = 2 * H;
+  const size_t row4 = static_cast<size_t>(4) * H;  // floats of one CTA's partial
+  float s = 0.f, e = 0.f;
+  if (col < H2) {
+    const int ka = (sl * P) / kLnFinishSlices;
+    const int kb = ((sl + 1) * P) / kLnFinishSlices;
+    const float* p = part + static_cast<size_t>(ka) * row4 + col;
+    int kk = ka;
+    for (; kk + 4 <= kb; kk += 4, p += 4 * row4) {
+      float hi[4], lo[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        hi[u] = p[u * row4];
+        lo[u] = p[u * row4 + H2];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float err;
+        s = two_sum_ln(s, hi[u], err);
+        e = __fadd_rn(e, __fadd_rn(err, lo[u]));
+      }
+    }
+    for (; kk < kb; ++kk, p += row4) {
+      float err;
+      s = two_sum_ln(s, p[0], err);
+      e = __fadd_rn(e, __fadd_rn(err, p[H2]));
+    }
+  }
+  sh[sl][cl] = s;
+  se[sl][cl] = e;
+  __syncthreads();
+#pragma unroll
+  for (int stride = kLnFinishSlices / 2; stride > 0; stride >>= 1) {
+    if (sl < stride) {
+      float err;
+      const float S = two_sum_ln(sh[sl][cl], sh[sl + stride][cl], err);
+      se[sl][cl] = __fadd_rn(__fadd_rn(se[sl][cl], se[sl + stride][cl]), err);
+      sh[sl][cl] = S;
+    }
+    __syncthreads();
+  }
+  if (sl == 0 && col < H2) {
+    const float out = __fadd_rn(sh[0][cl], se[0][cl]);
+    if (col < H)
+      dw[col] = out;
+    else
+      db[col - H] = out;
+  }
+}
+
+namespace {
+
+template <int VPT, int kCls>
+const void* ln_bwd_ptr_v(bool fp32w) {
+  return fp32w ? reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, true>)
+               : reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, false>);
+}
+
+// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3.
+const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
+  if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide>(fp32w);
+  return s.vpt == 1 ? ln_bwd_ptr_v<1, kLnBwdMulti>(fp32w) : ln_bwd_ptr_v<2, kLnBwdMulti>(fp32w);
+}
+
+}  // namespace
+
+}  // namespace lnorm
+
+namespace rmsn {
+cudaError_t prepare_kernel(const void* fn, size_t smem);       // rmsn_api.cu
+int blocks_per_sm(const void* fn, int threads, size_t smem);   // rmsn_api.cu
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       void** args);                           // rmsn_api.cu
+}  // namespace rmsn
+
+namespace lnorm {
+
+int ln_bwd_blocks_per_sm(const LnShape& s, bool fp32w) {
+  return rmsn::blocks_per_sm(pick_ln_bwd(s, fp32w), s.threads, s.smem);
+}
+
+cudaError_t ln_launch_bwd_rows(const LnBwdArgs& a, const LnShape& s, bool fp32w,
+                               cudaStream_t st) {
+  const void* fn = pick_ln_bwd(s, fp32w);
+  cudaError_t e = rmsn::prepare_kernel(fn, s.smem);
+  if (e != cudaSuccess) return e;
+  LnBwdArgs copy = a;
+  void* args[] = {&copy};
+  return rmsn::launch_pdl(fn, dim3(static_cast<unsigned>(a.P)),
+                          dim3(static_cast<unsigned>(s.threads)), s.smem, st, args);
+}
+
+cudaError_t ln_launch_finish(const float* part, float* dw, float* db, int P, int H,
+                             cudaStream_t st) {
+  const void* fn = reinterpret_cast<const void*>(&ln_finish_kernel);
+  void* args[] = {&part, &dw, &db, &P, &H};
+  const unsigned grid = static_cast<unsigned>((2 * H + kLnFinishCols - 1) / kLnFinishCols);
+  return rmsn::launch_pdl(fn, dim3(grid), dim3(kLnFinishCols * kLnFinishSlices), 0, st, args);
+}
+
+}  // namespace lnorm

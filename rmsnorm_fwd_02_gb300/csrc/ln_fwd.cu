@@ -1,0 +1,387 @@
+// ln_fwd.cu -- LayerNorm training forward for sm_103a.
+//
+// Per row of H elements (LayerNorm with weight w and bias b, the normalization benchmarked
+// beside RMSNorm in ROCm TransformerEngine PR #478's normalization tables; the pages give
+// no formula, so this is the textbook one):
+//   mean = (1/H) sum_j x_j,   var = (1/H) sum_j (x_j - mean)^2,   rstd = 1/sqrt(var + eps)
+//   y_j  = BF16(((x_j - mean) * rstd) * w_j + b_j)      (FP32, one fma, RNE to BF16)
+//
+// Both statistics in one reduction per row: each thread forms, for its own elements of the
+// row shifted by K (the row's first element), their sum S and the sum M of their squared
+// deviations from their own mean (two passes over its registers), and the threads'
+// (count n, S, M) triples merge pairwise by Chan, Golub and LeVeque's update (1979):
+//   S = S_a + S_b,   M = M_a + M_b + (n_b S_a - n_a S_b)^2 / (n_a n_b (n_a + n_b)).
+// Then mean = K + S/H and var = M/H.  Unlike sum(x^2) - H*mean^2 this keeps the variance's
+// accuracy when |mean| >> std; unlike a two-pass variance over the whole row it needs one
+// reduction, so the row pipeline is the RMSNorm forward's: the producer warp stages rows
+// into the ring, and split-phase rows let the reduction of row j overlap phase B
+// (normalize and store) of row j-1.
+#include "ln_launch.h"
+#include "rmsn_common.cuh"
+
+namespace lnorm {
+
+using namespace rmsn;
+
+namespace {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// The 8 weights (or biases) of one column vector, kept in registers as loaded: BF16 as one
+// uint4 of pairs (half the registers of FP32), FP32 as two float4.
+template <bool kFp32>
+struct Param8;
+template <>
+struct Param8<false> {
+  uint4 u;
+};
+template <>
+struct Param8<true> {
+  float4 a, b;
+};
+
+template <bool kFp32>
+__device__ __forceinline__ void load_param8(const void* p, int c, Param8<kFp32>& out) {
+  if constexpr (kFp32) {
+    const float4* q = reinterpret_cast<const float4*>(p) + 2 * c;
+    out.a = __ldg(q);
+    out.b = __ldg(q + 1);
+  } else {
+    out.u = __ldg(reinterpret_cast<const uint4*>(p) + c);
+  }
+}
+
+// Elements 2q and 2q+1 of a column vector's parameters, as an FP32 pair (q a constant
+// after unrolling).
+template <bool kFp32>
+__device__ __forceinline__ f2 param_pair(const Param8<kFp32>& p, int q) {
+  if constexpr (kFp32) {
+    return q == 0 ? f2_make(p.a.x, p.a.y)
+                  : (q == 1 ? f2_make(p.a.z, p.a.w)
+                            : (q == 2 ? f2_make(p.b.x, p.b.y) : f2_make(p.b.z, p.b.w)));
+  } else {
+    return bf2_to_f2(u4_get(p.u, q));
+  }
+}
+
+// The row's first element as FP32: the shift K of the row's statistics.  Taking the sums
+// of x - K (exact in FP32 when the BF16 values x and K are within a factor 2^15 of each
+// other or one is zero, else rounded once) keeps the merge's
+// rounding error proportional to |mean - K| / std instead of |mean| / std: the pairwise
+// update is first-order in that ratio (Chan, Golub and LeVeque, 1983), and K is one of the
+// row's own values.
+__device__ __forceinline__ float row_shift(const __nv_bfloat16* xs) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(xs)) << 16);
+}
+
+// Merges (S, M) over an aligned block of W lanes (W = 8, 16 or 32) by the pairwise update.
+// `n` is this lane's element count.  Both partners of a step evaluate the same expression
+// from the same two operands (addition and multiplication commute, and a - b is exactly
+// -(b - a)), so every lane of the block ends with the same bits.  With `uniform` (every
+// lane of the warp has the same count: warp-uniform) each step merges equal counts, and
+// the factor n_b^2 / (n_a n_b (n_a + n_b)) is 1/(2n): q0 = 1/(2 n0), halved per step, no
+// division.  Otherwise the counts travel with the sums and the factor is divided out.
+__device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, float q0,
+                                               bool uniform, int W) {
+  float q = q0;
+  for (int o = W >> 1; o > 0; o >>= 1) {
+    const float Sb = __shfl_xor_sync(kFullMask, S, o);
+    const float Mb = __shfl_xor_sync(kFullMask, M, o);
+    float corr;
+    if (uniform) {
+      const float d = __fsub_rn(S, Sb);
+      corr = __fmul_rn(__fmul_rn(d, d), q);
+      q = __fmul_rn(q, 0.5f);
+    } else {
+      const float nb = __shfl_xor_sync(kFullMask, n, o);
+      const float nn = __fadd_rn(n, nb);
+      const float d = __fsub_rn(__fmul_rn(nb, S), __fmul_rn(n, Sb));
+      corr = (n > 0.f && nb > 0.f)
+                 ? __fdiv_rn(__fmul_rn(d, d), __fmul_rn(__fmul_rn(n, nb), nn))
+                 : 0.f;
+      n = nn;
+    }
+    S = __fadd_rn(S, Sb);
+    M = __fadd_rn(__fadd_rn(M, Mb), corr);
+  }
+}
+
+}  // namespace
+
+// One build per vector count and parameter dtype; one CTA an SM, up to 480 consumers +
+// the producer warp (16 warps: 128 registers a thread).
+template <int VPT, bool kFp32W>
+__global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const LnFwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int H = a.H;
+  const int NV = H >> 3;
+  const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const int NW = NTg >> 5;
+  const size_t stage_elems = static_cast<size_t>(G) * H;
+  const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
+  const LnSmem L = ln_smem_layout(S, 1, G, H, red_smem ? G : 0, 0);
+
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kLnRedBufs][G]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kLnRedBufs][G][32]
+  float* wtab = reinterpret_cast<float*>(smem + L.wtab);         // [3][16]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+
+  const int tid = threadIdx.x;
+  const int ncons = G * NTg;
+  const int32_t k = blockIdx.x;
+  const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
+  const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
+  const int32_t nstage = (r1 - r0 + G - 1) / G;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
+    }
+    if (red_smem) {
+      for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
+      // per warp of a group: its element count c, the count of the warps before it, and
+      // the merge factor 1/(pre * c * (pre + c)) (0 for the first warp)
+      float pre = 0.f;
+      for (int w = 0; w < NW; ++w) {
+        int cnt = 0;
+        for (int v = 0; v < VPT; ++v) {
+          const int left = NV - v * NTg - 32 * w;
+          cnt += left <= 0 ? 0 : (left >= 32 ? 32 : left);
+        }
+        const float c = 8.f * static_cast<float>(cnt);
+        wtab[w] = c;
+        wtab[kLnMaxWarpsPerGroup + w] = pre;
+        wtab[2 * kLnMaxWarpsPerGroup + w] =
+            (pre > 0.f && c > 0.f)
+                ? static_cast<float>(1.0 / (static_cast<double>(pre) * c * (pre + c)))
+                : 0.f;
+        pre += c;
+      }
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+
+  if (tid >= ncons) {  // ---- producer warp ----
+    if (tid == ncons) {
+      const uint64_t pol = l2_evict_first_policy();
+      int32_t j = 0;
+      for (; j < nstage; ++j) {
+        const int s = j % S;
+        if (j >= S &&
+            !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                               a.err, kErrProducerWait))
+          break;
+        const int32_t ra = r0 + j * G;
+        const int32_t rb = min(ra + G, r1);
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u);
+        copy_rows_contig(ring + s * stage_elems, a.x, H, ra, rb, &full[s], pol);
+      }
+      mbar_drain(full, S, j);
+    }
+    return;
+  }
+
+  // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
+  const int g = tid / NTg;
+  const int lt = tid - g * NTg;
+  const int wg = lt >> 5, lane = tid & 31;
+  Param8<kFp32W> wv[VPT], bv[VPT];
+  int nvec = 0;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if (c < NV) {
+      load_param8<kFp32W>(a.w, c, wv[v]);
+      load_param8<kFp32W>(a.b, c, bv[v]);
+      ++nvec;
+    }
+  }
+  const float n_lane = 8.f * static_cast<float>(nvec);
+  const float inv_n = nvec ? 1.0f / n_lane : 0.f;  // 1/(2 n_lane) = inv_n / 2 exactly
+  const bool uniform = __all_sync(kFullMask, nvec == __shfl_sync(kFullMask, nvec, 0));
+  const int W = NTg < 32 ? NTg : 32;
+  const float hf = static_cast<float>(H);  // exact for H < 2^24
+  // Rows of this warp's first group: every lane of a warp runs the same iterations (the
+  // shuffles need them all); groups past the chunk's end skip the row work.
+  const int g0 = red_smem ? g : (tid & ~31) / NTg;
+  const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
+
+  float s_carry = 0.f, m_carry = 0.f;  // sub-warp groups: row j-1's merged statistics
+  for (int32_t j = 0; j <= ng; ++j) {
+    float St = 0.f, Mt = 0.f;
+    // ---- phase A, row j: this thread's sum and sum of squared deviations ----
+    if (j < ng) {
+      const int32_t row = r0 + j * G + g;
+      const int s = j % S;
+      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                        kErrConsumerWait);
+      if (row < r1) {
+        const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+        // statistics of x - K, K the row's first element (one value for the whole group)
+        const f2 K2 = f2_splat(row_shift(xs));
+        uint4 xr[VPT];
+        f2 s0 = f2_splat(0.f), s1 = f2_splat(0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          xr[v] = make_uint4(0u, 0u, 0u, 0u);
+          if (c < NV) {
+            xr[v] = lds128(xs + c * 8);
+            s0 = f2_add(s0, f2_sub(bf2_to_f2(xr[v].x), K2));
+            s1 = f2_add(s1, f2_sub(bf2_to_f2(xr[v].y), K2));
+            s0 = f2_add(s0, f2_sub(bf2_to_f2(xr[v].z), K2));
+            s1 = f2_add(s1, f2_sub(bf2_to_f2(xr[v].w), K2));
+          }
+        }
+        const f2 sp = f2_add(s0, s1);
+        St = f2_lo(sp) + f2_hi(sp);
+        const f2 m2 = f2_splat(St * inv_n);
+        f2 q0a = f2_splat(0.f), q1a = f2_splat(0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const f2 e = f2_sub(f2_sub(bf2_to_f2(u4_get(xr[v], q)), K2), m2);
+              if (q & 1)
+                q1a = f2_fma(e, e, q1a);
+              else
+                q0a = f2_fma(e, e, q0a);
+            }
+          }
+        }
+        const f2 qp = f2_add(q0a, q1a);
+        Mt = f2_lo(qp) + f2_hi(qp);
+      }
+    }
+    // ---- phase B, row j-1: mean, rstd, y ----
+    // The staged vectors go to registers and the stage is released at once; then the
+    // row's merged statistics are awaited (normally long complete), and row j's lane merge
+    // runs inside B's arithmetic.
+    if (j >= 1) {
+      const int32_t jj = j - 1;
+      const int32_t row = r0 + jj * G + g;
+      const int s = jj % S;
+      const bool valid = row < r1;
+      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      uint4 hv[VPT];
+      const float K = valid ? row_shift(xs) : 0.f;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        hv[v] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid && c < NV) hv[v] = lds128(xs + c * 8);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp has its vectors of the stage
+      float Sg = s_carry, Mg = m_carry;
+      if (red_smem) {
+        const int rb = (jj % kLnRedBufs) * G + g;
+        mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u, abort_flag,
+                          a.err, kErrConsumerWait);
+        // the warps' partials merged in warp order: the same bits in every thread
+        const float* sl = slots + rb * 32;
+        Sg = sl[0];
+        Mg = sl[1];
+        for (int i = 1; i < NW; ++i) {
+          const float2 p = *reinterpret_cast<const float2*>(sl + 2 * i);
+          const float d = __fsub_rn(__fmul_rn(wtab[i], Sg),
+                                    __fmul_rn(wtab[kLnMaxWarpsPerGroup + i], p.x));
+          const float corr = __fmul_rn(__fmul_rn(d, d), wtab[2 * kLnMaxWarpsPerGroup + i]);
+          Sg = __fadd_rn(Sg, p.x);
+          Mg = __fadd_rn(__fadd_rn(Mg, p.y), corr);
+        }
+      }
+      if (j < ng) stat_butterfly(St, Mt, n_lane, 0.5f * inv_n, uniform, W);
+      if (valid) {
+        const float mean = __fadd_rn(K, __fdiv_rn(Sg, hf));
+        const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(Mg, hf), a.eps));
+        const f2 mu2 = f2_splat(mean), rs2 = f2_splat(rs);
+        const size_t out_row = static_cast<size_t>(row) * H;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int c = lt + v * NTg;
+          if (c < NV) {
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const f2 xh = f2_mul(f2_sub(bf2_to_f2(u4_get(hv[v], q)), mu2), rs2);
+              o[q] = f2_to_bf2(f2_fma(xh, param_pair<kFp32W>(wv[v], q),
+                                      param_pair<kFp32W>(bv[v], q)));
+            }
+            stg128(a.y + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
+          }
+        }
+        if (lt == 0) {
+          a.mean[row] = mean;
+          a.rstd[row] = rs;
+        }
+      }
+    } else if (j < ng) {
+      stat_butterfly(St, Mt, n_lane, 0.5f * inv_n, uniform, W);
+    }
+    // ---- publish row j's per-warp statistics ----
+    if (j < ng && red_smem && lane == 0) {
+      const int rb = (j % kLnRedBufs) * G + g;
+      *reinterpret_cast<float2*>(slots + rb * 32 + 2 * wg) = make_float2(St, Mt);
+      mbar_arrive(&redb[rb]);
+    }
+    s_carry = St;
+    m_carry = Mt;
+  }
+}
+
+namespace {
+
+template <int VPT>
+const void* ln_fwd_ptr_v(bool fp32w) {
+  return fp32w ? reinterpret_cast<const void*>(&ln_fwd_kernel<VPT, true>)
+               : reinterpret_cast<const void*>(&ln_fwd_kernel<VPT, false>);
+}
+
+// built for 1, 2 and 4 vectors a thread
+const void* pick_ln_fwd(const LnShape& s, bool fp32w) {
+  switch (s.vpt) {
+    case 1: return ln_fwd_ptr_v<1>(fp32w);
+    case 2: return ln_fwd_ptr_v<2>(fp32w);
+    default: return ln_fwd_ptr_v<4>(fp32w);
+  }
+}
+
+}  // namespace
+
+}  // namespace lnorm
+
+namespace rmsn {
+cudaError_t prepare_kernel(const void* fn, size_t smem);       // rmsn_api.cu
+int blocks_per_sm(const void* fn, int threads, size_t smem);   // rmsn_api.cu
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       void** args);                           // rmsn_api.cu
+}  // namespace rmsn
+
+namespace lnorm {
+
+int ln_fwd_blocks_per_sm(const LnShape& s, bool fp32w) {
+  return rmsn::blocks_per_sm(pick_ln_fwd(s, fp32w), s.threads, s.smem);
+}
+
+cudaError_t ln_launch_fwd(const LnFwdArgs& a, const LnShape& s, bool fp32w, cudaStream_t st) {
+  const void* fn = pick_ln_fwd(s, fp32w);
+  cudaError_t e = rmsn::prepare_kernel(fn, s.smem);
+  if (e != cudaSuccess) return e;
+  LnFwdArgs copy = a;
+  void* args[] = {&copy};
+  return rmsn::launch_pdl(fn, dim3(static_cast<unsigned>(a.P)),
+                          dim3(static_cast<unsigned>(s.threads)), s.smem, st, args);
+}
+
+}  // namespace lnorm

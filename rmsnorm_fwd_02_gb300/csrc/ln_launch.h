@@ -1,0 +1,122 @@
+// ln_launch.h -- LayerNorm training: argument blocks, launch shapes and the shared-memory
+// carve-up of the row kernels (host + device).
+//
+// The LayerNorm kernels stage rows exactly like the RMSNorm ones (rmsn_common.cuh: one
+// producer warp, bulk asynchronous copies into an S-stage mbarrier ring, row groups of
+// threads that own fixed 16-byte column vectors, split-phase rows); what differs is the
+// per-row reduction (two quantities) and the backward's second column sum (db).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lnorm {
+
+constexpr int kLnMaxH = 8192;
+constexpr int kLnProducerThreads = 32;
+constexpr int kLnRedBufs = 4;        // rotation of the per-row reduction buffers
+constexpr int kLnMaxWarpsPerGroup = 16;
+
+// Shape classes, each its own kernel build (launch bounds = consumers + producer warp):
+//  kLnFwd       forward, up to 480 consumers, one CTA an SM (16 warps: 128 registers)
+//  kLnBwdMulti  backward with 1- or 2-vector threads, up to 480 consumers (128 registers)
+//  kLnBwdWide   backward with 3-vector threads, up to 352 consumers (12 warps, three on a
+//               scheduler partition: 168 registers), for rows past 480 2-vector threads;
+//               the dw and db running sums and their compensations take 32 registers a
+//               column vector
+enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2 };
+constexpr int ln_consumers(int cls) { return cls == kLnBwdWide ? 352 : 480; }
+constexpr int ln_max_threads(int cls) { return ln_consumers(cls) + kLnProducerThreads; }
+
+// Floats per stage of a staged per-row FP32 array (mean, rstd): the stage's `rows` values
+// start up to 3 floats into their first 16-byte block, and a slot stays whole blocks.
+__host__ __device__ constexpr int ln_stat_stride(int rows) {
+  return rows == 0 ? 0 : ((rows + 6) & ~3);
+}
+
+// Byte offsets of a row kernel's shared memory:
+//   ring   [stages][tensors][groups][H] BF16 staged rows (offset 0)
+//   full, empty   [stages] mbarriers
+//   redb   [kLnRedBufs][red_groups] mbarriers of the per-row reductions
+//   slots  [kLnRedBufs][red_groups][32] FP32: two partials per warp (2w, 2w+1)
+//   stat   [stages][2][ln_stat_stride(stat_rows)] FP32 staged mean, rstd (backward)
+//   wtab   [3][kLnMaxWarpsPerGroup] FP32 per-warp counts, prefix counts and combine
+//          factors of the forward's variance merge
+//   abort  the CTA's abort flag of the bounded waits
+struct LnSmem {
+  size_t full, empty, redb, slots, stat, wtab, abort_flag, total;
+};
+
+__host__ __device__ inline LnSmem ln_smem_layout(int stages, int tensors, int groups, int H,
+                                                 int red_groups, int stat_rows) {
+  LnSmem L;
+  size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
+  L.full = off;
+  off += 8 * static_cast<size_t>(stages);
+  L.empty = off;
+  off += 8 * static_cast<size_t>(stages);
+  L.redb = off;
+  off += 8 * kLnRedBufs * static_cast<size_t>(red_groups);
+  off = (off + 127) & ~static_cast<size_t>(127);
+  L.slots = off;
+  off += 4 * kLnRedBufs * 32 * static_cast<size_t>(red_groups);
+  L.stat = off;  // 128-byte aligned
+  off += 4 * static_cast<size_t>(stages) * 2 * ln_stat_stride(stat_rows);
+  L.wtab = off;  // 16-byte aligned
+  off += 4 * 3 * kLnMaxWarpsPerGroup;
+  L.abort_flag = off;
+  off += 16;
+  L.total = off;
+  return L;
+}
+
+struct LnShape {
+  int vpt;      // 16-byte column vectors per consumer thread
+  int ntg;      // threads per row group: 8, 16 or a multiple of 32
+  int groups;   // row groups per CTA = rows per stage
+  int stages;   // ring depth
+  int tensors;  // BF16 tensors staged per row (1 forward, 2 backward)
+  int threads;  // groups * ntg + producer warp
+  size_t smem;  // dynamic shared memory bytes
+  int cls;      // kLnFwd, kLnBwdMulti or kLnBwdWide
+};
+
+struct LnFwdArgs {
+  const __nv_bfloat16* x;  // [R, H]
+  const void* w;           // [H]
+  const void* b;           // [H], same dtype as w
+  __nv_bfloat16* y;        // [R, H]
+  float* mean;             // [R]
+  float* rstd;             // [R]
+  int32_t R, H;
+  float eps;
+  int32_t groups, ntg, stages, P;
+  unsigned* err;
+};
+
+struct LnBwdArgs {
+  const __nv_bfloat16* x;   // [R, H]
+  const __nv_bfloat16* dy;  // [R, H]
+  const float* mean;        // [R]
+  const float* rstd;        // [R]
+  const void* w;            // [H]
+  __nv_bfloat16* dx;        // [R, H]
+  float* part;              // [P][2][2H]: per CTA, (hi, lo) rows over dw's H then db's H
+  int32_t R, H;
+  int32_t groups, ntg, stages, P;
+  unsigned* err;
+};
+
+LnShape ln_fwd_shape(int H);
+LnShape ln_bwd_shape(int H);
+
+cudaError_t ln_launch_fwd(const LnFwdArgs& a, const LnShape& s, bool fp32w, cudaStream_t st);
+cudaError_t ln_launch_bwd_rows(const LnBwdArgs& a, const LnShape& s, bool fp32w,
+                               cudaStream_t st);
+cudaError_t ln_launch_finish(const float* part, float* dw, float* db, int P, int H,
+                             cudaStream_t st);
+int ln_fwd_blocks_per_sm(const LnShape& s, bool fp32w);
+int ln_bwd_blocks_per_sm(const LnShape& s, bool fp32w);
+
+}  // namespace lnorm

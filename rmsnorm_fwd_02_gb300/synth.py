@@ -150,3 +150,56 @@ def heads_strided(T: int, seed: int = 0) -> Case:
 def heads_contig(T: int, seed: int = 0) -> Case:
     """[T,4,256] contiguous, FP32 w[256]."""
     return make_case(seed, T, 256, nh=4, w_fp32=True, label=f"heads4_T{T}")
+
+
+# ---- LayerNorm beside it ----------------------------------------------------------------
+#
+# The normalization tables of ROCm TransformerEngine PR #478 benchmark LayerNorm on M rows
+# of hidden_size in BF16 (M 1024..8192; hidden 3584, 4096, 8192 and 16384, the last past
+# this library's H <= 8192).  The pages give neither eps nor distributions: eps is 1e-5
+# (the usual LayerNorm default) and the draws follow the RMSNorm recipe above, plus a bias
+# 0.1 * N(0, 1) and, optionally, a per-row offset so that some rows have |mean| >> std.
+
+LN_EPS = 1e-5
+LN_M = (1024, 2048, 4096, 8192)
+LN_H = (3584, 4096, 8192)
+
+
+@dataclass
+class LnCase:
+    """One seeded LayerNorm input set: x, dy BF16 [R, H]; w, b [H] (both BF16 or both
+    FP32)."""
+    R: int
+    H: int
+    x: np.ndarray
+    dy: np.ndarray
+    w: np.ndarray
+    b: np.ndarray
+    eps: float = LN_EPS
+    label: str = ""
+
+    @property
+    def wb_fp32(self) -> bool:
+        return self.w.dtype == np.float32
+
+
+def make_ln_case(seed: int, R: int, H: int, *, wb_fp32: bool = False,
+                 row_offset: float = 0.0, label: str = "") -> LnCase:
+    """Draw order: x, dy, w, b, then (row_offset != 0) one offset per row, scaled by
+    row_offset and added to that row of x before the rounding."""
+    rng = np.random.default_rng(seed)
+    xf = _normal(rng, R * H)
+    dyf = _normal(rng, R * H)
+    wf = (1.0 + 0.1 * _normal(rng, H)).astype(np.float32)
+    bf = (0.1 * _normal(rng, H)).astype(np.float32)
+    if row_offset != 0.0 and R > 0:
+        off = (np.float32(row_offset) * _normal(rng, R)).astype(np.float32)
+        xf = (xf.reshape(R, H) + off[:, None]).reshape(-1)
+    return LnCase(
+        R=R, H=H,
+        x=to_bf16_bits(xf),
+        dy=to_bf16_bits(dyf),
+        w=wf if wb_fp32 else to_bf16_bits(wf),
+        b=bf if wb_fp32 else to_bf16_bits(bf),
+        label=label or f"layernorm_M{R}_H{H}",
+    )

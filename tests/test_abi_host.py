@@ -30,7 +30,8 @@ def declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(HEADER_DIR, fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(rmsnorm_train_\w+)\s*\(", text, re.M)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:rmsnorm|layernorm)_train_\w+)\s*\(",
+                                text, re.M)
     return names
 
 

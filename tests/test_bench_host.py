@@ -21,6 +21,15 @@ def test_byte_model():
     assert bench.bwd_bytes(R, H, 4) == 6 * R * H + 4 * R + 4 * H + 4 * H
 
 
+def test_layernorm_byte_model():
+    R, H = 8192, 4096
+    # forward: x read, y written, w and b read, mean and rstd written
+    assert bench.ln_fwd_bytes(R, H, 2) == 2 * R * H + 2 * R * H + 2 * 2 * H + 8 * R
+    # backward: x, dy read, dx written, mean and rstd read, w read, dw and db written
+    assert bench.ln_bwd_bytes(R, H, 4) == 6 * R * H + 8 * R + 4 * H + 8 * H
+    assert all(H <= 8192 for _, H in bench.LN_SWEEP)
+
+
 def test_peak_fallback_when_no_measured_file(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
