@@ -1,18 +1,18 @@
-"""The oracle reproduces tests/golden/oracle_small.txt bit for bit.
+"""The oracles reproduce tests/golden/oracle_small.txt and layernorm_small.txt bit for bit.
 
-The fixture was written by tests/golden/make_golden.py, which calls only the oracle on
-typed-in inputs.  It catches drift of the oracle between machines (the GPU host is
+The fixtures were written by tests/golden/make_golden.py and make_golden_layernorm.py,
+which call only the oracle on typed-in inputs.  It catches drift of the oracle between machines (the GPU host is
 aarch64) and any later edit of its arithmetic.
 """
 import os
 
 import numpy as np
 
-from golden import make_golden
+from golden import make_golden, make_golden_layernorm
 
 
-def _read():
-    path = os.path.join(os.path.dirname(__file__), "golden", "oracle_small.txt")
+def _read(name="oracle_small.txt"):
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
     out = {}
     with open(path) as f:
         for line in f:
@@ -26,6 +26,14 @@ def _read():
 def test_oracle_matches_golden_bitwise():
     want = _read()
     got = make_golden.compute()
+    assert set(want) == set(got)
+    for k in want:
+        assert np.array_equal(want[k], got[k]), k
+
+
+def test_layernorm_oracle_matches_golden_bitwise():
+    want = _read("layernorm_small.txt")
+    got = make_golden_layernorm.compute()
     assert set(want) == set(got)
     for k in want:
         assert np.array_equal(want[k], got[k]), k
