@@ -18,6 +18,7 @@
  *             dw_j = sum over rows of dy_j * xhat_j,   db_j = sum over rows of dy_j  (FP32)
  *
  * Rows are contiguous: x, y, dy, dx are [R, H]; mean and rstd are [R]; w, b, dw, db [H].
+ * When R == 0 the row tensors (x, y, dy, dx, mean, rstd) may be NULL.
  * Alignment: tensor pointers 16-byte aligned except mean and rstd (4-byte; the backward
  * reads them fastest when both are 16-byte aligned); H a multiple of 8.
  * Limits: 8 <= H <= 8192 (RMSN_ERR_UNSUPPORTED above), 0 <= R < 2^31.

@@ -145,7 +145,8 @@ int layernorm_train_fwd(const void* x, const void* w, const void* b, int wb_dtyp
                         void* stream) {
   int st = check_sizes(R, H, wb_dtype);
   if (st != RMSN_OK) return st;
-  if (!x || !w || !b || !y || !mean || !rstd) return RMSN_ERR_INVALID_ARG;
+  // the row tensors may be NULL when there are no rows (nothing is read or written)
+  if (!w || !b || (R > 0 && (!x || !y || !mean || !rstd))) return RMSN_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(b) || !aligned16(y) || !aligned4(mean) ||
       !aligned4(rstd))
     return RMSN_ERR_INVALID_ARG;
@@ -207,7 +208,9 @@ int layernorm_train_bwd(const void* x, const void* dy, const float* mean, const 
                         int deterministic, void* stream) {
   int st = check_sizes(R, H, wb_dtype);
   if (st != RMSN_OK) return st;
-  if (!x || !dy || !mean || !rstd || !w || !dx || !dw || !db) return RMSN_ERR_INVALID_ARG;
+  // the row tensors may be NULL when there are no rows (dw and db are still zero-filled)
+  if (!w || !dw || !db || (R > 0 && (!x || !dy || !mean || !rstd || !dx)))
+    return RMSN_ERR_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return RMSN_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(dy) || !aligned16(w) || !aligned16(dx) || !aligned16(dw) ||
       !aligned16(db) || !aligned16(workspace) || !aligned4(mean) || !aligned4(rstd))

@@ -53,6 +53,8 @@ def bwd(lib, x=BAD_PTR, dy=BAD_PTR, mean=BAD_PTR2, rstd=BAD_PTR2, w=BAD_PTR, wd=
     (dict(eps=-1.0), INVALID),
     (dict(eps=float("nan")), INVALID),
     (dict(R=0), OK),                         # empty: nothing to do, no CUDA call
+    (dict(R=0, x=None, y=None, mean=None, rstd=None), OK),   # no rows: row tensors unused
+    (dict(R=0, w=None), INVALID),
 ])
 def test_layernorm_fwd_rejects_before_any_cuda_call(lib, kw, want):
     assert fwd(lib, **kw) == want
@@ -74,6 +76,7 @@ def test_layernorm_fwd_rejects_before_any_cuda_call(lib, kw, want):
     (dict(ws=MISALIGNED), INVALID),
     (dict(rstd=BAD_PTR2 + 1), INVALID),
     (dict(wd=7), INVALID),
+    (dict(R=0, db=None), INVALID),           # dw and db are written even with no rows
 ])
 def test_layernorm_bwd_rejects_before_any_cuda_call(lib, kw, want):
     assert bwd(lib, **kw) == want
