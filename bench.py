@@ -683,7 +683,7 @@ def run_sweep(args):
 
 # ---- LayerNorm sweep (the normalization tables' shapes: M rows of hidden_size, BF16) ------
 
-LN_SWEEP = [(M, H) for H in (3584, 4096, 8192) for M in (1024, 2048, 4096, 8192)] + [
+LN_SWEEP = [(M, H) for H in (3584, 4096, 8192, 16384) for M in (1024, 2048, 4096, 8192)] + [
     (32768, 4096), (65536, 4096), (16384, 8192)]
 
 
@@ -699,7 +699,7 @@ def ln_bwd_bytes(R: int, H: int, wbytes: int) -> int:
 
 def run_ln_sweep(args):
     """The LayerNorm forward and backward (both modes) on the normalization tables' shapes
-    (M in 1024..8192 at hidden 3584, 4096, 8192) and a few larger M, timed like run_sweep:
+    (M in 1024..8192 at hidden 3584, 4096, 8192, 16384) and a few larger M, timed like run_sweep:
     isolated (L2 flushed by a read) and back to back over rotating input sets."""
     import torch
     from rmsnorm_fwd_02_gb300 import _native as N

@@ -21,7 +21,9 @@
  * When R == 0 the row tensors (x, y, dy, dx, mean, rstd) may be NULL.
  * Alignment: tensor pointers 16-byte aligned except mean and rstd (4-byte; the backward
  * reads them fastest when both are 16-byte aligned); H a multiple of 8.
- * Limits: 8 <= H <= 8192 (RMSN_ERR_UNSUPPORTED above), 0 <= R < 2^31.
+ * Limits: 0 <= R < 2^31; H a multiple of 8 up to 8192, or a multiple of 16 up to 16384
+ * (RMSN_ERR_UNSUPPORTED otherwise).  Above 8192 a cluster of two CTAs takes each row chunk,
+ * each CTA owning half of every row's columns.
  * Errors: argument checks return a nonzero status before anything is enqueued;
  * RMSN_ERR_CUDA reports a failed launch.  rmsnorm_train_status_str names a status.
  */
@@ -84,11 +86,13 @@ int layernorm_train_bwd(const void* x, const void* dy, const float* mean, const 
  * op LN_PLAN_FWD or LN_PLAN_BWD; writes min(n_out, LN_PLAN_FIELDS) values to `out` (host
  * memory) in the order: vectors per thread, threads per row group, row groups per CTA,
  * ring stages, threads per CTA, dynamic shared memory bytes, shape class, the class's
- * maximum threads per CTA, CTAs per SM the class is built for.
+ * maximum threads per CTA, CTAs per SM the class is built for, CTAs per row chunk (1, or
+ * 2 for a cluster pair; then the other fields describe one CTA of the pair, which owns
+ * H/2 columns).
  */
 #define LN_PLAN_FWD 0
 #define LN_PLAN_BWD 1
-#define LN_PLAN_FIELDS 9
+#define LN_PLAN_FIELDS 10
 int layernorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out);
 
 /*

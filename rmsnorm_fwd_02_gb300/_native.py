@@ -47,6 +47,7 @@ PLAN_FWD, PLAN_FWD_RESIDUAL, PLAN_BWD, PLAN_BWD_DH = 0, 1, 2, 3
 LN_PLAN_FWD, LN_PLAN_BWD = 0, 1
 PLAN_FIELDS = ("vpt", "group_threads", "groups", "stages", "threads", "smem", "cls",
                "class_max_threads", "class_blocks_per_sm")
+LN_PLAN_FIELDS = PLAN_FIELDS + ("cluster_ctas",)
 
 _lib = None
 
@@ -172,11 +173,11 @@ def layernorm_train_bwd(x, dy, mean, rstd, w, wb_dtype, dx, dw, db, workspace, w
 
 def layernorm_train_launch_plan(H, op):
     """The library's LayerNorm launch plan for op LN_PLAN_FWD / LN_PLAN_BWD, as a dict."""
-    out = (C.c_int64 * len(PLAN_FIELDS))()
-    st = lib().layernorm_train_launch_plan(H, op, out, len(PLAN_FIELDS))
+    out = (C.c_int64 * len(LN_PLAN_FIELDS))()
+    st = lib().layernorm_train_launch_plan(H, op, out, len(LN_PLAN_FIELDS))
     if st != RMSN_OK:
         raise RmsnError("layernorm_train_launch_plan", st)
-    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+    return dict(zip(LN_PLAN_FIELDS, (int(v) for v in out)))
 
 
 def layernorm_train_device_error(reset=True):

@@ -52,11 +52,19 @@ int device_setup(int dev) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// Widths: multiples of 8 up to kLnMaxH (one CTA a row chunk), and multiples of 16 up to
+// kLnMaxHPair (a CTA pair, each owning a 16-byte-aligned half of every row).
+int check_width(int32_t H) {
+  if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
+  if (H > kLnMaxHPair || (H > kLnMaxH && (H % 16) != 0)) return RMSN_ERR_UNSUPPORTED;
+  return RMSN_OK;
+}
+
 int check_sizes(int64_t R, int32_t H, int wb_dtype) {
   if (R < 0) return RMSN_ERR_INVALID_ARG;
   if (wb_dtype != RMSN_W_BF16 && wb_dtype != RMSN_W_FP32) return RMSN_ERR_INVALID_ARG;
-  if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
-  if (H > kLnMaxH) return RMSN_ERR_UNSUPPORTED;
+  const int st = check_width(H);
+  if (st != RMSN_OK) return st;
   if (R > INT32_MAX - 1) return RMSN_ERR_UNSUPPORTED;
   return RMSN_OK;
 }
@@ -68,32 +76,35 @@ int group_threads(int nv, int vpt) {
   return per <= 8 ? 8 : (per <= 16 ? 16 : (per + 31) / 32 * 32);
 }
 
-// The shape of class `cls` with `vpt` vectors a thread; groups == 0 if a row does not fit.
-LnShape make_shape(int H, int tensors, int vpt, int cls) {
+// The shape of class `cls` with `vpt` vectors a thread for rows of H columns (a pair: each
+// CTA owns H/2 of them); groups == 0 if a row does not fit.
+LnShape make_shape(int H, int tensors, int vpt, int cls, bool pair) {
   LnShape s{};
-  const int nv = H / 8;
+  const int Hc = pair ? H / 2 : H;
+  const int nv = Hc / 8;
   s.vpt = vpt;
   s.cls = cls;
   s.tensors = tensors;
+  s.pair = pair ? 1 : 0;
   s.ntg = group_threads(nv, vpt);
   const int budget = ln_consumers(cls);
   if (s.ntg > budget) return s;
+  if (pair && s.ntg < 32) return s;  // a pair exchanges whole warps' partials
   s.groups = budget / s.ntg;  // sub-warp groups: a whole number of warps (budget % 32 == 0)
   if (s.ntg >= 32 && s.groups > kLnMaxWarpsPerGroup) s.groups = kLnMaxWarpsPerGroup;
   s.threads = s.groups * s.ntg + kLnProducerThreads;
-  const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
+  const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * Hc * 2;
   const int st = static_cast<int>(kLnRingTarget / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kLnMaxStages ? kLnMaxStages : st);
-  s.smem = ln_smem_layout(s.stages, tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0,
-                          tensors == 2 ? s.groups : 0)
-               .total;
+  s.smem = ln_shape_layout(s.stages, tensors, s.groups, H, s.ntg, pair).total;
   return s;
 }
 
 // Among the candidate builds: the most rows in flight (row groups), then the most threads
 // with row data, preferring shapes whose ring still holds three stages.
 LnShape pick_shape(int H, int tensors, const int (*cand)[2], int ncand) {
-  const int nv = H / 8;
+  const bool pair = H > kLnMaxH;
+  const int nv = (pair ? H / 2 : H) / 8;
   LnShape best{}, any{};
   auto busy = [nv](const LnShape& s) { return s.groups * ((nv + s.vpt - 1) / s.vpt); };
   auto better = [&](const LnShape& u, const LnShape& v) {
@@ -101,7 +112,7 @@ LnShape pick_shape(int H, int tensors, const int (*cand)[2], int ncand) {
     return u.groups != v.groups ? u.groups > v.groups : busy(u) > busy(v);
   };
   for (int i = 0; i < ncand; ++i) {
-    const LnShape s = make_shape(H, tensors, cand[i][0], cand[i][1]);
+    const LnShape s = make_shape(H, tensors, cand[i][0], cand[i][1], pair);
     if (s.groups == 0) continue;
     if (better(s, any)) any = s;
     if (s.stages >= 3 && better(s, best)) best = s;
@@ -109,15 +120,20 @@ LnShape pick_shape(int H, int tensors, const int (*cand)[2], int ncand) {
   return best.groups != 0 ? best : any;
 }
 
+// Row chunks of a launch: at most one wave -- of CTAs, or of CTA pairs on two SMs each.
+int64_t chunk_cap(int sms, int occ, bool pair) {
+  const int64_t ctas = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+  return pair ? (ctas / 2 > 0 ? ctas / 2 : 1) : ctas;
+}
+
 int bwd_partials(int32_t R, const LnShape& s, bool det, int dev, bool fp32w) {
   int64_t want = (static_cast<int64_t>(R) + s.groups - 1) / s.groups;
   if (want < 1) want = 1;
   int64_t cap;
   if (det) {
-    cap = kLnDetSMs;
+    cap = chunk_cap(kLnDetSMs, 1, s.pair != 0);
   } else {
-    const int occ = ln_bwd_blocks_per_sm(s, fp32w);
-    cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
+    cap = chunk_cap(g_sms[dev], ln_bwd_blocks_per_sm(s, fp32w), s.pair != 0);
   }
   return static_cast<int>(want < cap ? want : cap);
 }
@@ -125,8 +141,29 @@ int bwd_partials(int32_t R, const LnShape& s, bool det, int dev, bool fp32w) {
 }  // namespace
 
 LnShape ln_fwd_shape(int H) {
+  if (H > kLnMaxH) {
+    static const int pair_cand[][2] = {{4, kLnFwdPair}};
+    return pick_shape(H, 1, pair_cand, 1);
+  }
   static const int cand[][2] = {{1, kLnFwd}, {2, kLnFwd}, {4, kLnFwd}};
   return pick_shape(H, 1, cand, 3);
+}
+
+cudaError_t ln_launch_pair(const void* fn, unsigned pairs, unsigned threads, size_t smem,
+                           cudaStream_t st, void** args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 LnShape ln_bwd_shape(int H) {
@@ -159,9 +196,8 @@ int layernorm_train_fwd(const void* x, const void* w, const void* b, int wb_dtyp
 
   const bool fp32w = (wb_dtype == RMSN_W_FP32);
   const LnShape s = ln_fwd_shape(H);
-  const int occ = ln_fwd_blocks_per_sm(s, fp32w);
-  int64_t P = (R + s.groups - 1) / s.groups;
-  const int64_t cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
+  int64_t P = (R + s.groups - 1) / s.groups;  // row chunks (CTAs, or CTA pairs)
+  const int64_t cap = chunk_cap(g_sms[dev], ln_fwd_blocks_per_sm(s, fp32w), s.pair != 0);
   if (P > cap) P = cap;
 
   LnFwdArgs a{};
@@ -254,12 +290,12 @@ int layernorm_train_bwd(const void* x, const void* dy, const float* mean, const 
 
 int layernorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out) {
   if (!out || n_out < 0 || (op != LN_PLAN_FWD && op != LN_PLAN_BWD)) return RMSN_ERR_INVALID_ARG;
-  if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
-  if (H > kLnMaxH) return RMSN_ERR_UNSUPPORTED;
+  const int st = check_width(H);
+  if (st != RMSN_OK) return st;
   const LnShape s = op == LN_PLAN_BWD ? ln_bwd_shape(H) : ln_fwd_shape(H);
   const int64_t v[LN_PLAN_FIELDS] = {s.vpt,  s.ntg, s.groups, s.stages, s.threads,
                                      static_cast<int64_t>(s.smem), s.cls,
-                                     ln_max_threads(s.cls), 1};
+                                     ln_max_threads(s.cls), 1, s.pair ? 2 : 1};
   for (int i = 0; i < n_out && i < LN_PLAN_FIELDS; ++i) out[i] = v[i];
   return RMSN_OK;
 }

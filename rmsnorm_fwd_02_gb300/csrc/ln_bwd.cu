@@ -15,8 +15,8 @@
 // compensation term, and a CTA writes its partial as an unevaluated (hi, lo) FP32 pair per
 // column; the finish adds the P pairs in a fixed order with TwoSum, so dw and db are
 // bit-reproducible for a fixed partition and dx does not depend on the partition at all.
+#include "ln_common.cuh"
 #include "ln_launch.h"
-#include "rmsn_common.cuh"
 
 namespace lnorm {
 
@@ -80,31 +80,38 @@ __device__ __forceinline__ f2 w_pair(const W8<kFp32>& p, int q) {
 }  // namespace
 
 // Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdWide up to
-// 352; each + the producer warp, one CTA an SM.
-template <int VPT, int kCls, bool kFp32W>
+// 352; each + the producer warp, one CTA an SM.  kPair: the CTA is one of a cluster of two
+// that share each row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp
+// row groups only); both CTAs add the row sums of both halves in the same order.
+template <int VPT, int kCls, bool kFp32W, bool kPair>
 __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     ln_bwd_rows_kernel(const LnBwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = a.H;
-  const int NV = H >> 3;
+  const int rank = kPair ? static_cast<int>(cluster_cta_rank()) : 0;
+  const int Hc = kPair ? (H >> 1) : H;  // the columns this CTA owns
+  const int col0 = rank * Hc;
+  const int NV = Hc >> 3;
   const int G = a.groups, NTg = a.ntg, S = a.stages;
   const int NW = NTg >> 5;
-  const size_t stage_elems = static_cast<size_t>(2) * G * H;  // x rows, then dy rows
+  const int NWt = kPair ? 2 * NW : NW;  // warps whose partials a row's sums add
+  const int SF = kPair ? kLnSlotFloatsPair : kLnSlotFloats;
+  const size_t stage_elems = static_cast<size_t>(2) * G * Hc;  // x rows, then dy rows
   const bool red_smem = NTg >= 32;
-  const LnSmem L = ln_smem_layout(S, 2, G, H, red_smem ? G : 0, G);
+  const LnSmem L = ln_shape_layout(S, 2, G, H, NTg, kPair);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
   uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kLnRedBufs][G]
-  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kLnRedBufs][G][32]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kLnRedBufs][G][SF]
   float* stat = reinterpret_cast<float*>(smem + L.stat);         // [S][2][SP] mean, rstd
   const int SP = ln_stat_stride(G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
 
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
-  const int32_t k = blockIdx.x;
+  const int32_t k = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : blockIdx.x;
   const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
   const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
   const int32_t nstage = (r1 - r0 + G - 1) / G;
@@ -115,11 +122,12 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
     }
     if (red_smem)
-      for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
+      for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NWt));
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before any remote use
   pdl_wait_prior_grid();
   pdl_allow_next_grid();
 
@@ -154,16 +162,26 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
           cp_async_mbar_arrive(&full[s]);
         }
         const uint32_t st_bytes = static_cast<uint32_t>(b4 - a4) * 4u;
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 4u + 2u * st_bytes);
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * Hc * 4u + 2u * st_bytes);
         if (st_bytes) {
           bulk_g2s(md, a.mean + a4, st_bytes, &full[s], pol);
           bulk_g2s(rd, a.rstd + a4, st_bytes, &full[s], pol);
         }
         __nv_bfloat16* dst = ring + s * stage_elems;
-        copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
-        copy_rows_contig(dst + static_cast<size_t>(G) * H, a.dy, H, ra, rb, &full[s], pol);
+        if constexpr (kPair) {  // this CTA's half of each row
+          copy_half_rows(dst, a.x, H, Hc, col0, ra, rb, &full[s], pol);
+          copy_half_rows(dst + static_cast<size_t>(G) * Hc, a.dy, H, Hc, col0, ra, rb, &full[s],
+                         pol);
+        } else {
+          copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
+          copy_rows_contig(dst + static_cast<size_t>(G) * H, a.dy, H, ra, rb, &full[s], pol);
+        }
       }
       mbar_drain(full, S, j);
+    }
+    if constexpr (kPair) {
+      __syncwarp();
+      cluster_sync_all();  // neither CTA exits while its peer may still write its slots
     }
     return;
   }
@@ -203,13 +221,13 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       if (row < r1) {
         const float mu = stat[s * 2 * SP + (row - ((r0 + j * G) & ~3))];
         const f2 mu2 = f2_splat(mu);
-        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
           if (c < NV) {
             const uint4 xv = lds128(st + c * 8);
-            const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+            const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), w_pair<kFp32W>(wv[v], q));
@@ -231,9 +249,15 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       if (red_smem) {
         const float wg_s = warp_allsum(pg);
         const float wgd_s = warp_allsum(pgd);
-        if (lane == 0) {
+        if (lane == 0) {  // a pair: into both CTAs' slots
           const int rb = (j % kLnRedBufs) * G + g;
-          *reinterpret_cast<float2*>(slots + rb * 32 + 2 * wg) = make_float2(wg_s, wgd_s);
+          float* slot = slots + rb * SF + 2 * (rank * NW + wg);
+          *reinterpret_cast<float2*>(slot) = make_float2(wg_s, wgd_s);
+          if constexpr (kPair) {
+            const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
+            st_peer_f2(peer_addr(slot, peer), wg_s, wgd_s);
+            mbar_arrive_peer(peer_addr(&redb[rb], peer));
+          }
           mbar_arrive(&redb[rb]);
         }
       } else {
@@ -249,12 +273,16 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       float SG = sg_carry, SGD = sgd_carry;
       if (red_smem) {
         const int rb = (jj % kLnRedBufs) * G + g;
-        mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u, abort_flag,
-                          a.err, kErrConsumerWait);
-        const float* sl = slots + rb * 32;
+        if constexpr (kPair)
+          mbar_wait_bounded_cluster(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u,
+                                    abort_flag, a.err, kErrConsumerWait);
+        else
+          mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u, abort_flag,
+                            a.err, kErrConsumerWait);
+        const float* sl = slots + rb * SF;
         SG = 0.f;
         SGD = 0.f;
-        for (int i = 0; i < NW; ++i) {  // warp order: the same bits in every thread
+        for (int i = 0; i < NWt; ++i) {  // warp order: the same bits in every thread
           const float2 p = *reinterpret_cast<const float2*>(sl + 2 * i);
           SG += p.x;
           SGD += p.y;
@@ -269,14 +297,14 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
         // xhat*c2 = d * (r^2 SGD / H): one product of d, so the cancelling terms meet in
         // a single fma
         const f2 ncr2 = f2_splat(-(SGD * (rs * inv_h)) * rs);
-        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
-        const size_t out_row = static_cast<size_t>(row) * H;
+        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
+        const size_t out_row = static_cast<size_t>(row) * H + col0;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
           if (c < NV) {
             const uint4 xv = lds128(st + c * 8);
-            const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+            const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -301,7 +329,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 
   // ---- this CTA's partials: per column (hi, lo) with hi + lo == acc + cmp exactly ----
   // part row 0 (hi) and row 1 (lo), each over dw's H columns then db's H columns
-  float* part = a.part + static_cast<size_t>(k) * 4 * H;
+  float* part = a.part + static_cast<size_t>(k) * 4 * H + col0;  // this CTA's columns
   if (G == 1) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -326,6 +354,10 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
         }
       }
     }
+    if constexpr (kPair) {
+      __syncwarp();
+      cluster_sync_all();
+    }
     return;
   }
   // several row groups: combine them through shared memory in group order, dw then db.
@@ -349,8 +381,8 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
           hi[q] = f2_add(acc, cmp);
           lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
         }
-        ulonglong2* ph = reinterpret_cast<ulonglong2*>(cbuf + (2 * g) * H);
-        ulonglong2* pl = reinterpret_cast<ulonglong2*>(cbuf + (2 * g + 1) * H);
+        ulonglong2* ph = reinterpret_cast<ulonglong2*>(cbuf + (2 * g) * Hc);
+        ulonglong2* pl = reinterpret_cast<ulonglong2*>(cbuf + (2 * g + 1) * Hc);
         ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
         ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
         pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
@@ -358,19 +390,23 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       }
     }
     named_bar_sync(15, ncons);
-    for (int col = tid; col < H; col += ncons) {
+    for (int col = tid; col < Hc; col += ncons) {
       const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
       float sacc = 0.f, e = 0.f;
       for (int gi = 0; gi < G; ++gi) {
         float err;
-        sacc = two_sum_ln(sacc, cbuf[(2 * gi) * H + at], err);
-        e = __fadd_rn(e, __fadd_rn(err, cbuf[(2 * gi + 1) * H + at]));
+        sacc = two_sum_ln(sacc, cbuf[(2 * gi) * Hc + at], err);
+        e = __fadd_rn(e, __fadd_rn(err, cbuf[(2 * gi + 1) * Hc + at]));
       }
       const float hi = __fadd_rn(sacc, e);
       part[qty * H + col] = hi;
       part[2 * H + qty * H + col] = __fsub_rn(e, __fsub_rn(hi, sacc));
     }
     named_bar_sync(15, ncons);  // cbuf is rewritten by the next quantity
+  }
+  if constexpr (kPair) {
+    __syncwarp();
+    cluster_sync_all();
   }
 }
 
@@ -389,19 +425,19 @@ __global__ void __launch_bounds__(kLnFinishCols* kLnFinishSlices)
   const int sl = threadIdx.x / kLnFinishCols;
   const int col = blockIdx.x * kLnFinishCols + cl;
   const int H2 = 2 * H;
-  const size_t row4 = static_cast<size_t>(4) * H;  // floats of one CTA's partial
+  const int row4 = 4 * H;  // floats of one CTA's partial (P * row4 < 2^31 at every size)
   float s = 0.f, e = 0.f;
   if (col < H2) {
     const int ka = (sl * P) / kLnFinishSlices;
     const int kb = ((sl + 1) * P) / kLnFinishSlices;
-    const float* p = part + static_cast<size_t>(ka) * row4 + col;
+    int off = ka * row4 + col;
     int kk = ka;
-    for (; kk + 4 <= kb; kk += 4, p += 4 * row4) {
+    for (; kk + 4 <= kb; kk += 4, off += 4 * row4) {
       float hi[4], lo[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        hi[u] = p[u * row4];
-        lo[u] = p[u * row4 + H2];
+        hi[u] = part[off + u * row4];
+        lo[u] = part[off + u * row4 + H2];
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -410,10 +446,10 @@ __global__ void __launch_bounds__(kLnFinishCols* kLnFinishSlices)
         e = __fadd_rn(e, __fadd_rn(err, lo[u]));
       }
     }
-    for (; kk < kb; ++kk, p += row4) {
+    for (; kk < kb; ++kk, off += row4) {
       float err;
-      s = two_sum_ln(s, p[0], err);
-      e = __fadd_rn(e, __fadd_rn(err, p[H2]));
+      s = two_sum_ln(s, part[off], err);
+      e = __fadd_rn(e, __fadd_rn(err, part[off + H2]));
     }
   }
   sh[sl][cl] = s;
@@ -440,16 +476,21 @@ __global__ void __launch_bounds__(kLnFinishCols* kLnFinishSlices)
 
 namespace {
 
-template <int VPT, int kCls>
+template <int VPT, int kCls, bool kPair>
 const void* ln_bwd_ptr_v(bool fp32w) {
-  return fp32w ? reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, true>)
-               : reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, false>);
+  return fp32w ? reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, true, kPair>)
+               : reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, false, kPair>);
 }
 
-// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3.
+// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3; the pair builds
+// (half-rows of 4100..8192 columns) for 2 (multi) and 3 (wide).
 const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
-  if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide>(fp32w);
-  return s.vpt == 1 ? ln_bwd_ptr_v<1, kLnBwdMulti>(fp32w) : ln_bwd_ptr_v<2, kLnBwdMulti>(fp32w);
+  if (s.pair)
+    return s.cls == kLnBwdWide ? ln_bwd_ptr_v<3, kLnBwdWide, true>(fp32w)
+                               : ln_bwd_ptr_v<2, kLnBwdMulti, true>(fp32w);
+  if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide, false>(fp32w);
+  return s.vpt == 1 ? ln_bwd_ptr_v<1, kLnBwdMulti, false>(fp32w)
+                    : ln_bwd_ptr_v<2, kLnBwdMulti, false>(fp32w);
 }
 
 }  // namespace
@@ -476,6 +517,9 @@ cudaError_t ln_launch_bwd_rows(const LnBwdArgs& a, const LnShape& s, bool fp32w,
   if (e != cudaSuccess) return e;
   LnBwdArgs copy = a;
   void* args[] = {&copy};
+  if (s.pair)
+    return ln_launch_pair(fn, static_cast<unsigned>(a.P), static_cast<unsigned>(s.threads),
+                          s.smem, st, args);
   return rmsn::launch_pdl(fn, dim3(static_cast<unsigned>(a.P)),
                           dim3(static_cast<unsigned>(s.threads)), s.smem, st, args);
 }

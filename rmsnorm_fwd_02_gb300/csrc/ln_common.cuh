@@ -1,0 +1,90 @@
+// ln_common.cuh -- device helpers of the LayerNorm kernels beyond rmsn_common.cuh: the
+// thread-block-cluster operations of the CTA-pair builds (hidden sizes above 8192, where
+// one row's columns are split between the two CTAs of a cluster, on two SMs).
+//
+// A pair exchanges each row's per-warp partial sums through distributed shared memory: a
+// warp stores its partial into the peer CTA's reduction slots (st.shared::cluster) and
+// arrives on the peer's reduction barrier with release semantics at cluster scope; the
+// peer's waiters acquire at cluster scope.  Every remote access happens between two
+// cluster barriers: one after the barriers are initialised, one before either CTA exits.
+#pragma once
+
+#include "rmsn_common.cuh"
+
+namespace lnorm {
+
+using namespace rmsn;
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the variable at `p` (this CTA's shared memory) in the
+// CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+
+__device__ __forceinline__ void st_peer_f2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_bounded with acquire at cluster scope: the barrier's arrivals include the peer
+// CTA's, which release its stores into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_t parity,
+                                                          volatile int* abort_flag,
+                                                          unsigned* err_word, unsigned errbit) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err_word, errbit);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// All threads of both CTAs of the cluster; every thread of a warp executes it together.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Rows [ra, rb) of a row-major [R, H] BF16 tensor, columns [col0, col0 + Hc), into
+// consecutive Hc-element slots at `dst`: one bulk copy per row (the half-rows are not
+// contiguous).  Hc * 2 and col0 * 2 are multiples of 16 bytes.
+__device__ __forceinline__ void copy_half_rows(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                               int32_t H, int32_t Hc, int32_t col0, int32_t ra,
+                                               int32_t rb, uint64_t* bar, uint64_t pol) {
+  const uint32_t bytes = static_cast<uint32_t>(Hc) * 2u;
+  for (int32_t r = ra; r < rb; ++r, dst += Hc)
+    bulk_g2s(dst, src + static_cast<int64_t>(r) * H + col0, bytes, bar, pol);
+}
+
+}  // namespace lnorm

@@ -16,8 +16,8 @@
 // reduction, so the row pipeline is the RMSNorm forward's: the producer warp stages rows
 // into the ring, and split-phase rows let the reduction of row j overlap phase B
 // (normalize and store) of row j-1.
+#include "ln_common.cuh"
 #include "ln_launch.h"
-#include "rmsn_common.cuh"
 
 namespace lnorm {
 
@@ -74,6 +74,12 @@ __device__ __forceinline__ float row_shift(const __nv_bfloat16* xs) {
   return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(xs)) << 16);
 }
 
+// The same for a CTA of a pair, from the row's staged 16-byte head (element 0 in the low
+// half of the first word).
+__device__ __forceinline__ float head_shift(const uint4* h) {
+  return __uint_as_float(h->x << 16);
+}
+
 // Merges (S, M) over an aligned block of W lanes (W = 8, 16 or 32) by the pairwise update.
 // `n` is this lane's element count.  Both partners of a step evaluate the same expression
 // from the same two operands (addition and multiplication commute, and a - b is exactly
@@ -109,29 +115,40 @@ __device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, floa
 }  // namespace
 
 // One build per vector count and parameter dtype; one CTA an SM, up to 480 consumers +
-// the producer warp (16 warps: 128 registers a thread).
-template <int VPT, bool kFp32W>
-__global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const LnFwdArgs a) {
+// the producer warp (16 warps: 128 registers a thread).  kPair (class kLnFwdPair, up to
+// 256 consumers, 4-vector threads): the CTA is one of a
+// cluster of two that share each row, this one owning the columns [rank*H/2, (rank+1)*H/2)
+// (whole-warp row groups only); the two CTAs merge both halves' warp statistics, in the
+// same order, so they compute the same mean and rstd.
+template <int VPT, bool kFp32W, bool kPair>
+__global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1)
+    ln_fwd_kernel(const LnFwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int H = a.H;
-  const int NV = H >> 3;
+  const int rank = kPair ? static_cast<int>(cluster_cta_rank()) : 0;
+  const int Hc = kPair ? (H >> 1) : H;  // the columns this CTA owns
+  const int col0 = rank * Hc;
+  const int NV = Hc >> 3;
   const int G = a.groups, NTg = a.ntg, S = a.stages;
   const int NW = NTg >> 5;
-  const size_t stage_elems = static_cast<size_t>(G) * H;
+  const int NWt = kPair ? 2 * NW : NW;  // warps whose partials a row's statistics merge
+  const int SF = kPair ? kLnSlotFloatsPair : kLnSlotFloats;
+  const size_t stage_elems = static_cast<size_t>(G) * Hc;
   const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
-  const LnSmem L = ln_smem_layout(S, 1, G, H, red_smem ? G : 0, 0);
+  const LnSmem L = ln_shape_layout(S, 1, G, H, NTg, kPair);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
   uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kLnRedBufs][G]
-  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kLnRedBufs][G][32]
-  float* wtab = reinterpret_cast<float*>(smem + L.wtab);         // [3][16]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kLnRedBufs][G][SF]
+  uint4* head = reinterpret_cast<uint4*>(smem + L.head);          // [S][G] (pair)
+  float* wtab = reinterpret_cast<float*>(smem + L.wtab);         // [3][kLnWtab]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
 
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
-  const int32_t k = blockIdx.x;
+  const int32_t k = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : blockIdx.x;
   const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
   const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
   const int32_t nstage = (r1 - r0 + G - 1) / G;
@@ -142,20 +159,22 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
       mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
     }
     if (red_smem) {
-      for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
-      // per warp of a group: its element count c, the count of the warps before it, and
-      // the merge factor 1/(pre * c * (pre + c)) (0 for the first warp)
+      for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NWt));
+      // per warp of a group (of both CTAs of a pair, rank 0's first: the two halves have
+      // the same layout): its element count c, the count of the warps before it, and the
+      // merge factor 1/(pre * c * (pre + c)) (0 for the first warp)
       float pre = 0.f;
-      for (int w = 0; w < NW; ++w) {
+      for (int wt = 0; wt < NWt; ++wt) {
+        const int w = wt % NW;
         int cnt = 0;
         for (int v = 0; v < VPT; ++v) {
           const int left = NV - v * NTg - 32 * w;
           cnt += left <= 0 ? 0 : (left >= 32 ? 32 : left);
         }
         const float c = 8.f * static_cast<float>(cnt);
-        wtab[w] = c;
-        wtab[kLnMaxWarpsPerGroup + w] = pre;
-        wtab[2 * kLnMaxWarpsPerGroup + w] =
+        wtab[wt] = c;
+        wtab[kLnWtab + wt] = pre;
+        wtab[2 * kLnWtab + wt] =
             (pre > 0.f && c > 0.f)
                 ? static_cast<float>(1.0 / (static_cast<double>(pre) * c * (pre + c)))
                 : 0.f;
@@ -166,6 +185,7 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
     fence_barrier_init();
   }
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before any remote use
   pdl_wait_prior_grid();
   pdl_allow_next_grid();
 
@@ -181,10 +201,23 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
           break;
         const int32_t ra = r0 + j * G;
         const int32_t rb = min(ra + G, r1);
-        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u);
-        copy_rows_contig(ring + s * stage_elems, a.x, H, ra, rb, &full[s], pol);
+        if constexpr (kPair) {
+          // this CTA's half of each row, and each row's first 16 bytes (the shift)
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * (Hc * 2u + 16u));
+          copy_half_rows(ring + s * stage_elems, a.x, H, Hc, col0, ra, rb, &full[s], pol);
+          for (int32_t r = ra; r < rb; ++r)
+            bulk_g2s(&head[s * G + (r - ra)], a.x + static_cast<int64_t>(r) * H, 16u, &full[s],
+                     pol);
+        } else {
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u);
+          copy_rows_contig(ring + s * stage_elems, a.x, H, ra, rb, &full[s], pol);
+        }
       }
       mbar_drain(full, S, j);
+    }
+    if constexpr (kPair) {
+      __syncwarp();
+      cluster_sync_all();  // neither CTA exits while its peer may still write its slots
     }
     return;
   }
@@ -225,8 +258,9 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
                         kErrConsumerWait);
       if (row < r1) {
         const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
-        // statistics of x - K, K the row's first element (one value for the whole group)
-        const f2 K2 = f2_splat(row_shift(xs));
+        // statistics of x - K, K the row's first element (one value for the whole group,
+        // and for both CTAs of a pair)
+        const f2 K2 = f2_splat(kPair ? head_shift(&head[s * G + g]) : row_shift(xs));
         uint4 xr[VPT];
         f2 s0 = f2_splat(0.f), s1 = f2_splat(0.f);
 #pragma unroll
@@ -274,7 +308,7 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
       const bool valid = row < r1;
       const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
       uint4 hv[VPT];
-      const float K = valid ? row_shift(xs) : 0.f;
+      const float K = !valid ? 0.f : (kPair ? head_shift(&head[s * G + g]) : row_shift(xs));
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         const int c = lt + v * NTg;
@@ -286,17 +320,21 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
       float Sg = s_carry, Mg = m_carry;
       if (red_smem) {
         const int rb = (jj % kLnRedBufs) * G + g;
-        mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u, abort_flag,
-                          a.err, kErrConsumerWait);
-        // the warps' partials merged in warp order: the same bits in every thread
-        const float* sl = slots + rb * 32;
+        if constexpr (kPair)
+          mbar_wait_bounded_cluster(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u,
+                                    abort_flag, a.err, kErrConsumerWait);
+        else
+          mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kLnRedBufs) & 1u, abort_flag,
+                            a.err, kErrConsumerWait);
+        // the warps' partials merged in warp order: the same bits in every thread (of both
+        // CTAs of a pair)
+        const float* sl = slots + rb * SF;
         Sg = sl[0];
         Mg = sl[1];
-        for (int i = 1; i < NW; ++i) {
+        for (int i = 1; i < NWt; ++i) {
           const float2 p = *reinterpret_cast<const float2*>(sl + 2 * i);
-          const float d = __fsub_rn(__fmul_rn(wtab[i], Sg),
-                                    __fmul_rn(wtab[kLnMaxWarpsPerGroup + i], p.x));
-          const float corr = __fmul_rn(__fmul_rn(d, d), wtab[2 * kLnMaxWarpsPerGroup + i]);
+          const float d = __fsub_rn(__fmul_rn(wtab[i], Sg), __fmul_rn(wtab[kLnWtab + i], p.x));
+          const float corr = __fmul_rn(__fmul_rn(d, d), wtab[2 * kLnWtab + i]);
           Sg = __fadd_rn(Sg, p.x);
           Mg = __fadd_rn(__fadd_rn(Mg, p.y), corr);
         }
@@ -306,7 +344,7 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
         const float mean = __fadd_rn(K, __fdiv_rn(Sg, hf));
         const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(Mg, hf), a.eps));
         const f2 mu2 = f2_splat(mean), rs2 = f2_splat(rs);
-        const size_t out_row = static_cast<size_t>(row) * H;
+        const size_t out_row = static_cast<size_t>(row) * H + col0;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
@@ -321,7 +359,7 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
             stg128(a.y + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
           }
         }
-        if (lt == 0) {
+        if (lt == 0 && rank == 0) {
           a.mean[row] = mean;
           a.rstd[row] = rs;
         }
@@ -329,31 +367,44 @@ __global__ void __launch_bounds__(ln_max_threads(kLnFwd), 1) ln_fwd_kernel(const
     } else if (j < ng) {
       stat_butterfly(St, Mt, n_lane, 0.5f * inv_n, uniform, W);
     }
-    // ---- publish row j's per-warp statistics ----
+    // ---- publish row j's per-warp statistics (a pair: into both CTAs' slots) ----
     if (j < ng && red_smem && lane == 0) {
       const int rb = (j % kLnRedBufs) * G + g;
-      *reinterpret_cast<float2*>(slots + rb * 32 + 2 * wg) = make_float2(St, Mt);
+      const int wi = rank * NW + wg;
+      float* slot = slots + rb * SF + 2 * wi;
+      *reinterpret_cast<float2*>(slot) = make_float2(St, Mt);
+      if constexpr (kPair) {
+        const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
+        st_peer_f2(peer_addr(slot, peer), St, Mt);
+        mbar_arrive_peer(peer_addr(&redb[rb], peer));
+      }
       mbar_arrive(&redb[rb]);
     }
     s_carry = St;
     m_carry = Mt;
   }
+  if constexpr (kPair) {
+    __syncwarp();
+    cluster_sync_all();  // neither CTA exits while its peer may still write its slots
+  }
 }
 
 namespace {
 
-template <int VPT>
+template <int VPT, bool kPair>
 const void* ln_fwd_ptr_v(bool fp32w) {
-  return fp32w ? reinterpret_cast<const void*>(&ln_fwd_kernel<VPT, true>)
-               : reinterpret_cast<const void*>(&ln_fwd_kernel<VPT, false>);
+  return fp32w ? reinterpret_cast<const void*>(&ln_fwd_kernel<VPT, true, kPair>)
+               : reinterpret_cast<const void*>(&ln_fwd_kernel<VPT, false, kPair>);
 }
 
-// built for 1, 2 and 4 vectors a thread
+// built for 1, 2 and 4 vectors a thread; the pair build (half-rows of 4104..8192
+// columns) for 4
 const void* pick_ln_fwd(const LnShape& s, bool fp32w) {
+  if (s.pair) return ln_fwd_ptr_v<4, true>(fp32w);
   switch (s.vpt) {
-    case 1: return ln_fwd_ptr_v<1>(fp32w);
-    case 2: return ln_fwd_ptr_v<2>(fp32w);
-    default: return ln_fwd_ptr_v<4>(fp32w);
+    case 1: return ln_fwd_ptr_v<1, false>(fp32w);
+    case 2: return ln_fwd_ptr_v<2, false>(fp32w);
+    default: return ln_fwd_ptr_v<4, false>(fp32w);
   }
 }
 
@@ -380,6 +431,9 @@ cudaError_t ln_launch_fwd(const LnFwdArgs& a, const LnShape& s, bool fp32w, cuda
   if (e != cudaSuccess) return e;
   LnFwdArgs copy = a;
   void* args[] = {&copy};
+  if (s.pair)
+    return ln_launch_pair(fn, static_cast<unsigned>(a.P), static_cast<unsigned>(s.threads),
+                          s.smem, st, args);
   return rmsn::launch_pdl(fn, dim3(static_cast<unsigned>(a.P)),
                           dim3(static_cast<unsigned>(s.threads)), s.smem, st, args);
 }

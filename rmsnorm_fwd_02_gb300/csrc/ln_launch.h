@@ -18,15 +18,19 @@ constexpr int kLnProducerThreads = 32;
 constexpr int kLnRedBufs = 4;        // rotation of the per-row reduction buffers
 constexpr int kLnMaxWarpsPerGroup = 16;
 
-// Shape classes, each its own kernel build (launch bounds = consumers + producer warp):
+// Shape classes, each its own kernel build (and a CTA-pair build of each for widths past
+// kLnMaxH) (launch bounds = consumers + producer warp):
 //  kLnFwd       forward, up to 480 consumers, one CTA an SM (16 warps: 128 registers)
 //  kLnBwdMulti  backward with 1- or 2-vector threads, up to 480 consumers (128 registers)
 //  kLnBwdWide   backward with 3-vector threads, up to 352 consumers (12 warps, three on a
 //               scheduler partition: 168 registers), for rows past 480 2-vector threads;
 //               the dw and db running sums and their compensations take 32 registers a
 //               column vector
-enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2 };
-constexpr int ln_consumers(int cls) { return cls == kLnBwdWide ? 352 : 480; }
+//  kLnFwdPair   forward of one CTA of a pair, up to 256 consumers (9 warps: 168 registers)
+enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3 };
+constexpr int ln_consumers(int cls) {
+  return cls == kLnBwdWide ? 352 : (cls == kLnFwdPair ? 256 : 480);
+}
 constexpr int ln_max_threads(int cls) { return ln_consumers(cls) + kLnProducerThreads; }
 
 // Floats per stage of a staged per-row FP32 array (mean, rstd): the stage's `rows` values
@@ -35,23 +39,36 @@ __host__ __device__ constexpr int ln_stat_stride(int rows) {
   return rows == 0 ? 0 : ((rows + 6) & ~3);
 }
 
-// Byte offsets of a row kernel's shared memory:
-//   ring   [stages][tensors][groups][H] BF16 staged rows (offset 0)
+// Widths above kLnMaxH (up to kLnMaxHPair, multiples of 16) run as CTA pairs: a cluster of
+// two CTAs per row chunk, each owning half of every row's columns (ln_common.cuh).
+constexpr int kLnMaxHPair = 16384;
+// Reduction slot floats per row group: two per warp, for the group's warps (single CTA) or
+// for the warps of both CTAs of a pair.
+constexpr int kLnSlotFloats = 32;
+constexpr int kLnSlotFloatsPair = 64;
+constexpr int kLnWtab = 32;  // entries per row of the forward's warp-merge table
+
+// Byte offsets of a row kernel's shared memory (Hc = the columns this CTA owns: H, or H/2
+// in a pair):
+//   ring   [stages][tensors][groups][Hc] BF16 staged rows (offset 0)
 //   full, empty   [stages] mbarriers
 //   redb   [kLnRedBufs][red_groups] mbarriers of the per-row reductions
-//   slots  [kLnRedBufs][red_groups][32] FP32: two partials per warp (2w, 2w+1)
+//   slots  [kLnRedBufs][red_groups][slot_floats] FP32: two partials per warp (2w, 2w+1)
 //   stat   [stages][2][ln_stat_stride(stat_rows)] FP32 staged mean, rstd (backward)
-//   wtab   [3][kLnMaxWarpsPerGroup] FP32 per-warp counts, prefix counts and combine
-//          factors of the forward's variance merge
+//   head   [stages][head_rows] 16-byte heads of the staged rows (pair forward: the row's
+//          first element, the shift both CTAs use)
+//   wtab   [3][kLnWtab] FP32 per-warp counts, prefix counts and combine factors of the
+//          forward's variance merge
 //   abort  the CTA's abort flag of the bounded waits
 struct LnSmem {
-  size_t full, empty, redb, slots, stat, wtab, abort_flag, total;
+  size_t full, empty, redb, slots, stat, head, wtab, abort_flag, total;
 };
 
-__host__ __device__ inline LnSmem ln_smem_layout(int stages, int tensors, int groups, int H,
-                                                 int red_groups, int stat_rows) {
+__host__ __device__ inline LnSmem ln_smem_layout(int stages, int tensors, int groups, int Hc,
+                                                 int red_groups, int stat_rows,
+                                                 int slot_floats, int head_rows) {
   LnSmem L;
-  size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
+  size_t off = static_cast<size_t>(stages) * tensors * groups * Hc * 2;  // multiple of 16
   L.full = off;
   off += 8 * static_cast<size_t>(stages);
   L.empty = off;
@@ -60,11 +77,13 @@ __host__ __device__ inline LnSmem ln_smem_layout(int stages, int tensors, int gr
   off += 8 * kLnRedBufs * static_cast<size_t>(red_groups);
   off = (off + 127) & ~static_cast<size_t>(127);
   L.slots = off;
-  off += 4 * kLnRedBufs * 32 * static_cast<size_t>(red_groups);
+  off += 4 * kLnRedBufs * static_cast<size_t>(slot_floats) * red_groups;
   L.stat = off;  // 128-byte aligned
   off += 4 * static_cast<size_t>(stages) * 2 * ln_stat_stride(stat_rows);
+  L.head = off;  // 16-byte aligned
+  off += 16 * static_cast<size_t>(stages) * head_rows;
   L.wtab = off;  // 16-byte aligned
-  off += 4 * 3 * kLnMaxWarpsPerGroup;
+  off += 4 * 3 * kLnWtab;
   L.abort_flag = off;
   off += 16;
   L.total = off;
@@ -80,6 +99,7 @@ struct LnShape {
   int threads;  // groups * ntg + producer warp
   size_t smem;  // dynamic shared memory bytes
   int cls;      // kLnFwd, kLnBwdMulti or kLnBwdWide
+  int pair;     // 1: a CTA pair per row chunk, each CTA owning half the columns
 };
 
 struct LnFwdArgs {
@@ -111,11 +131,23 @@ struct LnBwdArgs {
 LnShape ln_fwd_shape(int H);
 LnShape ln_bwd_shape(int H);
 
+// Shared memory of a shape (host and kernels agree through ln_smem_layout).
+__host__ __device__ inline LnSmem ln_shape_layout(int stages, int tensors, int groups, int H,
+                                                  int ntg, bool pair) {
+  const int Hc = pair ? H / 2 : H;
+  return ln_smem_layout(stages, tensors, groups, Hc, ntg >= 32 ? groups : 0,
+                        tensors == 2 ? groups : 0, pair ? kLnSlotFloatsPair : kLnSlotFloats,
+                        pair && tensors == 1 ? groups : 0);
+}
+
 cudaError_t ln_launch_fwd(const LnFwdArgs& a, const LnShape& s, bool fp32w, cudaStream_t st);
 cudaError_t ln_launch_bwd_rows(const LnBwdArgs& a, const LnShape& s, bool fp32w,
                                cudaStream_t st);
 cudaError_t ln_launch_finish(const float* part, float* dw, float* db, int P, int H,
                              cudaStream_t st);
+// Launches `pairs` clusters of two CTAs (grid 2 * pairs) of a pair build.
+cudaError_t ln_launch_pair(const void* fn, unsigned pairs, unsigned threads, size_t smem,
+                           cudaStream_t st, void** args);
 int ln_fwd_blocks_per_sm(const LnShape& s, bool fp32w);
 int ln_bwd_blocks_per_sm(const LnShape& s, bool fp32w);
 

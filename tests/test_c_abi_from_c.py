@@ -15,7 +15,7 @@ PROGRAM = r"""
 #include "layernorm_train.h"   /* includes rmsnorm_train.h */
 
 int main(void) {
-  int64_t p[RMSN_PLAN_FIELDS];
+  int64_t p[16];
   int i;
   if (rmsnorm_train_launch_plan(4096, RMSN_PLAN_BWD, p, RMSN_PLAN_FIELDS) != RMSN_OK) return 1;
   printf("rms_bwd_plan");
@@ -31,7 +31,7 @@ int main(void) {
   printf("rms_fwd_null %d\n", rmsnorm_train_fwd(NULL, NULL, NULL, RMSN_W_BF16, NULL, NULL,
                                                 NULL, 4, 1, 64, 64, 64, 1e-6f, NULL));
   printf("ln_fwd_wide %d\n", layernorm_train_fwd(NULL, NULL, NULL, RMSN_W_BF16, NULL, NULL,
-                                                 NULL, 4, 16384, 1e-5f, NULL));
+                                                 NULL, 4, 16400, 1e-5f, NULL));
   return 0;
 }
 """
@@ -56,9 +56,9 @@ def test_c_program_links_and_sees_the_bindings_values(tmp_path, libdir):
     rp = N.rmsnorm_train_launch_plan(4096, N.PLAN_BWD)
     assert [int(v) for v in got["rms_bwd_plan"].split()] == [rp[k] for k in N.PLAN_FIELDS]
     lp = N.layernorm_train_launch_plan(4096, N.LN_PLAN_FWD)
-    assert [int(v) for v in got["ln_fwd_plan"].split()] == [lp[k] for k in N.PLAN_FIELDS]
+    assert [int(v) for v in got["ln_fwd_plan"].split()] == [lp[k] for k in N.LN_PLAN_FIELDS]
     assert int(got["rms_ws"]) == N.rmsnorm_train_bwd_workspace_bytes(65536, 1, 4096, 1)
     assert int(got["ln_ws"]) == N.layernorm_train_bwd_workspace_bytes(8192, 4096, 1)
     assert got["status3"] == N.status_str(3)
     assert int(got["rms_fwd_null"]) == 1          # RMSN_ERR_INVALID_ARG
-    assert int(got["ln_fwd_wide"]) == 2           # RMSN_ERR_UNSUPPORTED (H > 8192)
+    assert int(got["ln_fwd_wide"]) == 2           # RMSN_ERR_UNSUPPORTED (H > 16384)

@@ -138,8 +138,9 @@ def run_and_check(case, deterministic=True, misalign_stats=False):
     return dict(y_clause=n_y, dx_clause=n_dx, dx=dx, dw=dw, db=db)
 
 
-# (R, H, wb_fp32, row_offset): every build (forward 1/2/4 vectors; backward 1/2 and 3),
-# sub-warp and multi-warp row groups, ragged widths and row tails, rows with |mean| >> std
+# (R, H, wb_fp32, row_offset): every build (forward 1/2/4 vectors; backward 1/2 and 3; the
+# CTA-pair builds), sub-warp and multi-warp row groups, ragged widths and row tails, rows
+# with |mean| >> std
 PARITY = [
     (1, 8, True, 0.0),
     (7, 24, False, 0.0),
@@ -153,6 +154,10 @@ PARITY = [
     (5, 7688, False, 0.0),
     (17, 8192, True, 20.0),
     (1000, 6144, False, 1.0),
+    # past 8192: a cluster of two CTAs per row chunk, each owning half the columns
+    (33, 8208, True, 0.0),
+    (64, 12288, False, 30.0),
+    (200, 16384, True, 0.0),
 ]
 
 
@@ -162,7 +167,7 @@ def test_layernorm_parity(R, H, wf, off):
     run_and_check(case, deterministic=True)
 
 
-@pytest.mark.parametrize("M,H", [(8192, 4096), (4096, 8192), (2048, 3584)])
+@pytest.mark.parametrize("M,H", [(8192, 4096), (4096, 8192), (2048, 3584), (2048, 16384)])
 def test_layernorm_parity_benchmark_shapes(M, H):
     # the pages' table shapes (M rows of hidden_size), every element against the oracle
     case = S.make_ln_case(0, M, H)
@@ -210,7 +215,19 @@ def test_layernorm_autograd_matches_direct_calls():
     assert torch.equal(w.grad, dw2.to(w.dtype)) and torch.equal(b.grad, db2.to(b.dtype))
 
 
+def test_layernorm_pair_deterministic_bits_and_modes():
+    case = S.make_ln_case(6, 700, 16384, wb_fp32=True)
+    a = run_and_check(case, deterministic=True)
+    b = run_and_check(case, deterministic=True)
+    c = run_and_check(case, deterministic=False)
+    for k in ("dx", "dw", "db"):
+        assert torch.equal(a[k], b[k]), k
+    assert torch.equal(a["dx"], c["dx"])
+
+
 def test_layernorm_no_device_error_flags():
     case = S.make_ln_case(2, 500, 4096)
+    run_and_check(case)
+    case = S.make_ln_case(2, 100, 16384)
     run_and_check(case)
     assert N.layernorm_train_device_error(reset=True) == 0
