@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
-    if (c < NV) load_w8_raw<kFp32W>(a.w, c, wv[v]);
+    // the weights of the row's column vector col0/8 + c (a pair: this CTA's half)
+    if (c < NV) load_w8_raw<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       aw[v][q] = f2_splat(0.f);

@@ -116,10 +116,10 @@ __device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, floa
 
 // One build per vector count and parameter dtype; one CTA an SM, up to 480 consumers +
 // the producer warp (16 warps: 128 registers a thread).  kPair (class kLnFwdPair, up to
-// 256 consumers, 4-vector threads): the CTA is one of a
-// cluster of two that share each row, this one owning the columns [rank*H/2, (rank+1)*H/2)
-// (whole-warp row groups only); the two CTAs merge both halves' warp statistics, in the
-// same order, so they compute the same mean and rstd.
+// 256 consumers, 4-vector threads): the CTA is one of a cluster of two that share each
+// row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp row groups only);
+// the two CTAs merge both halves' warp statistics in the same order, so they compute the
+// same mean and rstd.
 template <int VPT, bool kFp32W, bool kPair>
 __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1)
     ln_fwd_kernel(const LnFwdArgs a) {
@@ -232,8 +232,9 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
     if (c < NV) {
-      load_param8<kFp32W>(a.w, c, wv[v]);
-      load_param8<kFp32W>(a.b, c, bv[v]);
+      // the parameters of the row's column vector col0/8 + c (a pair: this CTA's half)
+      load_param8<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
+      load_param8<kFp32W>(a.b, (col0 >> 3) + c, bv[v]);
       ++nvec;
     }
   }
