@@ -231,3 +231,31 @@ def test_layernorm_no_device_error_flags():
     case = S.make_ln_case(2, 100, 16384)
     run_and_check(case)
     assert N.layernorm_train_device_error(reset=True) == 0
+
+
+@pytest.mark.parametrize("M,H", [(1000, 4096), (300, 16384)])
+def test_layernorm_cuda_graph_replay_matches_eager(M, H):
+    # forward + deterministic backward captured once and replayed: the same bits as the
+    # eager calls (the launches take no host-side state that a replay would skip)
+    case = S.make_ln_case(13, M, H)
+    x = dev_bf16(case.x).view(M, H)
+    dy = dev_bf16(case.dy).view(M, H)
+    w, b = dev_any(case.w), dev_any(case.b)
+    y0, m0, r0 = layernorm_fwd(x, w, b)
+    dx0, dw0, db0 = layernorm_bwd(dy, x, m0, r0, w)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):   # warm-up on the capture stream
+            layernorm_fwd(x, w, b)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        y1, m1, r1 = layernorm_fwd(x, w, b)
+        dx1, dw1, db1 = layernorm_bwd(dy, x, m1, r1, w)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, c in ((y0, y1), (m0, m1), (r0, r1), (dx0, dx1), (dw0, dw1), (db0, db1)):
+        assert torch.equal(a, c)
