@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm_train.so")
 SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_small.cu",
            "ln_api.cu", "ln_fwd.cu", "ln_bwd.cu"]
-HEADERS = ["rmsn_common.cuh", "rmsn_launch.h", "ln_launch.h"]
+HEADERS = ["rmsn_common.cuh", "rmsn_launch.h", "ln_launch.h", "ln_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -43,40 +43,6 @@ __device__ __forceinline__ void comp_add(f2& acc, f2& cmp, f2 p) {
   acc = t;
 }
 
-// The 8 weights of column vector c, kept as loaded (BF16: one uint4 of pairs).
-template <bool kFp32>
-struct W8;
-template <>
-struct W8<false> {
-  uint4 u;
-};
-template <>
-struct W8<true> {
-  float4 a, b;
-};
-
-template <bool kFp32>
-__device__ __forceinline__ void load_w8_raw(const void* p, int c, W8<kFp32>& out) {
-  if constexpr (kFp32) {
-    const float4* q = reinterpret_cast<const float4*>(p) + 2 * c;
-    out.a = __ldg(q);
-    out.b = __ldg(q + 1);
-  } else {
-    out.u = __ldg(reinterpret_cast<const uint4*>(p) + c);
-  }
-}
-
-template <bool kFp32>
-__device__ __forceinline__ f2 w_pair(const W8<kFp32>& p, int q) {
-  if constexpr (kFp32) {
-    return q == 0 ? f2_make(p.a.x, p.a.y)
-                  : (q == 1 ? f2_make(p.a.z, p.a.w)
-                            : (q == 2 ? f2_make(p.b.x, p.b.y) : f2_make(p.b.z, p.b.w)));
-  } else {
-    return bf2_to_f2(u4_get(p.u, q));
-  }
-}
-
 }  // namespace
 
 // Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdWide up to
@@ -190,13 +156,13 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
-  W8<kFp32W> wv[VPT];
+  Param8<kFp32W> wv[VPT];
   f2 aw[VPT][4], cw[VPT][4], ab[VPT][4], cb[VPT][4];  // dw and db: sums, compensations
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
     // the weights of the row's column vector col0/8 + c (a pair: this CTA's half)
-    if (c < NV) load_w8_raw<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
+    if (c < NV) load_param8<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       aw[v][q] = f2_splat(0.f);
@@ -231,7 +197,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
             const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), w_pair<kFp32W>(wv[v], q));
+              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), param_pair<kFp32W>(wv[v], q));
               const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
               if (q & 1) {
                 gb = f2_add(gb, gw);
@@ -311,7 +277,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
             for (int q = 0; q < 4; ++q) {
               const f2 d2 = bf2_to_f2(u4_get(dv, q));
               const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
-              const f2 gw = f2_mul(d2, w_pair<kFp32W>(wv[v], q));
+              const f2 gw = f2_mul(d2, param_pair<kFp32W>(wv[v], q));
               const f2 t = f2_fma(dd, ncr2, f2_sub(gw, c1));  // g - c1 - xhat*c2, over r
               o[q] = f2_to_bf2(f2_mul(t, rs2));
               comp_add(aw[v][q], cw[v][q], f2_mul(f2_mul(d2, dd), rs2));  // dy * xhat

@@ -87,4 +87,42 @@ __device__ __forceinline__ void copy_half_rows(__nv_bfloat16* dst, const __nv_bf
     bulk_g2s(dst, src + static_cast<int64_t>(r) * H + col0, bytes, bar, pol);
 }
 
+// The 8 weights (or biases) of one column vector, kept in registers as loaded: BF16 as one
+// uint4 of pairs (half the registers of FP32), FP32 as two float4.
+template <bool kFp32>
+struct Param8;
+template <>
+struct Param8<false> {
+  uint4 u;
+};
+template <>
+struct Param8<true> {
+  float4 a, b;
+};
+
+// Loads column vector c (elements 8c .. 8c+7) of a BF16 or FP32 parameter array.
+template <bool kFp32>
+__device__ __forceinline__ void load_param8(const void* p, int c, Param8<kFp32>& out) {
+  if constexpr (kFp32) {
+    const float4* q = reinterpret_cast<const float4*>(p) + 2 * c;
+    out.a = __ldg(q);
+    out.b = __ldg(q + 1);
+  } else {
+    out.u = __ldg(reinterpret_cast<const uint4*>(p) + c);
+  }
+}
+
+// Elements 2q and 2q+1 of a column vector's parameters, as an FP32 pair (q a constant
+// after unrolling).
+template <bool kFp32>
+__device__ __forceinline__ f2 param_pair(const Param8<kFp32>& p, int q) {
+  if constexpr (kFp32) {
+    return q == 0 ? f2_make(p.a.x, p.a.y)
+                  : (q == 1 ? f2_make(p.a.z, p.a.w)
+                            : (q == 2 ? f2_make(p.b.x, p.b.y) : f2_make(p.b.z, p.b.w)));
+  } else {
+    return bf2_to_f2(u4_get(p.u, q));
+  }
+}
+
 }  // namespace lnorm
