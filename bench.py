@@ -699,7 +699,9 @@ def ln_bwd_bytes(R: int, H: int, wbytes: int) -> int:
 
 def run_ln_sweep(args):
     """The LayerNorm forward and backward (both modes) on the normalization tables' shapes
-    (M in 1024..8192 at hidden 3584, 4096, 8192, 16384) and a few larger M, timed like run_sweep:
+    (M in 1024..8192 at hidden 3584, 4096, 8192, 16384) and a few larger M, with RMSNorm's
+    forward and deterministic backward on the same inputs beside them (H <= 8192), timed
+    like run_sweep:
     isolated (L2 flushed by a read) and back to back over rotating input sets."""
     import torch
     from rmsnorm_fwd_02_gb300 import _native as N
@@ -765,6 +767,29 @@ def run_ln_sweep(args):
 
             rows.append(("ln_bwd_det" if det else "ln_bwd_nondet", bwd,
                          ln_bwd_bytes(M, H, wbytes)))
+        if H <= 8192:
+            # RMSNorm on the same rows, weight and gradient (the tables put the two norms
+            # side by side): forward, and the deterministic backward on its rstd
+            nws_r = N.rmsnorm_train_bwd_workspace_bytes(M, 1, H, 1)
+            ws_r = torch.empty(max(nws_r, 16), dtype=torch.uint8, device=dev)
+
+            def rms_fwd(i):
+                q = sets[i]
+                st = lib.rmsnorm_train_fwd(q["x"].data_ptr(), None, w.data_ptr(), wd,
+                                           q["y"].data_ptr(), None, q["rstd"].data_ptr(),
+                                           M, 1, H, H, H, 1e-6, sh)
+                assert st == 0, st
+
+            def rms_bwd(i):
+                q = sets[i]
+                st = lib.rmsnorm_train_bwd(q["x"].data_ptr(), q["dy"].data_ptr(), None,
+                                           q["rstd"].data_ptr(), w.data_ptr(), wd,
+                                           q["dx"].data_ptr(), q["dw"].data_ptr(),
+                                           ws_r.data_ptr(), nws_r, M, 1, H, H, H, 1, sh)
+                assert st == 0, st
+
+            rows.append(("rms_fwd", rms_fwd, fwd_bytes(M, H, wbytes)))
+            rows.append(("rms_bwd_det", rms_bwd, bwd_bytes(M, H, wbytes)))
         if args.sweep_once:
             torch.cuda.synchronize()
             rows[1][1](0)
