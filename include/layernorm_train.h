@@ -60,9 +60,9 @@ int layernorm_train_fwd(const void* x, const void* w, const void* b, int wb_dtyp
 size_t layernorm_train_bwd_workspace_bytes(int64_t R, int32_t H, int deterministic);
 
 /*
- * Backward: dx (BF16), dw and db (FP32).  dw and db are compensated FP32 partial sums per
- * CTA added in a fixed order, held to the same per-element budget as the RMSNorm dw
- * (atol 1e-4 + rtol 1e-4 of an FP64 sum).
+ * Backward: dx (BF16), dw and db (FP32): per-CTA partial sums (dw's compensated) added in
+ * a fixed order, held to the same per-element budget as the RMSNorm dw (atol 1e-4 +
+ * rtol 1e-4 of an FP64 sum).
  *   x          BF16 [R, H], the forward's input
  *   dy         BF16 [R, H], upstream gradient of y
  *   mean, rstd FP32 [R] as returned by the forward

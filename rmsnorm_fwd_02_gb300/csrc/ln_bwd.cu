@@ -11,10 +11,13 @@
 // The two row sums (sum g, sum g*d) travel together through one reduction per row, so the
 // pipeline is the RMSNorm backward's: a producer warp stages x, dy and the rows' mean and
 // rstd; phase A of row j forms the partial sums; phase B of row j-1 writes dx and adds the
-// row to the thread's dw and db running sums.  Each running sum carries a Fast2Sum
-// compensation term, and a CTA writes its partial as an unevaluated (hi, lo) FP32 pair per
-// column; the finish adds the P pairs in a fixed order with TwoSum, so dw and db are
-// bit-reproducible for a fixed partition and dx does not depend on the partition at all.
+// row to the thread's dw and db running sums.  dw's running sum carries a Fast2Sum
+// compensation term (plain FP32 sums of dy * xhat over a CTA's few hundred rows drift past
+// the per-element budget); db's does not need one (its terms are BF16 values, which add
+// almost exactly in FP32).  A CTA writes its partial as an unevaluated (hi, lo) FP32 pair
+// per column (db: lo = 0); the finish adds the P pairs in a fixed order with TwoSum, so dw
+// and db are bit-reproducible for a fixed partition and dx does not depend on the partition
+// at all.
 #include "ln_common.cuh"
 #include "ln_launch.h"
 
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
   Param8<kFp32W> wv[VPT];
-  f2 aw[VPT][4], cw[VPT][4], ab[VPT][4], cb[VPT][4];  // dw and db: sums, compensations
+  f2 aw[VPT][4], cw[VPT][4], ab[VPT][4];  // dw: sum and compensation; db: sum
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
@@ -168,7 +171,6 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       aw[v][q] = f2_splat(0.f);
       cw[v][q] = f2_splat(0.f);
       ab[v][q] = f2_splat(0.f);
-      cb[v][q] = f2_splat(0.f);
     }
   }
   const float inv_h = 1.0f / static_cast<float>(H);
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
               const f2 t = f2_fma(dd, ncr2, f2_sub(gw, c1));  // g - c1 - xhat*c2, over r
               o[q] = f2_to_bf2(f2_mul(t, rs2));
               comp_add(aw[v][q], cw[v][q], f2_mul(f2_mul(d2, dd), rs2));  // dy * xhat
-              comp_add(ab[v][q], cb[v][q], d2);                            // dy
+              ab[v][q] = f2_add(ab[v][q], d2);                             // dy
             }
             stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
           }
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const f2 acc = qty == 0 ? aw[v][q] : ab[v][q];
-            const f2 cmp = qty == 0 ? cw[v][q] : cb[v][q];
+            const f2 cmp = qty == 0 ? cw[v][q] : f2_splat(0.f);
             hi[q] = f2_add(acc, cmp);
             lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
           }
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const f2 acc = qty == 0 ? aw[v][q] : ab[v][q];
-          const f2 cmp = qty == 0 ? cw[v][q] : cb[v][q];
+          const f2 cmp = qty == 0 ? cw[v][q] : f2_splat(0.f);
           hi[q] = f2_add(acc, cmp);
           lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
         }
