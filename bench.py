@@ -222,7 +222,8 @@ def d2d_copy_gbps(torch, dev, stream, nbytes: int = 1 << 30, reps: int = 10) -> 
 # ---- the CPU oracle baseline ------------------------------------------------------------
 
 def oracle_step(case, rows: np.ndarray):
-    """One forward + backward of the FP64 oracle over the rows `rows` of `case`."""
+    """One forward + backward of the FP64 oracle over the rows `rows` of `case` (plain
+    rows).  Returns the block's dw (the sum over its rows)."""
     import oracle
     H = case.H
     sub_x = case.x.reshape(-1, H)[rows].reshape(-1)
@@ -231,28 +232,71 @@ def oracle_step(case, rows: np.ndarray):
     _, r64, _ = oracle.fwd(sub_x, case.w, case.eps, n, 1, H, H, H)
     r_in = r64.astype(np.float32).astype(np.float64)
     oracle.bwd_dx(sub_x, sub_dy, r_in, case.w, n, 1, H, H, H)
-    oracle.bwd_dw(sub_x, sub_dy, r_in, n, 1, H, H, H)
+    return oracle.bwd_dw(sub_x, sub_dy, r_in, n, 1, H, H, H)
 
 
-def cpu_baseline(case, wbytes: int, budget_s: float = 10.0, rows_per_step: int = 64):
-    rng = np.random.default_rng(1)
-    rows = np.sort(rng.choice(case.R, size=min(rows_per_step, case.R), replace=False))
-    n_steps = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle_step(case, rows)
-        n_steps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    nbytes = (fwd_bytes(rows.size, case.H, wbytes) + bwd_bytes(rows.size, case.H, wbytes))
+class OracleRunner:
+    """Times the oracle as it stands on this host's cores: one thread per row block (the
+    oracle's C functions run without the GIL), each block's forward, dx and dw by the
+    oracle itself, the blocks' dw added in block order afterwards.  The row blocks split
+    a fixed random sample of the workload's rows."""
+
+    def __init__(self, case, rows_per_thread: int, threads: int | None = None):
+        from concurrent.futures import ThreadPoolExecutor
+        self.case = case
+        self.threads = max(1, threads or (os.cpu_count() or 1))
+        n = min(rows_per_thread * self.threads, case.R)
+        rng = np.random.default_rng(1)
+        rows = np.sort(rng.choice(case.R, size=n, replace=False))
+        self.blocks = [b for b in np.array_split(rows, self.threads) if b.size]
+        self.rows = int(rows.size)
+        self.pool = ThreadPoolExecutor(max_workers=self.threads) if self.threads > 1 else None
+
+    def step(self):
+        if self.pool is None:
+            parts = [oracle_step(self.case, b) for b in self.blocks]
+        else:
+            parts = list(self.pool.map(lambda b: oracle_step(self.case, b), self.blocks))
+        dw = parts[0]
+        for p in parts[1:]:
+            dw = dw + p
+        return dw
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+
+def cpu_baseline(case, wbytes: int, budget_s: float = 10.0, rows_per_thread: int = 64):
+    """The oracle's forward + backward throughput on this host, single-threaded and on all
+    cores (each for about half of `budget_s`)."""
+    out = {}
+    for threads in (1, os.cpu_count() or 1):
+        runner = OracleRunner(case, rows_per_thread, threads)
+        n_steps = 0
+        t0 = time.perf_counter()
+        while True:
+            runner.step()
+            n_steps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s / 2:
+                break
+        runner.close()
+        nbytes = fwd_bytes(runner.rows, case.H, wbytes) + bwd_bytes(runner.rows, case.H, wbytes)
+        out[threads] = (nbytes * n_steps / el / 1e9, n_steps, runner.rows, el)
+    cores = max(out)
+    v, n_steps, rows, el = out[cores]
+    v1, n1, rows1, el1 = out[1]
     return {
-        "value": nbytes * n_steps / el / 1e9,
+        "value": v,
         "unit": "GB/s",
-        "cores": 1,
+        "cores": cores,
+        "host_cpu_count": os.cpu_count(),
+        "single_thread_value": v1,
         "kind": "oracle",
-        "sample": (f"{n_steps} x forward+backward of {rows.size} random rows of the "
-                   f"[{case.T},{case.H}] workload, {el:.1f} s single-threaded FP64"),
+        "sample": (f"{n_steps} x forward+backward of {rows} random rows of the "
+                   f"[{case.T},{case.H}] workload in {cores} row blocks on {cores} threads "
+                   f"({el:.1f} s); single-threaded: {n1} x {rows1} rows ({el1:.1f} s); FP64"),
     }
 
 
@@ -265,24 +309,26 @@ def run_reference(args):
     from rmsnorm_fwd_02_gb300 import synth
     case = synth.make_case(0, args.T, args.H)
     wbytes = 2
-    rows = np.arange(min(64, case.R), dtype=np.int64)
+    runner = OracleRunner(case, rows_per_thread=64)
     for _ in range(args.warmup):
-        oracle_step(case, rows)
+        runner.step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(case, rows)
+        runner.step()
     el = time.perf_counter() - t0
-    nbytes = fwd_bytes(rows.size, case.H, wbytes) + bwd_bytes(rows.size, case.H, wbytes)
+    runner.close()
+    nbytes = fwd_bytes(runner.rows, case.H, wbytes) + bwd_bytes(runner.rows, case.H, wbytes)
     value = nbytes * args.steps / el / 1e9
-    sample = f"each step: forward+backward of {rows.size} rows of [{args.T},{args.H}]"
+    sample = (f"each step: forward+backward of {runner.rows} random rows of "
+              f"[{args.T},{args.H}] in {runner.threads} row blocks on {runner.threads} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": runner.threads,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -299,6 +345,25 @@ def workload_config(args):
         "deterministic": not args.nondet,
         "l2": "inputs larger than L2 (no flush): 2*T*H bytes per tensor",
     }
+
+
+def target_summary(configs, target=0.75):
+    """The cells at T >= 8192 whose forward or backward (either mode, either clock) falls
+    below `target` of the peak; the configurations' stated goal is none."""
+    if not configs:
+        return None
+    below, n = [], 0
+    for name, ops in configs.items():
+        T = int(name.split("_T")[1].split("_")[0])
+        if T < 8192:
+            continue
+        for op, r in ops.items():
+            n += 1
+            worst = min(r["frac"], r["stream_frac"])
+            if worst < target:
+                below.append({"cell": name, "op": op, "frac": r["frac"],
+                              "stream_frac": r["stream_frac"]})
+    return {"target_frac": target, "ops_checked": n, "below": below}
 
 
 # ---- our arm -------------------------------------------------------------------------------
@@ -370,8 +435,10 @@ def run_ours(args):
     barrier(dist)
     total_ms = t_begin.elapsed_time(t_end)
 
-    # ---- device-timed region 2: the same steps with events around each op ----
-    k2 = min(args.steps, 500)
+    # ---- device-timed region 2: the same steps with events around each op (at least
+    # about a second of them, so the clock sampler sees the GPU under load) ----
+    k2 = max(min(args.steps, 500), int(args.min_op_seconds / max(total_ms / args.steps * 1e-3,
+                                                                  1e-6)))
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k2)]
     torch.cuda.synchronize()
     for i in range(k2):
@@ -381,10 +448,22 @@ def run_ours(args):
         bwd_call(xp, dyp, wp, dxp, rp, dwp)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    wall1 = time.time()
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    clocks = sampler.summary(wall0, wall1) if sampler else None
+
+    # ---- every configuration's cells at T >= 8192 (and the tiny one), each op timed
+    # isolated and back to back (time_cell); rank 0 only, still under the clock sampler ----
+    configs = None
+    if rank == 0 and not args.skip_configs:
+        env = _cell_env(torch, N, dev, stream)
+        configs = {}
+        for cell in CONFIG_CELLS:
+            configs[cell_name(cell)] = {r.pop("op"): r for r in time_cell(env, cell,
+                                                                          args.config_reps)}
+        del env
+        torch.cuda.empty_cache()
+    wall2 = time.time()
+    clocks = sampler.summary(wall0, wall2) if sampler else None
     if sampler:
         sampler.stop()
     max_ms = reduce_max(total_ms, dist)
@@ -489,37 +568,94 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 3 * args.steps,  # fwd + bwd row pass + dw finish per step
         "clocks": clocks,
+        "configs": configs,
+        "configs_target": target_summary(configs),
         "source_hash": kernel_source_hash(),
     }
     print(json.dumps(line))
     return 0
 
 
-# ---- per-workload sweep (one JSON line per op and workload; not the headline) -----------
+# ---- per-cell timing: the default run's per-configuration table and the sweep ----------
 
+# The configurations' cells with T >= 8192 (where the 75 %-of-peak target applies) and the
+# tiny one: name, T, H, heads, buffer heads, FP32 weight, residual form, outlier rows.
+CONFIG_CELLS = (
+    [("tiny", 64, 256, 1, None, True, False, 0.0)]
+    + [("plain", T, 4096, 1, None, False, False, 0.0) for T in (16384, 65536)]
+    + [("stress", T, H, 1, None, True, False, 0.01)
+       for H in (1536, 2048, 5120) for T in (32768, 65536, 98304, 131072)]
+    + [("residual", T, 6144, 1, None, False, True, 0.0) for T in (30720, 65536)]
+    + [("heads24of32", 65536, 256, 24, 32, True, False, 0.0),
+       ("heads4", 65536, 256, 4, None, True, False, 0.0)]
+)
+
+# --sweep: the same families at more row counts (label, T, H, nh, buf_heads, w_fp32,
+# residual, outlier rows)
 SWEEP = [
-    # label, T, H, nh, buf_heads, w_fp32, residual
-    ("plain", 16384, 4096, 1, None, False, False),
-    ("plain", 65536, 4096, 1, None, False, False),
-    ("stress", 32768, 1536, 1, None, True, False),
-    ("stress", 65536, 1536, 1, None, True, False),
-    ("stress", 131072, 1536, 1, None, True, False),
-    ("stress", 32768, 2048, 1, None, True, False),
-    ("stress", 131072, 2048, 1, None, True, False),
-    ("stress", 32768, 5120, 1, None, True, False),
-    ("stress", 131072, 5120, 1, None, True, False),
-    ("residual", 30720, 6144, 1, None, False, True),
-    ("residual", 65536, 6144, 1, None, False, True),
-    ("heads24of32", 4096, 256, 24, 32, True, False),
-    ("heads24of32", 16384, 256, 24, 32, True, False),
-    ("heads24of32", 65536, 256, 24, 32, True, False),
-    ("heads4", 65536, 256, 4, None, True, False),
+    ("plain", 16384, 4096, 1, None, False, False, 0.0),
+    ("plain", 65536, 4096, 1, None, False, False, 0.0),
+    ("stress", 32768, 1536, 1, None, True, False, 0.01),
+    ("stress", 65536, 1536, 1, None, True, False, 0.01),
+    ("stress", 131072, 1536, 1, None, True, False, 0.01),
+    ("stress", 32768, 2048, 1, None, True, False, 0.01),
+    ("stress", 131072, 2048, 1, None, True, False, 0.01),
+    ("stress", 32768, 5120, 1, None, True, False, 0.01),
+    ("stress", 131072, 5120, 1, None, True, False, 0.01),
+    ("residual", 30720, 6144, 1, None, False, True, 0.0),
+    ("residual", 65536, 6144, 1, None, False, True, 0.0),
+    ("heads24of32", 4096, 256, 24, 32, True, False, 0.0),
+    ("heads24of32", 16384, 256, 24, 32, True, False, 0.0),
+    ("heads24of32", 65536, 256, 24, 32, True, False, 0.0),
+    ("heads4", 65536, 256, 4, None, True, False, 0.0),
 ]
 
+L2_BYTES = 129 << 20
 
-def _sweep_timers(torch, stream, flush):
-    """The sweep's two clocks (see run_sweep): isolated launches after a read-based L2
-    flush, and launches back to back over rotating input sets."""
+
+def device_case(torch, dev, T, H, nh=1, buf_heads=None, w_fp32=False, residual=False,
+                outlier_frac=0.0, seed=0):
+    """Timing inputs drawn on the device by torch's seeded generator, with the
+    configurations' distributions (x, residual, dy, dh ~ N(0,1) rounded to BF16; w =
+    1 + 0.1*N(0,1); outlier rows x16).  Parity is the tests' job: these only need the
+    shapes and value ranges, and drawing them on the device keeps the run short."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    bh = buf_heads or nh
+
+    def draw(n):
+        return torch.randn(n, generator=g, device=dev, dtype=torch.float32)
+
+    x = draw(T * bh * H)
+    if outlier_frac > 0.0 and T > 0:
+        n = max(1, int(round(outlier_frac * T * nh)))
+        rows = torch.randperm(T * nh, generator=g, device=dev)[:n]
+        xv = x.view(T, bh, H)
+        xv[rows // nh, rows % nh] *= 16.0
+    d = {"x": x.to(torch.bfloat16)}
+    del x
+    if residual:
+        d["res"] = draw(T * bh * H).to(torch.bfloat16)
+    d["dy"] = draw(T * nh * H).to(torch.bfloat16)
+    if residual:
+        d["dh"] = draw(T * nh * H).to(torch.bfloat16)
+    w = 1.0 + 0.1 * draw(H)
+    d["w"] = w if w_fp32 else w.to(torch.bfloat16)
+    return d
+
+
+def _cell_timers(torch, stream, flush):
+    """Two clocks, CUDA events on the launch stream:
+
+    isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
+              The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
+              flush would leave dirty lines whose write-back lands inside the next timed
+              kernel).  Includes the launch's ramp-up and tail and the gap before the first
+              CTA starts.
+    stream    `reps` launches back to back inside one event pair, rotating over copies of
+              the inputs and outputs so that every launch finds its inputs out of L2 (the
+              sets in between exceed twice the L2); time / launches.  This is the op as a
+              training step runs it, queued behind other work."""
 
     def timed(fn, reps):
         out = []
@@ -557,127 +693,120 @@ def _sweep_timers(torch, stream, flush):
     return timed, timed_stream
 
 
-def run_sweep(args):
-    """Times each op of each workload (forward; backward in both modes, with and without dh
-    in the residual form; the checkpointed step 2xfwd+bwd = forward, forward recompute,
-    deterministic backward) two ways, CUDA events on the launch stream:
+def time_cell(env, cell, reps, ckpt=False, once=False):
+    """Times every op of one cell (forward; backward in both modes, with and without dh in
+    the residual form; with ckpt the checkpointed step 2xfwd+bwd = forward, forward
+    recompute, deterministic backward) with both clocks of _cell_timers.  Returns one
+    record per op.  With once, runs each op once, untimed (for a profiler)."""
+    torch, N, lib, dev, stream, flush, peak, peak_kind = env
+    _, T, H, nh, bh, w32, res, outl = cell
+    sh = stream.cuda_stream
+    R = T * nh
+    wbytes = 4 if w32 else 2
+    wd = N.RMSN_W_FP32 if w32 else N.RMSN_W_BF16
+    base = device_case(torch, dev, T, H, nh, bh, w32, res, outl)
+    w = base.pop("w")
+    s_tok_in, s_head_in = (bh or nh) * H, H
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values()) + 3 * R * H * 2
+    nsets = 1 if once or set_bytes >= 2 * L2_BYTES else -(-2 * L2_BYTES // set_bytes) + 1
+    sets = []
+    for i in range(nsets):
+        q = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        q["y"] = torch.empty(R * H, dtype=torch.bfloat16, device=dev)
+        q["h"] = torch.empty_like(q["y"]) if res else None
+        q["dx"] = torch.empty_like(q["y"])
+        q["rstd"] = torch.empty(R, dtype=torch.float32, device=dev)
+        q["dw"] = torch.empty(H, dtype=torch.float32, device=dev)
+        sets.append(q)
 
-    isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
-              The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
-              flush would leave dirty lines whose write-back lands inside the next timed
-              kernel).  Includes the launch's ramp-up and tail and the gap before the first
-              CTA starts.
-    stream    `reps` launches back to back inside one event pair, rotating over copies of
-              the inputs and outputs so that every launch finds its inputs out of L2 (the
-              sets in between exceed twice the L2); time / launches.  This is the op as a
-              training step runs it, queued behind other work."""
+    def fwd(i):
+        q = sets[i]
+        st = lib.rmsnorm_train_fwd(q["x"].data_ptr(), q["res"].data_ptr() if res else None,
+                                   w.data_ptr(), wd, q["y"].data_ptr(),
+                                   q["h"].data_ptr() if res else None, q["rstd"].data_ptr(),
+                                   T, nh, H, s_tok_in, s_head_in, 1e-6, sh)
+        assert st == 0, st
+
+    for i in range(nsets):
+        fwd(i)
+    s_tok, s_head = (nh * H, H) if res else (s_tok_in, s_head_in)
+    fwd_b = (8 if res else 4) * R * H + 4 * R + wbytes * H
+    ops = [("fwd", fwd, fwd_b)]
+    for det in (1, 0):
+        nws = N.rmsnorm_train_bwd_workspace_bytes(T, nh, H, det)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+        for use_dh in ((False, True) if res else (False,)):
+            def bwd(i, det=det, use_dh=use_dh, ws=ws, nws=nws):
+                q = sets[i]
+                xs = q["h"] if res else q["x"]
+                st = lib.rmsnorm_train_bwd(xs.data_ptr(), q["dy"].data_ptr(),
+                                           q["dh"].data_ptr() if use_dh else None,
+                                           q["rstd"].data_ptr(), w.data_ptr(), wd,
+                                           q["dx"].data_ptr(), q["dw"].data_ptr(),
+                                           ws.data_ptr(), nws, T, nh, H, s_tok, s_head,
+                                           det, sh)
+                assert st == 0, st
+
+            name = ("bwd_det" if det else "bwd_nondet") + ("+dh" if use_dh else "")
+            bwd_b = (8 if use_dh else 6) * R * H + 4 * R + wbytes * H + 4 * H
+            ops.append((name, bwd, bwd_b))
+            if ckpt and det and not use_dh:
+                def step(i, bwd=bwd):
+                    fwd(i)
+                    fwd(i)
+                    bwd(i)
+
+                ops.append(("2xfwd+bwd_det", step, 2 * fwd_b + bwd_b))
+    timed, timed_stream = _cell_timers(torch, stream, flush)
+    out = []
+    for name, fn, nbytes in ops:
+        if once:
+            fn(0)
+            torch.cuda.synchronize()
+            out.append({"op": name, "ran_once": True})
+            continue
+        us = timed(fn, reps)
+        us_s = timed_stream(fn, nsets, reps)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        gbs_s = nbytes / (us_s * 1e-6) / 1e9
+        out.append({"op": name, "us": round(us, 2), "GBps": round(gbs, 1),
+                    "frac": round(gbs / peak, 4), "stream_us": round(us_s, 2),
+                    "stream_GBps": round(gbs_s, 1), "stream_frac": round(gbs_s / peak, 4),
+                    "input_sets": nsets, "bytes": nbytes})
+    del sets, base, w
+    torch.cuda.empty_cache()
+    return out
+
+
+def cell_name(cell):
+    label, T, H = cell[0], cell[1], cell[2]
+    return f"{label}_T{T}_H{H}"
+
+
+def _cell_env(torch, N, dev, stream):
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
+    peak, peak_kind = measured_peak()
+    return (torch, N, N.lib(), dev, stream, flush, peak, peak_kind)
+
+
+def run_sweep(args):
+    """Times each op of each workload of SWEEP (one JSON line per op) with time_cell's two
+    clocks; --sweep-once runs each op once, untimed."""
     import torch
     from rmsnorm_fwd_02_gb300 import _native as N
-    from rmsnorm_fwd_02_gb300 import synth
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    lib = N.lib()
-    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
-    peak, peak_kind = measured_peak()
-    l2_bytes = 129 << 20
-
-    def dbf(bits):
-        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
-
-    timed, timed_stream = _sweep_timers(torch, stream, flush)
-
-    for label, T, H, nh, bh, w32, res in SWEEP:
+    env = _cell_env(torch, N, dev, torch.cuda.current_stream(dev))
+    for cell in SWEEP:
+        label, T, H, nh = cell[:4]
         if args.sweep_filter and args.sweep_filter != f"{label}_{T}_{H}":
             continue
-        c = synth.make_case(0, T, H, nh=nh, buf_heads=bh, w_fp32=w32, residual=res, dh=res)
-        R = c.R
-        wbytes = 4 if w32 else 2
-        wd = 1 if w32 else 0
-        base = {"x": dbf(c.x), "dy": dbf(c.dy)}
-        if res:
-            base["rr"], base["dh"] = dbf(c.residual), dbf(c.dh)
-        w = torch.from_numpy(c.w).to(dev) if w32 else dbf(c.w)
-        set_bytes = sum(t.numel() * t.element_size() for t in base.values()) + 3 * R * H * 2
-        nsets = 1 if args.sweep_once else max(2, -(-2 * l2_bytes // set_bytes) + 1)
-        sets = []
-        for i in range(nsets):
-            st = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
-            st["y"] = torch.empty(R * H, dtype=torch.bfloat16, device=dev)
-            st["h"] = torch.empty_like(st["y"]) if res else None
-            st["dx"] = torch.empty_like(st["y"])
-            st["rstd"] = torch.empty(R, dtype=torch.float32, device=dev)
-            st["dw"] = torch.empty(H, dtype=torch.float32, device=dev)
-            sets.append(st)
-
-        def fwd(i):
-            q = sets[i]
-            st = lib.rmsnorm_train_fwd(q["x"].data_ptr(), q["rr"].data_ptr() if res else None,
-                                       w.data_ptr(), wd, q["y"].data_ptr(),
-                                       q["h"].data_ptr() if res else None,
-                                       q["rstd"].data_ptr(), T, nh, H, c.s_tok, c.s_head,
-                                       1e-6, sh)
-            assert st == 0, st
-
-        for i in range(1 if args.sweep_once else nsets):
-            fwd(i)
-        s_tok, s_head = (nh * H, H) if res else (c.s_tok, c.s_head)
-        rows = [("fwd", fwd, (8 if res else 4) * R * H + 4 * R + wbytes * H)]
-        for det in (1, 0):
-            for use_dh in ((False, True) if res else (False,)):
-                nws = N.rmsnorm_train_bwd_workspace_bytes(T, nh, H, det)
-                ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
-
-                def bwd(i, det=det, use_dh=use_dh, ws=ws, nws=nws):
-                    q = sets[i]
-                    xs = q["h"] if res else q["x"]
-                    st = lib.rmsnorm_train_bwd(xs.data_ptr(), q["dy"].data_ptr(),
-                                               q["dh"].data_ptr() if use_dh else None,
-                                               q["rstd"].data_ptr(), w.data_ptr(), wd,
-                                               q["dx"].data_ptr(), q["dw"].data_ptr(),
-                                               ws.data_ptr(), nws, T, nh, H, s_tok, s_head,
-                                               det, sh)
-                    assert st == 0, st
-
-                name = ("bwd_det" if det else "bwd_nondet") + ("+dh" if use_dh else "")
-                bwd_bytes_ = (8 if use_dh else 6) * R * H + 4 * R + wbytes * H + 4 * H
-                rows.append((name, bwd, bwd_bytes_))
-                if det and not use_dh:
-                    # the checkpointed step: forward, forward recompute, backward
-                    def ckpt(i, bwd=bwd):
-                        fwd(i)
-                        fwd(i)
-                        bwd(i)
-
-                    rows.append(("2xfwd+bwd_det", ckpt, 2 * rows[0][2] + bwd_bytes_))
-        if args.sweep_once:
-            torch.cuda.synchronize()
-            for name, fn, nbytes in rows:
-                if name.startswith("2x") or "nondet" in name or name == "fwd":
-                    continue   # the forward already ran once, for the backward's rstd
-                fn(0)
-                torch.cuda.synchronize()
-                print(json.dumps({"sweep": label, "op": name, "T": T, "H": H, "nh": nh,
-                                  "ran_once": True}), flush=True)
-            del sets, base, w
-            torch.cuda.empty_cache()
-            continue
-        for name, fn, nbytes in rows:
-            us = timed(fn, args.sweep_reps)
-            us_s = timed_stream(fn, nsets, args.sweep_reps)
-            gbs = nbytes / (us * 1e-6) / 1e9
-            gbs_s = nbytes / (us_s * 1e-6) / 1e9
-            print(json.dumps({"sweep": label, "op": name, "T": T, "H": H, "nh": nh,
-                              "w": "fp32" if w32 else "bf16", "us": round(us, 2),
-                              "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
-                              "stream_us": round(us_s, 2), "stream_GBps": round(gbs_s, 1),
-                              "stream_frac": round(gbs_s / peak, 4), "input_sets": nsets,
-                              "peak": peak, "peak_kind": peak_kind,
-                              "bytes": nbytes}), flush=True)
-        del sets, base, w
-        torch.cuda.empty_cache()
+        for rec in time_cell(env, cell, args.sweep_reps, ckpt=True, once=args.sweep_once):
+            rec.update({"sweep": label, "T": T, "H": H, "nh": nh,
+                        "w": "fp32" if cell[5] else "bf16", "peak": env[6],
+                        "peak_kind": env[7]})
+            print(json.dumps(rec), flush=True)
     return 0
 
 
@@ -714,8 +843,8 @@ def run_ln_sweep(args):
     lib = N.lib()
     flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peak()
-    l2_bytes = 129 << 20
-    timed, timed_stream = _sweep_timers(torch, stream, flush)
+    l2_bytes = L2_BYTES
+    timed, timed_stream = _cell_timers(torch, stream, flush)
 
     def dbf(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -828,6 +957,11 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-dw-check", action="store_true")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="leave out the per-configuration table")
+    ap.add_argument("--config-reps", type=int, default=20)
+    ap.add_argument("--min-op-seconds", type=float, default=1.0,
+                    help="least duration of the per-op timing loop (clock samples)")
     ap.add_argument("--sweep", action="store_true",
                     help="time each op on every workload family (one line each) instead")
     ap.add_argument("--sweep-reps", type=int, default=30)

@@ -25,7 +25,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-EPS = 1e-6
+EPS = float(np.float32(1e-6))  # the FP32 eps the kernels receive, widened exactly
 
 
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -159,7 +159,7 @@ def heads_contig(T: int, seed: int = 0) -> Case:
 # (the usual LayerNorm default) and the draws follow the RMSNorm recipe above, plus a bias
 # 0.1 * N(0, 1) and, optionally, a per-row offset so that some rows have |mean| >> std.
 
-LN_EPS = 1e-5
+LN_EPS = float(np.float32(1e-5))  # FP32, as the kernels receive it
 LN_M = (1024, 2048, 4096, 8192)
 LN_H = (3584, 4096, 8192, 16384)
 

@@ -13,6 +13,11 @@ Gates (the op's stated accuracy, flashinfer PR #8827 description and Measurement
   rstd    |rstd - rstd64| <= 1e-6 * rstd64
   h       bit-exact (one rounding of an exact sum)
   dw      |dw - dw64| <= 1e-4 + 1e-4 * |dw64| for every element
+Every gate is applied element by element on every row of every case, at full size; the
+oracle runs in row chunks on the host's cores.  The elements that need dx's cancellation
+clause are counted and held under a ceiling (a fraction of all elements): the clause
+covers the rare elements whose value is far below the terms that form it, not a broad
+loss of accuracy.
 The backward is fed rstd = FP32(rstd64), the oracle's own correctly rounded forward rstd,
 so no oracle input ever comes from the CUDA path; the oracle's dx and dw use that same
 FP32 value widened to FP64 (the gate).  dw against the oracle at rstd64 itself, the other
@@ -22,6 +27,7 @@ from __future__ import annotations
 
 import json
 import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -33,6 +39,12 @@ DEV = "cuda"
 DW_ATOL = 1e-4
 DW_RTOL = 1e-4
 RSTD_RTOL = 1e-6
+# Rows per oracle chunk: about 4 Mi elements (32 MiB of FP64 per array).
+CHUNK_ELEMS = 1 << 22
+# Ceiling on the elements of dx that may use the cancellation allowance instead of the
+# 1-ulp gate (a fraction of all elements, plus a few for the smallest cases).
+DX_CANCEL_MAX_FRAC = 1e-6
+DX_CANCEL_SLACK = 4
 
 
 def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -58,14 +70,6 @@ def ordinal(bits: np.ndarray) -> np.ndarray:
     b = bits.astype(np.int64)
     mag = b & 0x7FFF
     return np.where(b & 0x8000, -mag, mag)
-
-
-def sample_rows(R: int, n: int = 48, seed: int = 99) -> np.ndarray:
-    if R <= 2 * n:
-        return np.arange(R, dtype=np.int64)
-    rng = np.random.default_rng(seed)
-    mid = rng.choice(np.arange(8, R - 8), size=n - 16, replace=False)
-    return np.unique(np.concatenate([np.arange(8), np.arange(R - 8, R), mid])).astype(np.int64)
 
 
 class DeviceCase:
@@ -110,36 +114,38 @@ def check_rstd(rstd_gpu: np.ndarray, rstd64: np.ndarray):
     return worst
 
 
-def check_bf16_1ulp(gpu_bits: np.ndarray, ref64: np.ndarray, what: str, extra_ok=None):
-    """Ordinal distance <= 1 from BF16_RNE(ref64); elements beyond it pass only if
-    |gpu - ref64| <= extra_ok + half a BF16 ulp of the GPU value.  Returns the largest
-    ordinal distance, the count that needed the second clause, and their worst ratio of
-    error to allowance."""
-    ref_bits = oracle.round_bf16(ref64)
-    d = np.abs(ordinal(gpu_bits.reshape(-1)) - ordinal(ref_bits.reshape(-1)))
-    bad = d > 1
-    n_extra = 0
-    worst = 0.0
-    if extra_ok is not None and bad.any():
-        gv = oracle.bf16_to_f64(gpu_bits.reshape(-1))
-        err = np.abs(gv - ref64.reshape(-1))
-        allow = extra_ok.reshape(-1) + np.abs(gv) * 2.0**-8
-        ok2 = err <= allow
-        n_extra = int((bad & ok2).sum())
-        worst = float((err[bad] / allow[bad]).max())
-        bad = bad & ~ok2
-    assert not bad.any(), (
-        f"{what}: {int(bad.sum())} elements beyond 1 BF16 ulp and the FP32 cancellation "
-        f"allowance (max ordinal distance {int(d.max())}, worst err/allowance {worst:.3f})")
-    return int(d.max()) if d.size else 0, n_extra, worst
+def _pool() -> ThreadPoolExecutor:
+    """Worker threads for the oracle and the comparisons: the oracle's C functions (called
+    through ctypes) and numpy's array loops run without the GIL, so row chunks proceed in
+    parallel on the host's cores."""
+    global _POOL
+    if _POOL is None:
+        _POOL = ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+_POOL = None
+
+
+def row_chunks(R: int, H: int):
+    step = max(1, CHUNK_ELEMS // max(H, 1))
+    return [(a, min(a + step, R)) for a in range(0, R, step)]
+
+
+def gather_rows(flat: np.ndarray, nh: int, H: int, s_tok: int, s_head: int,
+                rows: np.ndarray) -> np.ndarray:
+    """Rows of a strided activation buffer as a contiguous [len(rows), H] array."""
+    rows = np.asarray(rows, dtype=np.int64)
+    base = (rows // nh) * s_tok + (rows % nh) * s_head
+    return flat[base[:, None] + np.arange(H)[None, :]]
 
 
 def dx_cancel_tol(x_bits, dy_bits, w, r, H, dh_bits=None):
-    """E_j of the module docstring: the FP32 error of evaluating dx_j, per element."""
+    """E_j of the module docstring, per element of the given rows."""
     xv = oracle.bf16_to_f64(x_bits).reshape(-1, H)
     dyv = oracle.bf16_to_f64(dy_bits).reshape(-1, H)
     wv = oracle.bf16_to_f64(w) if w.dtype == np.uint16 else w.astype(np.float64)
-    rr = r.reshape(-1, 1)
+    rr = np.asarray(r, dtype=np.float64).reshape(-1, 1)
     xh = xv * rr
     g = dyv * wv
     c = (g * xh).mean(axis=1, keepdims=True)
@@ -153,18 +159,9 @@ def dx_cancel_tol(x_bits, dy_bits, w, r, H, dh_bits=None):
 def check_dw(dw_gpu: np.ndarray, dw64: np.ndarray):
     err = np.abs(dw_gpu.astype(np.float64) - dw64)
     budget = DW_ATOL + DW_RTOL * np.abs(dw64)
-    ratio = float((err / budget).max())
+    ratio = float((err / budget).max()) if err.size else 0.0
     assert ratio <= 1.0, f"dw worst err/budget {ratio:.4f} > 1"
     return ratio
-
-
-def gather_rows(flat: np.ndarray, case, rows: np.ndarray) -> np.ndarray:
-    """Rows of a strided activation buffer as a contiguous [len(rows), H] array."""
-    t = rows // case.nh
-    h = rows % case.nh
-    base = t * case.s_tok + h * case.s_head
-    idx = base[:, None] + np.arange(case.H)[None, :]
-    return flat[idx]
 
 
 def report(rec: dict):
@@ -184,39 +181,82 @@ def eager_fp32_dw(xs_dev, dy_dev, r_dev, c, s_tok, s_head):
     return (dy_dev.view(R, H).float() * xhat).sum(dim=0)
 
 
-def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=False,
-             check_eager=False):
-    """Forward + backward of `case` on the GPU against the oracle.  Rows beyond
-    `full_rows_limit` elements are sampled for y / h / dx; rstd and dw are checked in
-    full.  With check_eager, each mode's worst dw error must also be at most the FP32
-    eager reference's.  Returns a dict of the worst figures."""
+def _fwd_chunk(c, a, b, yb, hb):
+    """Oracle forward of rows [a, b); compares y (ordinal distance) and h (bits) with the
+    GPU's.  Returns (rstd64 of the rows, largest y distance, y elements beyond 1 ulp,
+    h elements that differ, the oracle's h bits of the rows or None)."""
+    rows = np.arange(a, b, dtype=np.int64)
+    y64, r64, h64 = oracle.fwd(c.x, c.w, c.eps, c.T, c.nh, c.H, c.s_tok, c.s_head,
+                               residual=c.residual, rows=rows)
+    d = np.abs(ordinal(yb[a:b]) - ordinal(oracle.round_bf16(y64)))
+    h_bad = 0 if hb is None else int(np.count_nonzero(hb[a:b] != h64))
+    return r64, int(d.max()), int(np.count_nonzero(d > 1)), h_bad, h64
+
+
+def _dx_chunk(ctx, a, b, dxb):
+    """Oracle dx of rows [a, b) against the GPU's bits.  Elements farther than one BF16
+    ulp from the rounded FP64 value must sit within the FP32 cancellation allowance E_j
+    (+ half a BF16 ulp of the GPU value); E is computed for the rows that hold such
+    elements only.  Returns (largest ordinal distance, elements that used the allowance,
+    their worst err/allowance, elements beyond both)."""
+    xs, nh, H, s_tok, s_head, dy, dh, w, r_in, T = ctx
+    rows = np.arange(a, b, dtype=np.int64)
+    dx64 = oracle.bwd_dx(xs, dy, r_in, w, T, nh, H, s_tok, s_head, dh=dh, rows=rows)
+    gb = dxb[a:b]
+    d = np.abs(ordinal(gb) - ordinal(oracle.round_bf16(dx64)))
+    far = d > 1
+    if not far.any():
+        return int(d.max()), 0, 0.0, 0
+    ri, ji = np.nonzero(far)
+    urows, pos = np.unique(ri, return_inverse=True)
+    grow = a + urows
+    E = dx_cancel_tol(gather_rows(xs, nh, H, s_tok, s_head, grow), dy.reshape(-1, H)[grow],
+                      w, r_in[grow], H,
+                      dh_bits=None if dh is None else dh.reshape(-1, H)[grow])
+    gv = oracle.bf16_to_f64(gb[ri, ji])
+    err = np.abs(gv - dx64[ri, ji])
+    allow = E[pos, ji] + np.abs(gv) * 2.0**-8
+    ok2 = err <= allow
+    return (int(d.max()), int(np.count_nonzero(ok2)), float((err / allow).max()),
+            int(np.count_nonzero(~ok2)))
+
+
+def run_case(case, modes=(True, False), with_dh=False, check_eager=False):
+    """Forward + backward of `case` on the GPU against the oracle, element by element on
+    every row: y, h and dx of every element, rstd of every row, dw of every column.  The
+    oracle runs in row chunks on the host's cores.  With check_eager, each mode's worst dw
+    error must also be at most the FP32 eager reference's.  Returns a dict of the worst
+    figures."""
     c = case
     R, H = c.R, c.H
     residual = c.residual is not None
     dc = DeviceCase(c)
-    full = R * H <= full_rows_limit
-    rows = None if full else sample_rows(R)
     out = {"case": c.label, "T": c.T, "nh": c.nh, "H": H, "R": R}
+    pool = _pool()
+    chunks = row_chunks(R, H)
 
     # ---- forward ----
     y, rstd, h = gpu_fwd(dc, residual)
     torch.cuda.synchronize()
-    _, rstd64, h_all = oracle.fwd(c.x, c.w, c.eps, c.T, c.nh, H, c.s_tok, c.s_head,
-                                  residual=c.residual, want_y=False)
-    rstd_g = rstd.cpu().numpy()
-    out["rstd_rel"] = check_rstd(rstd_g, rstd64)
-    y64, _, h_bits = oracle.fwd(c.x, c.w, c.eps, c.T, c.nh, H, c.s_tok, c.s_head,
-                                residual=c.residual, rows=rows)
     yb = bits_of(y).reshape(R, H)
-    out["y_ulp"], _, _ = check_bf16_1ulp(yb if rows is None else yb[rows], y64, "y")
+    hb = bits_of(h).reshape(R, H) if residual else None
+    res = list(pool.map(lambda ab: _fwd_chunk(c, ab[0], ab[1], yb, hb), chunks))
+    rstd64 = np.concatenate([q[0] for q in res]) if res else np.zeros(0)
+    out["rstd_rel"] = check_rstd(rstd.cpu().numpy(), rstd64)
+    y_far = sum(q[2] for q in res)
+    out["y_ulp"] = max((q[1] for q in res), default=0)
+    assert y_far == 0, f"y: {y_far} elements beyond 1 BF16 ulp (max distance {out['y_ulp']})"
+    h_all = None
     if residual:
-        hb = bits_of(h).reshape(R, H)
-        assert np.array_equal(hb, h_all.reshape(R, H)), "h not bit-exact"
+        h_bad = sum(q[3] for q in res)
+        assert h_bad == 0, f"h not bit-exact in {h_bad} elements"
+        h_all = np.concatenate([q[4] for q in res]).reshape(-1)
+    del yb, hb, res
 
     # ---- backward: saved input is x (plain) or the oracle's h (residual) ----
     if residual:
-        xs_bits = h_all.reshape(-1)
-        xs_dev = to_dev(xs_bits)
+        xs_bits = h_all
+        xs_dev = to_dev(h_all)
         s_tok, s_head = c.nh * H, H
     else:
         xs_bits = c.x
@@ -225,46 +265,58 @@ def run_case(case, modes=(True, False), full_rows_limit=4096 * 4096, with_dh=Fal
     r32 = rstd64.astype(np.float32)
     r_in = r32.astype(np.float64)
     r_dev = to_dev(r32)
-    dw64 = oracle.bwd_dw(xs_bits, c.dy, r_in, c.T, c.nh, H, s_tok, s_head)
+    dw_f = pool.submit(oracle.bwd_dw, xs_bits, c.dy, r_in, c.T, c.nh, H, s_tok, s_head)
     # the second rstd form: the FP64 rstd itself (reported, not gated -- the kernels are
     # handed the FP32 rstd a forward returns)
-    dw64_exact = oracle.bwd_dw(xs_bits, c.dy, rstd64, c.T, c.nh, H, s_tok, s_head)
-    dx64 = oracle.bwd_dx(xs_bits, c.dy, r_in, c.w, c.T, c.nh, H, s_tok, s_head,
-                         dh=c.dh if with_dh else None, rows=rows)
-    sel = np.arange(R) if rows is None else rows
-    xrows = gather_rows(xs_bits, c, sel) if not residual else xs_bits.reshape(R, H)[sel]
-    tol = dx_cancel_tol(xrows, c.dy.reshape(R, H)[sel], c.w, r_in[sel], H,
-                        dh_bits=c.dh.reshape(R, H)[sel] if with_dh else None)
+    dw_fx = pool.submit(oracle.bwd_dw, xs_bits, c.dy, rstd64, c.T, c.nh, H, s_tok, s_head)
+    ctx = (xs_bits, c.nh, H, s_tok, s_head, c.dy, c.dh if with_dh else None, c.w, r_in, c.T)
     eager_err = None
+    dws = {}
+    dx_first = None
+    n_elem = max(R * H, 1)
+    for det in modes:
+        dx, dw = gpu_bwd(dc, xs_dev, s_tok, s_head, r_dev, det, with_dh=with_dh)
+        torch.cuda.synchronize()
+        key = "det" if det else "nondet"
+        if dx_first is None:
+            dx_first = dx
+        else:
+            # the two modes share the row pass: dx is bit-identical
+            assert torch.equal(dx_first.view(torch.int16), dx.view(torch.int16)), \
+                "dx differs between modes"
+        dxb = bits_of(dx).reshape(R, H)
+        res = list(pool.map(lambda ab: _dx_chunk(ctx, ab[0], ab[1], dxb), chunks))
+        n_bad = sum(q[3] for q in res)
+        n_extra = sum(q[1] for q in res)
+        worst = max((q[2] for q in res), default=0.0)
+        out[f"dx_ulp_{key}"] = max((q[0] for q in res), default=0)
+        out[f"dx_cancel_{key}"] = n_extra
+        out[f"dx_cancel_frac_{key}"] = n_extra / n_elem
+        out[f"dx_cancel_worst_{key}"] = worst
+        assert n_bad == 0, (
+            f"dx (det={det}): {n_bad} elements beyond 1 BF16 ulp and the FP32 cancellation "
+            f"allowance (worst err/allowance {worst:.3f})")
+        assert n_extra <= DX_CANCEL_MAX_FRAC * n_elem + DX_CANCEL_SLACK, (
+            f"dx (det={det}): {n_extra} of {n_elem} elements needed the cancellation "
+            f"allowance, above the ceiling {DX_CANCEL_MAX_FRAC:g} of the elements")
+        dws[key] = dw.cpu().numpy()
+        del dxb
+    dw64 = dw_f.result()
+    dw64_exact = dw_fx.result()
     if check_eager:
         dw_e = eager_fp32_dw(xs_dev, dc.dy, r_dev, c, s_tok, s_head).cpu().numpy()
         eager_err = float(np.abs(dw_e.astype(np.float64) - dw64).max())
         out["dw_eager_fp32_max_err"] = eager_err
-    dws = {}
-    for det in modes:
-        dx, dw = gpu_bwd(dc, xs_dev, s_tok, s_head, r_dev, det, with_dh=with_dh)
-        torch.cuda.synchronize()
-        dxb = bits_of(dx).reshape(R, H)
-        ulp, n_extra, worst = check_bf16_1ulp(dxb[sel], dx64, f"dx (det={det})",
-                                              extra_ok=tol)
-        ratio = check_dw(dw.cpu().numpy(), dw64)
-        dws[det] = (dxb, dw.cpu().numpy())
-        key = "det" if det else "nondet"
+    for key, dwg in dws.items():
+        out[f"dw_ratio_{key}"] = check_dw(dwg, dw64)
         budget = DW_ATOL + DW_RTOL * np.abs(dw64_exact)
         out[f"dw_ratio_rstd64_{key}"] = float(
-            (np.abs(dw.cpu().numpy().astype(np.float64) - dw64_exact) / budget).max())
+            (np.abs(dwg.astype(np.float64) - dw64_exact) / budget).max()) if H else 0.0
         if eager_err is not None:
-            err = float(np.abs(dw.cpu().numpy().astype(np.float64) - dw64).max())
+            err = float(np.abs(dwg.astype(np.float64) - dw64).max())
             out[f"dw_max_err_{key}"] = err
             assert err <= eager_err, (
                 f"dw worst error {err:.3e} above the FP32 eager reference's {eager_err:.3e}")
-        out[f"dx_ulp_{key}"] = ulp
-        out[f"dx_cancel_{key}"] = n_extra
-        out[f"dx_cancel_worst_{key}"] = worst
-        out[f"dw_ratio_{key}"] = ratio
-    if len(dws) == 2:
-        # the two modes share the row pass: dx is bit-identical
-        assert np.array_equal(dws[True][0], dws[False][0]), "dx differs between modes"
     assert N.rmsnorm_train_device_error(reset=True) == 0
     report(out)
     return out

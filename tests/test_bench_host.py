@@ -65,7 +65,8 @@ def test_reference_arm_line(capsys):
                 "--warmup", "3"])
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == (os.cpu_count() or 1)
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["higher_is_better"] is True
 
@@ -111,3 +112,56 @@ def test_max_over_two_gloo_ranks(tmp_path):
     vals = sorted(float(l.split()[2]) for o in outs for l in o.splitlines()
                   if l.startswith("RESULT"))
     assert vals == [11.0, 11.0]
+
+
+def test_target_summary_lists_cells_below_target():
+    cfg = {
+        "tiny_T64_H256": {"fwd": {"frac": 0.01, "stream_frac": 0.02}},
+        "plain_T16384_H4096": {"fwd": {"frac": 0.80, "stream_frac": 0.85},
+                               "bwd_det": {"frac": 0.74, "stream_frac": 0.80}},
+        "residual_T65536_H6144": {"bwd_det+dh": {"frac": 0.9, "stream_frac": 0.7}},
+    }
+    out = bench.target_summary(cfg)
+    assert out["ops_checked"] == 3          # the T=64 cell is outside the target's range
+    assert [(b["cell"], b["op"]) for b in out["below"]] == [
+        ("plain_T16384_H4096", "bwd_det"), ("residual_T65536_H6144", "bwd_det+dh")]
+    assert bench.target_summary(None) is None
+
+
+def test_config_cells_cover_every_configuration_at_t_8192_and_above():
+    names = {bench.cell_name(c) for c in bench.CONFIG_CELLS}
+    for T in (16384, 65536):
+        assert f"plain_T{T}_H4096" in names
+    for H in (1536, 2048, 5120):
+        for T in (32768, 65536, 98304, 131072):
+            assert f"stress_T{T}_H{H}" in names
+    for T in (30720, 65536):
+        assert f"residual_T{T}_H6144" in names
+    assert {"heads24of32_T65536_H256", "heads4_T65536_H256", "tiny_T64_H256"} <= names
+
+
+def test_cpu_baseline_reports_single_and_all_cores():
+    from rmsnorm_fwd_02_gb300 import synth
+    c = synth.make_case(0, 40, 64)
+    out = bench.cpu_baseline(c, 2, budget_s=0.2, rows_per_thread=4)
+    assert out["kind"] == "oracle" and out["cores"] == (os.cpu_count() or 1)
+    assert out["value"] > 0 and out["single_thread_value"] > 0
+    assert out["host_cpu_count"] == os.cpu_count()
+
+
+def test_oracle_runner_blocks_sum_to_whole_sample_dw():
+    # the threaded harness only splits rows: its dw equals the oracle's over the same rows
+    import numpy as np
+    import oracle
+    from rmsnorm_fwd_02_gb300 import synth
+    c = synth.make_case(3, 50, 32)
+    r = bench.OracleRunner(c, rows_per_thread=5, threads=4)
+    dw = r.step()
+    r.close()
+    rows = np.concatenate(r.blocks)
+    sub_x = c.x.reshape(-1, 32)[rows].reshape(-1)
+    sub_dy = c.dy.reshape(-1, 32)[rows].reshape(-1)
+    _, r64, _ = oracle.fwd(sub_x, c.w, c.eps, rows.size, 1, 32, 32, 32)
+    want = oracle.bwd_dw(sub_x, sub_dy, r64.astype(np.float32).astype(np.float64),
+                         rows.size, 1, 32, 32, 32)
+    np.testing.assert_allclose(dw, want, rtol=1e-12, atol=1e-12)

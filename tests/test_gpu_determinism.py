@@ -24,26 +24,44 @@ def _bits(t):
     return parity.bits_of(t)
 
 
-@pytest.mark.parametrize("mk", [lambda: synth.stress(32768, 5120),
-                                lambda: synth.heads_strided(4096),
-                                lambda: synth.plain(4096)])
-def test_det_bitwise_10_runs(mk):
+DET_CASES = {
+    "tiny_T64_H256": (lambda: synth.tiny(), False),                # one-launch small path
+    "plain_T4096_H4096": (lambda: synth.plain(4096), False),
+    "plain_T65536_H4096": (lambda: synth.plain(65536), False),     # the headline workload
+    "stress_T32768_H5120": (lambda: synth.stress(32768, 5120), False),
+    "residual_T7168_H6144": (lambda: synth.residual(7168, with_dh=True), False),
+    "residual_T7168_H6144_dh": (lambda: synth.residual(7168, with_dh=True), True),
+    "residual_T96_H6144_dh": (lambda: synth.residual(96, with_dh=True), True),
+    "heads24of32_T4096": (lambda: synth.heads_strided(4096), False),
+    "heads4_T4096": (lambda: synth.heads_contig(4096), False),
+    "heads4_T65536": (lambda: synth.heads_contig(65536), False),
+}
+
+
+@pytest.mark.parametrize("name", list(DET_CASES))
+def test_det_bitwise_10_runs(name):
+    mk, with_dh = DET_CASES[name]
     c = mk()
+    residual = c.residual is not None
     dc = parity.DeviceCase(c)
-    y, rstd, _ = parity.gpu_fwd(dc, False)
+    y, rstd, h = parity.gpu_fwd(dc, residual)
+    # the backward's saved input: x itself, or h of the residual form
+    xs, s_tok, s_head = (h, c.nh * c.H, c.H) if residual else (dc.x, c.s_tok, c.s_head)
     ref = None
     for _ in range(10):
-        dx, dw = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, rstd, True)
+        dx, dw = parity.gpu_bwd(dc, xs, s_tok, s_head, rstd, True, with_dh=with_dh)
         cur = (_bits(dx), dw.cpu().numpy().view(np.uint32))
         if ref is None:
             ref = cur
         else:
             assert np.array_equal(ref[0], cur[0]) and np.array_equal(ref[1], cur[1])
-    y2, rstd2, _ = parity.gpu_fwd(dc, False)
+    y2, rstd2, h2 = parity.gpu_fwd(dc, residual)
     assert np.array_equal(_bits(y), _bits(y2))
     assert torch.equal(rstd, rstd2)
+    if residual:
+        assert np.array_equal(_bits(h), _bits(h2))
     # non-deterministic mode: same dx bits
-    dxn, _ = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, rstd, False)
+    dxn, _ = parity.gpu_bwd(dc, xs, s_tok, s_head, rstd, False, with_dh=with_dh)
     assert np.array_equal(ref[0], _bits(dxn))
     assert N.rmsnorm_train_device_error(reset=True) == 0
 
@@ -56,7 +74,7 @@ def test_per_head_equals_plain_bitwise(strided):
     dx, dw = parity.gpu_bwd(dc, dc.x, c.s_tok, c.s_head, rstd, True)
     # gathered contiguous copy as plain rows [T*nh, 256]
     rows = np.arange(c.R)
-    flat = parity.gather_rows(c.x, c, rows).reshape(-1)
+    flat = parity.gather_rows(c.x, c.nh, c.H, c.s_tok, c.s_head, rows).reshape(-1)
     p = synth.Case(T=c.R, nh=1, H=c.H, s_tok=c.H, s_head=c.H, x=flat, dy=c.dy, w=c.w)
     dp = parity.DeviceCase(p)
     y2, rstd2, _ = parity.gpu_fwd(dp, False)
