@@ -645,13 +645,15 @@ def device_case(torch, dev, T, H, nh=1, buf_heads=None, w_fp32=False, residual=F
 
 
 def _cell_timers(torch, stream, flush):
-    """Two clocks, CUDA events on the launch stream:
+    """Three clocks, CUDA events on the launch stream:
 
-    isolated  `reps` launches, each after an L2 flush outside the events; trimmed mean.
-              The flush READS a 512 MiB buffer, so L2 is cold but clean (a write-based
-              flush would leave dirty lines whose write-back lands inside the next timed
-              kernel).  Includes the launch's ramp-up and tail and the gap before the first
-              CTA starts.
+    graph     (the "frac" of a cell) the pages' method: the op captured once into a CUDA
+              graph, `reps` replays, each after an L2 flush outside the events; trimmed
+              mean.  The flush READS a 512 MiB buffer, so L2 is cold but clean (a
+              write-based flush would leave dirty lines whose write-back lands inside the
+              next timed kernel).  Includes the op's ramp-up and tail and the gap before
+              its first CTA starts.
+    eager     the same, launching the op directly instead of replaying a graph.
     stream    `reps` launches back to back inside one event pair, rotating over copies of
               the inputs and outputs so that every launch finds its inputs out of L2 (the
               sets in between exceed twice the L2); time / launches.  This is the op as a
@@ -676,6 +678,40 @@ def _cell_timers(torch, stream, flush):
         cut = len(out) // 10
         return statistics.fmean(out[cut:len(out) - cut])
 
+    def timed_graph(fn, reps, cur):
+        """isolated, the pages' way: the op captured once into a CUDA graph (fn launches on
+        the stream handle cur["sh"]), each replay after the same L2 flush"""
+        cs = torch.cuda.Stream()
+        cs.wait_stream(stream)
+        old = cur["sh"]
+        cur["sh"] = cs.cuda_stream
+        try:
+            with torch.cuda.stream(cs):
+                fn(0)   # warm-up on the capture stream
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                fn(0)
+        finally:
+            cur["sh"] = old
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        out = []
+        for _ in range(reps):
+            flush.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out.append(a.elapsed_time(b) * 1e3)
+        del g
+        out.sort()
+        cut = len(out) // 10
+        return statistics.fmean(out[cut:len(out) - cut])
+
     def timed_stream(fn, nsets, reps):
         n = max(reps, 2 * nsets)
         for i in range(nsets):
@@ -690,17 +726,17 @@ def _cell_timers(torch, stream, flush):
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / n
 
-    return timed, timed_stream
+    return timed, timed_stream, timed_graph
 
 
-def time_cell(env, cell, reps, ckpt=False, once=False):
+def time_cell(env, cell, reps, ckpt=False, once=False, only=None):
     """Times every op of one cell (forward; backward in both modes, with and without dh in
     the residual form; with ckpt the checkpointed step 2xfwd+bwd = forward, forward
     recompute, deterministic backward) with both clocks of _cell_timers.  Returns one
     record per op.  With once, runs each op once, untimed (for a profiler)."""
     torch, N, lib, dev, stream, flush, peak, peak_kind = env
     _, T, H, nh, bh, w32, res, outl = cell
-    sh = stream.cuda_stream
+    cur = {"sh": stream.cuda_stream}   # the stream the ops launch on (graph capture swaps it)
     R = T * nh
     wbytes = 4 if w32 else 2
     wd = N.RMSN_W_FP32 if w32 else N.RMSN_W_BF16
@@ -724,7 +760,7 @@ def time_cell(env, cell, reps, ckpt=False, once=False):
         st = lib.rmsnorm_train_fwd(q["x"].data_ptr(), q["res"].data_ptr() if res else None,
                                    w.data_ptr(), wd, q["y"].data_ptr(),
                                    q["h"].data_ptr() if res else None, q["rstd"].data_ptr(),
-                                   T, nh, H, s_tok_in, s_head_in, 1e-6, sh)
+                                   T, nh, H, s_tok_in, s_head_in, 1e-6, cur["sh"])
         assert st == 0, st
 
     for i in range(nsets):
@@ -744,7 +780,7 @@ def time_cell(env, cell, reps, ckpt=False, once=False):
                                            q["rstd"].data_ptr(), w.data_ptr(), wd,
                                            q["dx"].data_ptr(), q["dw"].data_ptr(),
                                            ws.data_ptr(), nws, T, nh, H, s_tok, s_head,
-                                           det, sh)
+                                           det, cur["sh"])
                 assert st == 0, st
 
             name = ("bwd_det" if det else "bwd_nondet") + ("+dh" if use_dh else "")
@@ -757,21 +793,26 @@ def time_cell(env, cell, reps, ckpt=False, once=False):
                     bwd(i)
 
                 ops.append(("2xfwd+bwd_det", step, 2 * fwd_b + bwd_b))
-    timed, timed_stream = _cell_timers(torch, stream, flush)
+    timed, timed_stream, timed_graph = _cell_timers(torch, stream, flush)
     out = []
+    if only:
+        ops = [o for o in ops if o[0] in only]
     for name, fn, nbytes in ops:
         if once:
             fn(0)
             torch.cuda.synchronize()
             out.append({"op": name, "ran_once": True})
             continue
-        us = timed(fn, reps)
+        us = timed_graph(fn, reps, cur)
+        us_e = timed(fn, reps)
         us_s = timed_stream(fn, nsets, reps)
         gbs = nbytes / (us * 1e-6) / 1e9
         gbs_s = nbytes / (us_s * 1e-6) / 1e9
         out.append({"op": name, "us": round(us, 2), "GBps": round(gbs, 1),
                     "frac": round(gbs / peak, 4), "stream_us": round(us_s, 2),
                     "stream_GBps": round(gbs_s, 1), "stream_frac": round(gbs_s / peak, 4),
+                    "eager_us": round(us_e, 2),
+                    "eager_frac": round(nbytes / (us_e * 1e-6) / 1e9 / peak, 4),
                     "input_sets": nsets, "bytes": nbytes})
     del sets, base, w
     torch.cuda.empty_cache()
@@ -802,7 +843,9 @@ def run_sweep(args):
         label, T, H, nh = cell[:4]
         if args.sweep_filter and args.sweep_filter != f"{label}_{T}_{H}":
             continue
-        for rec in time_cell(env, cell, args.sweep_reps, ckpt=True, once=args.sweep_once):
+        only = set(args.sweep_ops.split(",")) if args.sweep_ops else None
+        for rec in time_cell(env, cell, args.sweep_reps, ckpt=True, once=args.sweep_once,
+                             only=only):
             rec.update({"sweep": label, "T": T, "H": H, "nh": nh,
                         "w": "fp32" if cell[5] else "bf16", "peak": env[6],
                         "peak_kind": env[7]})
@@ -844,7 +887,7 @@ def run_ln_sweep(args):
     flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
     peak, peak_kind = measured_peak()
     l2_bytes = L2_BYTES
-    timed, timed_stream = _cell_timers(torch, stream, flush)
+    timed, timed_stream, _ = _cell_timers(torch, stream, flush)
 
     def dbf(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -970,6 +1013,9 @@ def main(argv=None):
     ap.add_argument("--sweep-layernorm", action="store_true",
                     help="with --sweep: the LayerNorm ops on the normalization tables' shapes "
                          "(filter entries as layernorm_M_H)")
+    ap.add_argument("--sweep-ops", default="",
+                    help="with --sweep: only these ops (comma-separated: fwd, bwd_det, "
+                         "bwd_nondet, bwd_det+dh, bwd_nondet+dh, 2xfwd+bwd_det, ...)")
     ap.add_argument("--sweep-once", action="store_true",
                     help="with --sweep: run each op of each selected workload once, untimed "
                          "(one launch of each kernel, for a profiler)")

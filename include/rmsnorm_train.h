@@ -13,8 +13,11 @@
  *
  * Two backward modes share one forward: deterministic != 0 gives bit-identical dw run to
  * run and across GPUs of any SM count (the row -> partial mapping depends on T, nh, H and
- * whether dh is given, never on the GPU); deterministic == 0 may size its partition to
- * the current GPU.  dx is the same in both modes, bit for bit.
+ * whether dh is given, never on the GPU; a second kernel adds the partials in a fixed
+ * order); deterministic == 0 runs as one row-pass kernel whose CTAs take rows as they
+ * go and add their dw partials into FP64 sums that the last CTA to finish rounds to dw,
+ * so its dw may differ between runs in the last bits (both modes keep dw within the same
+ * budget).  dx is the same in both modes, bit for bit.
  *
  * Rows and views (same PR, description: per-head views [T,24,256] strided and [T,4,256]
  * contiguous with a shared w[256]).  A normalized row is a pair (token t, head h),
@@ -32,7 +35,7 @@
  *  - Alignment: every tensor pointer 16-byte aligned, except rstd (4-byte aligned; the
  *    backward reads it fastest when it is 16-byte aligned); H a multiple of 8; s_tok and
  *    s_head multiples of 8 elements (each row is a 16-byte-aligned run).
- *  - Limits: 8 <= H <= 8192, T >= 0, nh >= 1, T*nh < 2^31.
+ *  - Limits: 8 <= H <= 8192, T >= 0, nh >= 1, T*nh <= 2^31 - 2^16.
  *  - Outputs must not overlap inputs.
  *  - Errors: argument checks happen before anything is enqueued and return a nonzero
  *    status without touching memory; RMSN_ERR_CUDA reports a failed launch (the CUDA
@@ -80,10 +83,11 @@ int rmsnorm_train_fwd(const void* x, const void* residual, const void* w, int w_
 
 /*
  * Bytes of device workspace rmsnorm_train_bwd needs for this shape and mode: 0 for
- * T*nh <= 256 rows (done in one launch without a workspace) and for T*nh == 0.  For
- * deterministic == 0 the size depends on the current device (its SM count); for
- * deterministic != 0 it depends on (T, nh, H) only.  Returns 0 on invalid sizes.
- * Host-only computation apart from a device-attribute query.
+ * T*nh <= 256 rows (done in one launch without a workspace) and for T*nh == 0.  Above
+ * that, deterministic != 0 needs P partials of 2*H floats (P <= 152 per CTA an SM the
+ * launch shape keeps resident, a function of (T, nh, H) only), and deterministic == 0
+ * needs 16 + 8*H bytes (two counters and H FP64 sums).  Returns 0 on invalid sizes.
+ * Host-only computation: no device access.
  */
 size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int deterministic);
 
@@ -103,8 +107,10 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
  *   dx         BF16 [T, nh, H] out
  *   dw         FP32 [H] out, overwritten (not accumulated); zero-filled when T*nh == 0
  *   workspace  device scratch of >= rmsnorm_train_bwd_workspace_bytes(...) bytes,
- *              16-byte aligned, no initial contents required; clobbered by the call
- *              (may be NULL when that size is 0)
+ *              16-byte aligned, no initial contents required (the non-deterministic
+ *              mode zeroes its counters and sums on the stream first); clobbered by the
+ *              call (may be NULL when that size is 0).  Two calls that may overlap on the
+ *              GPU need separate workspaces.
  *   deterministic  0 or 1 (see the top of this file)
  */
 int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float* rstd,
@@ -112,6 +118,30 @@ int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float
                       void* workspace, size_t workspace_bytes,
                       int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head,
                       int deterministic, void* stream);
+
+/*
+ * Backward that is not handed rstd: it recomputes rstd = 1/sqrt(mean(x^2) + eps) from the
+ * rows it already reads (one more multiply-add an element, no extra pass over x) and
+ * writes it to rstd_out.  For steps that checkpoint the forward's input but not its
+ * statistics: flashinfer PR #8827's Measurement section times the checkpointed step
+ * (forward, forward again, backward) as an op of its own, and this entry point replaces
+ * the second forward when only the backward needs it.
+ *
+ * Arguments as rmsnorm_train_bwd, except:
+ *   rstd_out   FP32 [T, nh] out (required, 4-byte aligned): the recomputed rstd, the
+ *              forward's formula in FP32 (its sum of squares may add in another order, so
+ *              a bit may differ from the forward's; both stay within 1e-6 of the exact
+ *              value)
+ *   eps        as passed to the forward; finite, >= 0
+ * The workspace is rmsnorm_train_bwd_workspace_bytes(T, nh, H, deterministic) bytes.  dx
+ * and dw follow the rules of rmsnorm_train_bwd with the recomputed rstd; the determinism
+ * contract is the same.
+ */
+int rmsnorm_train_bwd_recompute(const void* x, const void* dy, const void* dh, const void* w,
+                                int w_dtype, void* dx, float* dw, float* rstd_out,
+                                void* workspace, size_t workspace_bytes, int64_t T, int32_t nh,
+                                int32_t H, int64_t s_tok, int64_t s_head, float eps,
+                                int deterministic, void* stream);
 
 /*
  * Backward for callers that cannot allocate device memory where they call it -- e.g. a
@@ -128,8 +158,10 @@ int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float
  *    two unordered streams) race on it and must be serialized by the caller.  No initial
  *    contents are needed.
  *  - Returns RMSN_ERR_SCRATCH_LIMIT, with nothing enqueued, when the shape needs more than
- *    16 MiB of partials (rmsnorm_train_bwd_workspace_bytes() > 16 MiB); every shape up to
- *    H = 8192 fits on a 152-SM GB300 in both modes.
+ *    16 MiB (rmsnorm_train_bwd_workspace_bytes() > 16 MiB).  No supported shape does:
+ *    the deterministic mode needs at most 152 x 2 x 8192 x 4 bytes (9.5 MiB) and the
+ *    non-deterministic mode 16 + 8*H bytes, so this status is a guard, not a case a
+ *    caller meets.
  */
 int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, const float* rstd,
                               const void* w, int w_dtype, void* dx, float* dw,

@@ -31,6 +31,8 @@ SIGNATURES = {
                                  _i32, _i32, _i64, _i64, _int, _vp]),
     "rmsnorm_train_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _i64, _i32,
                                          _i32, _i64, _i64, _int, _vp]),
+    "rmsnorm_train_bwd_recompute": (_int, [_vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _size,
+                                           _i64, _i32, _i32, _i64, _i64, _f32, _int, _vp]),
     "rmsnorm_train_status_str": (C.c_char_p, [_int]),
     "rmsnorm_train_device_error": (_int, [C.POINTER(C.c_uint), _int]),
     "rmsnorm_train_launch_plan": (_int, [_i32, _int, C.POINTER(C.c_int64), _int]),
@@ -117,6 +119,17 @@ def rmsnorm_train_bwd(x, dy, dh, rstd, w, w_dtype, dx, dw, workspace, workspace_
                                  H, s_tok, s_head, int(deterministic), _stream(stream))
     if st != RMSN_OK:
         raise RmsnError("rmsnorm_train_bwd", st)
+
+
+def rmsnorm_train_bwd_recompute(x, dy, dh, w, w_dtype, dx, dw, rstd_out, workspace,
+                                workspace_bytes, T, nh, H, s_tok, s_head, eps, deterministic,
+                                stream=None):
+    st = lib().rmsnorm_train_bwd_recompute(_ptr(x), _ptr(dy), _ptr(dh), _ptr(w), w_dtype,
+                                           _ptr(dx), _ptr(dw), _ptr(rstd_out), _ptr(workspace),
+                                           workspace_bytes, T, nh, H, s_tok, s_head, eps,
+                                           int(deterministic), _stream(stream))
+    if st != RMSN_OK:
+        raise RmsnError("rmsnorm_train_bwd_recompute", st)
 
 
 def rmsnorm_train_bwd_noalloc(x, dy, dh, rstd, w, w_dtype, dx, dw, T, nh, H, s_tok, s_head,

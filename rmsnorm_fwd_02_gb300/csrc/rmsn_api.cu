@@ -18,6 +18,7 @@ __device__ unsigned g_err_word = 0u;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxRows = (int64_t{1} << 31) - (int64_t{1} << 16);
 // Shared-memory ring bytes per CTA (target): kernels built for two CTAs an SM take 96 KB
 // each; "wide" kernels, one CTA an SM, take twice that.
 constexpr size_t kRingTarget = 96 * 1024;
@@ -134,7 +135,8 @@ int check_view(int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head, 
   if (w_dtype != RMSN_W_BF16 && w_dtype != RMSN_W_FP32) return RMSN_ERR_INVALID_ARG;
   if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
   if (H > kMaxH) return RMSN_ERR_UNSUPPORTED;
-  if (T > 0 && T * static_cast<int64_t>(nh) > INT32_MAX - 1) return RMSN_ERR_UNSUPPORTED;
+  // row indices, plus a stage's worth of rows past the end, stay inside int32
+  if (T > 0 && T * static_cast<int64_t>(nh) > kMaxRows) return RMSN_ERR_UNSUPPORTED;
   if (s_tok < 0 || (s_tok % 8) != 0) return RMSN_ERR_INVALID_ARG;
   if (nh > 1 && (s_head < 0 || (s_head % 8) != 0)) return RMSN_ERR_INVALID_ARG;
   return RMSN_OK;
@@ -144,17 +146,12 @@ bool is_contig(int32_t nh, int32_t H, int64_t s_tok, int64_t s_head) {
   return s_tok == static_cast<int64_t>(nh) * H && (nh == 1 || s_head == H);
 }
 
-int bwd_partials(int32_t R, const Shape& s, bool det, int dev, bool fp32w) {
+// Deterministic backward: the partial count, a function of (R, the shape) only.
+int det_partials(int32_t R, const Shape& s) {
   const int64_t per = static_cast<int64_t>(s.groups) * kMinStagesPerCta;
   int64_t want = (R + per - 1) / per;
   if (want < 1) want = 1;
-  int64_t cap;
-  if (det) {
-    cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.cls);
-  } else {
-    const int occ = bwd_blocks_per_sm(s, fp32w);
-    cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
-  }
+  const int64_t cap = static_cast<int64_t>(kDetSMs) * bwd_design_blocks_per_sm(s.cls);
   return static_cast<int>(want < cap ? want : cap);
 }
 
@@ -245,6 +242,14 @@ Shape bwd_shape(int H, bool with_dh) {
   return make_shape(H, tensors, nv <= 768 ? 2 : 4, true, /*allow_multi=*/false);
 }
 
+Shape nd_shape(const Shape& s, int H) {
+  Shape n = s;
+  n.smem = smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0, s.groups,
+                       bwd_w_in_smem(s.cls, s.vpt) ? H : 0, s.stages)
+               .total;
+  return n;
+}
+
 cudaError_t prepare_kernel(const void* fn, size_t smem) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -294,6 +299,109 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Both backward entry points: rstd given (rstd_out unused), or rstd == nullptr and the
+// row pass recomputes it with eps, writing it to rstd_out (the small path computes it into
+// rstd_out first and reads it back).
+int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd, float eps,
+               float* rstd_out, const void* w, int w_dtype, void* dx, float* dw, void* workspace,
+               size_t workspace_bytes, int64_t T, int32_t nh, int32_t H, int64_t s_tok,
+               int64_t s_head, int deterministic, void* stream) {
+  int st = check_view(T, nh, H, s_tok, s_head, w_dtype);
+  if (st != RMSN_OK) return st;
+  if (!x || !dy || !w || !dx || !dw) return RMSN_ERR_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return RMSN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dh) || !aligned16(w) || !aligned16(dx) ||
+      !aligned16(dw) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(rstd) & 3u))
+    return RMSN_ERR_INVALID_ARG;
+  const int64_t R = T * static_cast<int64_t>(nh);
+
+  int dev = 0;
+  if ((st = current_device(&dev)) != RMSN_OK) return st;
+  if ((st = device_setup(dev)) != RMSN_OK) return st;
+  const cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
+
+  const bool fp32w = (w_dtype == RMSN_W_FP32);
+  if (bwd_is_small(R)) {  // one launch, no workspace
+    BwdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dy = static_cast<const __nv_bfloat16*>(dy);
+    a.dh = static_cast<const __nv_bfloat16*>(dh);
+    a.rstd = rstd;
+    a.eps = eps;
+    a.w = w;
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
+    a.R = static_cast<int32_t>(R);
+    a.err = g_err_ptr[dev];
+    if (rstd == nullptr && R > 0) {  // rstd first, then the one-launch backward reads it
+      if (launch_rstd_rows(a, rstd_out, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
+      a.rstd = rstd_out;
+    }
+    return launch_bwd_small(a, dw, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
+  }
+  const Shape s = bwd_shape(H, dh != nullptr);
+  if (R > 0 && !deterministic) {
+    // one launch: rows handed out as the CTAs go, dw finished by the last CTA
+    if (workspace == nullptr || workspace_bytes < nd_workspace_bytes(H)) return RMSN_ERR_WORKSPACE;
+    const Shape sn = nd_shape(s, H);
+    const int occ = bwd_nd_blocks_per_sm(sn, fp32w, rstd == nullptr);
+    const int64_t per = s.groups;
+    int64_t P = (R + per - 1) / per;
+    const int64_t cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
+    if (P > cap) P = cap;
+    BwdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dy = static_cast<const __nv_bfloat16*>(dy);
+    a.dh = static_cast<const __nv_bfloat16*>(dh);
+    a.rstd = rstd;
+    a.eps = eps;
+    a.rstd_out = rstd_out;
+    a.w = w;
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.ctl = static_cast<unsigned*>(workspace);
+    a.acc = reinterpret_cast<double*>(static_cast<unsigned char*>(workspace) + kNdCtlBytes);
+    a.dw = dw;
+    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
+    a.R = static_cast<int32_t>(R);
+    a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
+    a.groups = s.groups;
+    a.ntg = s.ntg;
+    a.stages = s.stages;
+    a.P = static_cast<int32_t>(P);
+    a.err = g_err_ptr[dev];
+    return launch_bwd_nd(a, sn, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
+  }
+  int P = 0;
+  if (R > 0) {
+    P = det_partials(static_cast<int32_t>(R), s);
+    const size_t need = static_cast<size_t>(P) * 2 * H * sizeof(float);
+    if (workspace == nullptr || workspace_bytes < need) return RMSN_ERR_WORKSPACE;
+
+    BwdArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.dy = static_cast<const __nv_bfloat16*>(dy);
+    a.dh = static_cast<const __nv_bfloat16*>(dh);
+    a.rstd = rstd;
+    a.eps = eps;
+    a.rstd_out = rstd_out;
+    a.w = w;
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.part = static_cast<float*>(workspace);
+    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
+    a.R = static_cast<int32_t>(R);
+    a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
+    a.groups = s.groups;
+    a.ntg = s.ntg;
+    a.stages = s.stages;
+    a.P = P;
+    a.err = g_err_ptr[dev];
+    if (launch_bwd_rows(a, s, fp32w, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
+  }
+  if (launch_dw_finish(static_cast<const float*>(workspace), dw, P, H, stream_) != cudaSuccess)
+    return RMSN_ERR_CUDA;
+  return RMSN_OK;
 }
 
 }  // namespace rmsn
@@ -368,28 +476,13 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
     return 0;
   const int64_t R = T * static_cast<int64_t>(nh);
   if (R == 0 || bwd_is_small(R)) return 0;  // small inputs take the one-launch path
-  // the launch shape (so the partial count) may differ with and without dh: one size
-  // serves both
-  const Shape s = bwd_shape(H, false);
-  int dev = 0;
-  if (!deterministic) {
-    if (current_device(&dev) != RMSN_OK || device_setup(dev) != RMSN_OK) return 0;
-  }
-  // the partition count of the non-deterministic mode is the larger of the two weight
-  // dtypes' occupancies, so one size serves both
-  int P = bwd_partials(static_cast<int32_t>(R), s, deterministic != 0, dev, false);
-  if (deterministic) {
-    const int Pd = bwd_partials(static_cast<int32_t>(R), bwd_shape(H, true), true, dev, false);
-    if (Pd > P) P = Pd;
-  } else {
-    int P2 = bwd_partials(static_cast<int32_t>(R), s, false, dev, true);
-    if (P2 > P) P = P2;
-    const Shape sd = bwd_shape(H, true);
-    P2 = bwd_partials(static_cast<int32_t>(R), sd, false, dev, false);
-    if (P2 > P) P = P2;
-    P2 = bwd_partials(static_cast<int32_t>(R), sd, false, dev, true);
-    if (P2 > P) P = P2;
-  }
+  // non-deterministic: the control words and the FP64 sums of the one-launch build
+  if (!deterministic) return nd_workspace_bytes(H);
+  // deterministic: P partials; the launch shape (so the partial count) may differ with
+  // and without dh, and one size serves both
+  int P = det_partials(static_cast<int32_t>(R), bwd_shape(H, false));
+  const int Pd = det_partials(static_cast<int32_t>(R), bwd_shape(H, true));
+  if (Pd > P) P = Pd;
   return static_cast<size_t>(P) * 2 * H * sizeof(float);
 }
 
@@ -397,62 +490,20 @@ int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float
                       const void* w, int w_dtype, void* dx, float* dw, void* workspace,
                       size_t workspace_bytes, int64_t T, int32_t nh, int32_t H, int64_t s_tok,
                       int64_t s_head, int deterministic, void* stream) {
-  int st = check_view(T, nh, H, s_tok, s_head, w_dtype);
-  if (st != RMSN_OK) return st;
-  if (!x || !dy || !rstd || !w || !dx || !dw) return RMSN_ERR_INVALID_ARG;
-  if (deterministic != 0 && deterministic != 1) return RMSN_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(dy) || !aligned16(dh) || !aligned16(w) || !aligned16(dx) ||
-      !aligned16(dw) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(rstd) & 3u))
-    return RMSN_ERR_INVALID_ARG;
-  const int64_t R = T * static_cast<int64_t>(nh);
+  if (!rstd) return RMSN_ERR_INVALID_ARG;
+  return bwd_common(x, dy, dh, rstd, 0.f, nullptr, w, w_dtype, dx, dw, workspace,
+                    workspace_bytes, T, nh, H, s_tok, s_head, deterministic, stream);
+}
 
-  int dev = 0;
-  if ((st = current_device(&dev)) != RMSN_OK) return st;
-  if ((st = device_setup(dev)) != RMSN_OK) return st;
-  const cudaStream_t stream_ = static_cast<cudaStream_t>(stream);
-
-  const bool fp32w = (w_dtype == RMSN_W_FP32);
-  if (bwd_is_small(R)) {  // one launch, no workspace
-    BwdArgs a{};
-    a.x = static_cast<const __nv_bfloat16*>(x);
-    a.dy = static_cast<const __nv_bfloat16*>(dy);
-    a.dh = static_cast<const __nv_bfloat16*>(dh);
-    a.rstd = rstd;
-    a.w = w;
-    a.dx = static_cast<__nv_bfloat16*>(dx);
-    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
-    a.R = static_cast<int32_t>(R);
-    a.err = g_err_ptr[dev];
-    return launch_bwd_small(a, dw, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
-  }
-  const Shape s = bwd_shape(H, dh != nullptr);
-  int P = 0;
-  if (R > 0) {
-    P = bwd_partials(static_cast<int32_t>(R), s, deterministic != 0, dev, fp32w);
-    const size_t need = static_cast<size_t>(P) * 2 * H * sizeof(float);
-    if (workspace == nullptr || workspace_bytes < need) return RMSN_ERR_WORKSPACE;
-
-    BwdArgs a{};
-    a.x = static_cast<const __nv_bfloat16*>(x);
-    a.dy = static_cast<const __nv_bfloat16*>(dy);
-    a.dh = static_cast<const __nv_bfloat16*>(dh);
-    a.rstd = rstd;
-    a.w = w;
-    a.dx = static_cast<__nv_bfloat16*>(dx);
-    a.part = static_cast<float*>(workspace);
-    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
-    a.R = static_cast<int32_t>(R);
-    a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
-    a.groups = s.groups;
-    a.ntg = s.ntg;
-    a.stages = s.stages;
-    a.P = P;
-    a.err = g_err_ptr[dev];
-    if (launch_bwd_rows(a, s, fp32w, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
-  }
-  if (launch_dw_finish(static_cast<const float*>(workspace), dw, P, H, stream_) != cudaSuccess)
-    return RMSN_ERR_CUDA;
-  return RMSN_OK;
+int rmsnorm_train_bwd_recompute(const void* x, const void* dy, const void* dh, const void* w,
+                                int w_dtype, void* dx, float* dw, float* rstd_out,
+                                void* workspace, size_t workspace_bytes, int64_t T, int32_t nh,
+                                int32_t H, int64_t s_tok, int64_t s_head, float eps,
+                                int deterministic, void* stream) {
+  if (!rstd_out || (reinterpret_cast<uintptr_t>(rstd_out) & 3u)) return RMSN_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return RMSN_ERR_INVALID_ARG;
+  return bwd_common(x, dy, dh, nullptr, eps, rstd_out, w, w_dtype, dx, dw, workspace,
+                    workspace_bytes, T, nh, H, s_tok, s_head, deterministic, stream);
 }
 
 int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out) {

@@ -1,0 +1,12 @@
+// rmsn_bwd_nd_rc.cu -- the non-deterministic row-pass builds of the RMSNorm training backward that
+// recompute rstd from the staged rows (rmsn_bwd_rows.cuh with kRc = true), in a
+// translation unit of their own so that the builds compile in parallel.
+#include "rmsn_bwd_rows.cuh"
+
+namespace rmsn {
+
+const void* bwd_rows_fn_nd_rc(const Shape& s, bool fp32w, bool dh) {
+  return pick_rows_kernel<true, true>(s, fp32w, dh);
+}
+
+}  // namespace rmsn

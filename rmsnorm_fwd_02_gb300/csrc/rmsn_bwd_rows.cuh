@@ -1,0 +1,535 @@
+// rmsn_bwd_rows.cuh -- the RMSNorm training backward's row pass for sm_103a: dx fused with
+// the compensated dw partial sums.  Included by rmsn_bwd.cu (deterministic builds: a fixed
+// chunk of rows per CTA, partials to a workspace, a separate fixed-order finish) and by
+// rmsn_bwd_nd.cu (non-deterministic builds: rows handed out as the CTAs go, partials added
+// into FP64 sums, dw rounded by the last CTA to finish; one launch).
+//
+// Per normalized row, with r the forward's rstd (flashinfer PR #8827, description: the
+// backward's BF16 dx and FP32 dw; the residual form's combined gradient):
+//   xhat_j = x_j * r,  g_j = dy_j * w_j,  c = (1/H) sum_j g_j * xhat_j
+//        = (r/H) * sum_j (dy_j * w_j) * x_j
+//   dx_j   = BF16((g_j - xhat_j * c) * r  [+ dh_j])
+//   dw_j  += dy_j * xhat_j          over every row of every CTA's rows
+//
+// dw accuracy (PR #8849 and PR #8827's route notes: every dw element within
+// atol 1e-4 + rtol 1e-4 of an FP64 sum, a budget plain FP32 running sums break at large
+// T).  Two error sources are removed: the rounding of each product and the rounding of
+// each addition.  With rstd split as rs_hi (its top 8 significant bits) + rs_lo, the
+// product dy*x*rs_hi is exact in FP32 (dy*x carries at most 16 significant bits), and
+// dy*x*rs_lo is 2^-8 smaller.  Each consumer thread keeps per column a running FP32 sum
+// of the exact products and a compensation term that collects each addition's Fast2Sum
+// error plus the small dy*x*rs_lo terms.  A CTA's groups combine into an unevaluated
+// (hi, lo) FP32 pair per column.  Deterministic builds write it as the CTA's partial; the
+// finish kernel adds the P pairs in a fixed order with Knuth's TwoSum, so dw is
+// bit-reproducible whenever P is (the row -> CTA mapping is fixed by (R, P)).
+// Non-deterministic builds add hi and lo, each exact in FP64, into an FP64 sum per column
+// (their order varies run to run, and an FP64 sum of at most a few hundred terms loses
+// nothing at FP32 precision); what remains is the final rounding of dw to FP32.  dx never
+// depends on the partition: it is bit-identical across modes.
+//
+// Split-phase rows (see the consumer loop) keep the row reduction off the critical path.
+// Arithmetic runs on packed FP32 pairs (f32x2): two columns per instruction.
+#pragma once
+
+#include "rmsn_common.cuh"
+#include "rmsn_launch.h"
+
+namespace rmsn {
+
+// Knuth's TwoSum: s + err == a + b exactly, no ordering assumption.
+__device__ __forceinline__ float two_sum(float a, float b, float& err) {
+  const float s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  const float ap = __fsub_rn(s, bp);
+  err = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+  return s;
+}
+
+// A row's two reduced sums: (dy*w)*x, and x^2 (builds that recompute rstd).
+struct RowSums {
+  float dot, ss;
+};
+
+// Loads an FP64 value from global memory at L2 (not through L1): the sums other CTAs
+// update with atomics.
+__device__ __forceinline__ double ld_cg_f64(const double* p) {
+  double v;
+  asm volatile("ld.global.cg.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Launch bounds per shape class (rmsn_launch.h): narrow CTAs of up to 256 consumers, two
+// an SM; multi-group CTAs of up to 480 consumers and wide CTAs (384 consumers with
+// 2-vector threads, 256 with 4-vector threads), one an SM; each + the producer warp.
+//
+// kRc = true: the backward is not handed rstd; phase A forms sum_j x_j^2 beside
+// sum_j (dy_j*w_j)*x_j (both through the one reduction) and phase B recomputes
+// rstd = 1/sqrt(sum x^2 / H + eps) as the forward does, writing it to a.rstd_out if given.
+// kND = false: CTA k owns rows [k*R/P, (k+1)*R/P) and writes its dw partial to a.part.
+// kND = true: the producer takes chunks of G rows (one ring stage) from the counter
+// a.ctl[0] as slots free up, one chunk ahead, and passes each chunk's first row to the
+// consumers through shared memory; a chunk start at or past R ends the CTA's work.  At
+// the end every CTA adds its partial into a.acc and takes a ticket from a.ctl[1]; the CTA
+// that takes the last ticket rounds the sums into a.dw.  Nothing waits on another CTA.
+template <int VPT, int kCls, bool kFp32W, bool kDh, bool kND, bool kRc>
+__global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_per_sm(kCls))
+    rmsn_bwd_rows_kernel(const BwdArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int NT = kDh ? 3 : 2;  // staged tensors: x, dy [, dh]
+  const int H = a.map.H;
+  const int NV = H >> 3;
+  const int G = a.groups, NTg = a.ntg, S = a.stages;
+  const int NW = NTg >> 5;
+  const size_t stage_elems = static_cast<size_t>(NT) * G * H;
+  const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
+  constexpr bool kWSmem = bwd_w_in_smem(kCls, VPT);
+  const SmemLayout L =
+      smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0, kND ? S : 0);
+
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
+  uint64_t* redb = reinterpret_cast<uint64_t*>(smem + L.redb);  // [kRedBufs][G]
+  float* slots = reinterpret_cast<float*>(smem + L.slots);       // [kRedBufs][G][32]
+  float* rs_ring = reinterpret_cast<float*>(smem + L.rs);        // [S][RSP] staged rstd
+  const int RSP = rs_stride(G);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  volatile int* last_flag = abort_flag + 1;
+  volatile int32_t* srow = reinterpret_cast<volatile int32_t*>(smem + L.srow);  // [S]
+
+  const int tid = threadIdx.x;
+  const int ncons = G * NTg;
+  const int32_t k = blockIdx.x;
+  int32_t r0 = 0, r1 = 0, nstage = 0;
+  if constexpr (!kND) {
+    r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
+    r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
+    nstage = (r1 - r0 + G - 1) / G;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
+    }
+    if (red_smem)
+      for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+
+  if (tid >= ncons) {  // ---- producer warp ----
+    if (tid == ncons) {
+      const uint64_t pol = l2_evict_first_policy();
+      const bool rs_bulk = !kRc && (reinterpret_cast<uintptr_t>(a.rstd) & 15u) == 0;
+      const RowMap m{a.map.nh, H, a.map.s_tok, a.map.s_head};
+      // rows [ra, rb) into slot s: x (strided), dy [, dh], and their rstd
+      auto issue = [&](int s, int32_t ra, int32_t rb) {
+        // The stage's rstd values travel with it, so no consumer waits on a global load:
+        // the whole 16-byte blocks of rstd covering rows [ra, rb) by one bulk copy (slot
+        // index r - a4), and rows past the last whole block of the array -- or every row,
+        // when rstd is not 16-byte aligned -- by 4-byte async copies that the same
+        // barrier tracks (one extra pending arrival, taken before the arrival below).
+        // (kRc: no rstd to stage.)
+        const int32_t a4 = ra & ~3;
+        const int32_t b4 = kRc ? a4 : (rs_bulk ? min((rb + 3) & ~3, a.R & ~3) : a4);
+        float* rsd = rs_ring + s * RSP;
+        if (!kRc && rb > b4) {
+          for (int32_t r = max(ra, b4); r < rb; ++r) cp_async_4(rsd + (r - a4), a.rstd + r);
+          cp_async_mbar_arrive(&full[s]);
+        }
+        const uint32_t rs_bytes = static_cast<uint32_t>(b4 - a4) * 4u;
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(rb - ra) * H * 2u * NT + rs_bytes);
+        if (rs_bytes) bulk_g2s(rsd, a.rstd + a4, rs_bytes, &full[s], pol);
+        __nv_bfloat16* dst = ring + s * stage_elems;
+        if (a.contig)
+          copy_rows_contig(dst, a.x, H, ra, rb, &full[s], pol);
+        else
+          copy_rows(dst, a.x, m, ra, rb, &full[s], pol);
+        copy_rows_contig(dst + G * H, a.dy, H, ra, rb, &full[s], pol);
+        if constexpr (kDh) copy_rows_contig(dst + 2 * G * H, a.dh, H, ra, rb, &full[s], pol);
+      };
+      int32_t j = 0;  // stages whose full barrier has been armed
+      if constexpr (kND) {
+        const uint32_t R = static_cast<uint32_t>(a.R);
+        uint32_t next = atomicAdd(a.ctl, static_cast<uint32_t>(G));
+        for (;; ++j) {
+          const int s = j % S;
+          if (j >= S &&
+              !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                                 a.err, kErrProducerWait))
+            break;
+          const uint32_t ra = next;
+          if (ra >= R) {  // no rows left: an empty stage tells the consumers to stop
+            srow[s] = -1;
+            mbar_arrive(&full[s]);
+            ++j;
+            break;
+          }
+          // the next chunk is taken now, so the atomic's round trip overlaps the wait
+          // for the next free slot
+          next = atomicAdd(a.ctl, static_cast<uint32_t>(G));
+          srow[s] = static_cast<int32_t>(ra);  // published by the arrival in issue()
+          issue(s, static_cast<int32_t>(ra), static_cast<int32_t>(min(ra + G, R)));
+        }
+      } else {
+        for (; j < nstage; ++j) {
+          const int s = j % S;
+          if (j >= S &&
+              !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                                 a.err, kErrProducerWait))
+            break;
+          const int32_t ra = r0 + j * G;
+          issue(s, ra, min(ra + G, r1));
+        }
+      }
+      mbar_drain(full, S, j);
+    }
+    if constexpr (!kND) return;
+    __syncwarp();  // the producer warp reconverges before the CTA-wide barriers below
+  }
+
+  // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
+  //
+  // Split-phase rows: phase A of row j forms each warp's partial of sum_j (dy*w)*x and
+  // arrives on the row's reduction mbarrier; phase B of row j-1 waits on that barrier
+  // (normally long complete), re-reads row j-1 from shared memory, and produces dx and
+  // the dw contributions.  Across rows a thread keeps only its columns' dw state and
+  // weight in registers (the 4-vector multi-group build reads the weight from shared
+  // memory instead).
+  const bool consumer = tid < ncons;
+  const int g = tid / NTg;
+  const int lt = tid - g * NTg;
+  const int wg = lt >> 5, lane = tid & 31;
+  f2 wv[kWSmem ? 1 : VPT][4];  // the weight of this thread's columns (registers)
+  f2 acc[VPT][4], cmp[VPT][4];
+  float* wsm = reinterpret_cast<float*>(smem + L.w);  // or FP32 in shared memory
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if constexpr (!kWSmem) {
+      if (consumer && c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[v][q] = f2_splat(0.f);
+      cmp[v][q] = f2_splat(0.f);
+    }
+  }
+  if (consumer) {
+    if constexpr (kWSmem) {
+      for (int c = tid; c < NV; c += ncons) {
+        f2 p[4];
+        load_w8_pairs<kFp32W>(a.w, c, p);
+        // two planes of float4 (columns 0-3 and 4-7 of each vector), so that a warp's
+        // reads of one plane are contiguous and free of bank conflicts
+        float4* d = reinterpret_cast<float4*>(wsm);
+        d[c] = make_float4(f2_lo(p[0]), f2_hi(p[0]), f2_lo(p[1]), f2_hi(p[1]));
+        d[NV + c] = make_float4(f2_lo(p[2]), f2_hi(p[2]), f2_lo(p[3]), f2_hi(p[3]));
+      }
+      named_bar_sync(14, ncons);
+    }
+  }
+  // this thread's weight pairs for column vector c (its v-th)
+  auto wvec = [&](int v, int c, f2 (&p)[4]) {
+    if constexpr (kWSmem) {
+      const float4 a4 = reinterpret_cast<const float4*>(wsm)[c];
+      const float4 b4 = reinterpret_cast<const float4*>(wsm)[NV + c];
+      p[0] = f2_make(a4.x, a4.y);
+      p[1] = f2_make(a4.z, a4.w);
+      p[2] = f2_make(b4.x, b4.y);
+      p[3] = f2_make(b4.z, b4.w);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) p[q] = wv[v][q];
+    }
+  };
+  const float inv_h = 1.0f / static_cast<float>(H);
+  const float hf = static_cast<float>(H);
+  // Phase A of group g's row in slot s (valid: the row exists): its share of
+  // sum (dy*w)*x (and, kRc, of sum x^2), reduced over the group (sub-warp groups: returned;
+  // whole-warp groups: published to the row's reduction slots).
+  auto phase_a = [&](int32_t j, int s, bool valid) -> RowSums {
+    const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+    f2 dot0 = f2_splat(0.f), dot1 = f2_splat(0.f);
+    f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);
+    if (valid) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          const uint4 xv = lds128(st + c * 8);
+          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+          f2 wl[4];
+          wvec(v, c, wl);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wl[q]);
+            const f2 x2 = bf2_to_f2(u4_get(xv, q));
+            if (q & 1) {
+              dot1 = f2_fma(gw, x2, dot1);
+              if constexpr (kRc) ss1 = f2_fma(x2, x2, ss1);
+            } else {
+              dot0 = f2_fma(gw, x2, dot0);
+              if constexpr (kRc) ss0 = f2_fma(x2, x2, ss0);
+            }
+          }
+        }
+      }
+    }
+    const f2 dsum = f2_add(dot0, dot1);
+    const float part = f2_lo(dsum) + f2_hi(dsum);
+    float spart = 0.f;
+    if constexpr (kRc) {
+      const f2 qsum = f2_add(ss0, ss1);
+      spart = f2_lo(qsum) + f2_hi(qsum);
+    }
+    if (red_smem) {
+      // slot row of 32 floats: the warps' sums of (dy*w)*x in [0, NW), of x^2 in
+      // [16, 16 + NW) (at most 12 warps a group)
+      const float dot = warp_allsum(part);
+      float ssw = 0.f;
+      if constexpr (kRc) ssw = warp_allsum(spart);
+      if (lane == 0) {
+        float* sl = slots + ((j % kRedBufs) * G + g) * 32;
+        sl[wg] = dot;
+        if constexpr (kRc) sl[16 + wg] = ssw;
+        mbar_arrive(&redb[(j % kRedBufs) * G + g]);
+      }
+      return RowSums{0.f, 0.f};
+    }
+    RowSums r{subwarp_allsum(part, NTg), 0.f};
+    if constexpr (kRc) r.ss = subwarp_allsum(spart, NTg);
+    return r;
+  };
+  // Phase B of stage jj (slot s, first row stage_ra): dx and the dw contributions.
+  auto phase_b = [&](int32_t jj, int s, int32_t stage_ra, int32_t row_end, RowSums sums) {
+    const int32_t row = stage_ra + g;
+    float dot = sums.dot, ss = sums.ss;
+    if (red_smem) {
+      const int rb = (jj % kRedBufs) * G + g;
+      mbar_wait_bounded(&redb[rb], static_cast<uint32_t>(jj / kRedBufs) & 1u, abort_flag, a.err,
+                        kErrConsumerWait);
+      dot = slot_sum(slots + rb * 32, NW);
+      if constexpr (kRc) ss = slot_sum(slots + rb * 32 + 16, NW);
+    }
+    if (row < row_end) {
+      // this row's rstd: staged with the row (the stage is held until phase B ends), or
+      // (kRc) recomputed from the row's sum of squares the way the forward forms it
+      float rs;
+      if constexpr (kRc) {
+        rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
+        if (a.rstd_out != nullptr && lt == 0) a.rstd_out[row] = rs;
+      } else {
+        rs = rs_ring[s * RSP + (row - (stage_ra & ~3))];
+      }
+      // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
+      // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
+      // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
+      const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
+      const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi);
+      const f2 rl2 = f2_splat(__fsub_rn(rs, rs_hi));
+      // c = (1/H) sum g*xhat = (rstd/H) sum (dy*w)*x
+      // dx = rstd*(g - x*(c*rstd)): xhat*c as one product of x, so the cancelling pair
+      // is a single fma; c*rstd is on the scale of dx, so no new overflow or underflow
+      const f2 ncr2 = f2_splat(-(dot * (rs * inv_h)) * rs);
+      const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      const size_t out_row = static_cast<size_t>(row) * H;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          const uint4 xv = lds128(st + c * 8);
+          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+          uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (kDh) hv = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+          f2 wl[4];
+          wvec(v, c, wl);
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const f2 x2 = bf2_to_f2(u4_get(xv, q));
+            const f2 d2 = bf2_to_f2(u4_get(dv, q));
+            const f2 gw = f2_mul(d2, wl[q]);
+            f2 d = f2_mul(f2_fma(x2, ncr2, gw), rs2);  // (g - xhat*c) * rstd
+            if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
+            o[q] = f2_to_bf2(d);
+            // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
+            // compensation term, which also collects dy*x*rs_lo
+            const f2 dyx = f2_mul(d2, x2);
+            const f2 p = f2_mul(dyx, rh2);
+            const f2 t = f2_add(acc[v][q], p);
+            const f2 e = f2_add(f2_sub(acc[v][q], t), p);
+            cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
+            acc[v][q] = t;
+          }
+          stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
+  };
+
+  if (consumer) {
+    if constexpr (kND) {
+      // Stages in the order the producer filled them; a negative chunk start (or an
+      // abort) ends the loop, warp-uniformly (every lane reads the same start).
+      RowSums carry{0.f, 0.f};
+      int32_t ra_prev = 0;
+      for (int32_t j = 0;; ++j) {
+        const int s = j % S;
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u,
+                                          abort_flag, a.err, kErrConsumerWait);
+        const int32_t ra = ok ? srow[s] : -1;
+        const bool stop = __any_sync(0xffffffffu, ra < 0);
+        RowSums cur{0.f, 0.f};
+        if (!stop) cur = phase_a(j, s, ra + g < a.R);
+        if (j >= 1) phase_b(j - 1, (j - 1) % S, ra_prev, a.R, carry);
+        if (stop) break;
+        ra_prev = ra;
+        carry = cur;
+      }
+    } else {
+      // Rows of this warp's first group: every lane of a warp runs the same iterations
+      // (the shuffles need them all); groups past the chunk's end skip the row work.
+      const int g0 = red_smem ? g : (tid & ~31) / NTg;
+      const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
+      RowSums carry{0.f, 0.f};  // sub-warp groups: row j-1's sums
+      for (int32_t j = 0; j <= ng; ++j) {
+        RowSums cur{0.f, 0.f};
+        if (j < ng) {
+          const int s = j % S;
+          mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                            kErrConsumerWait);
+          cur = phase_a(j, s, r0 + j * G + g < r1);
+        }
+        if (j >= 1) phase_b(j - 1, (j - 1) % S, r0 + (j - 1) * G, r1, carry);
+        carry = cur;
+      }
+    }
+  }
+
+  // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----
+  // Deterministic builds store it to a.part[k]; non-deterministic ones add hi and lo into
+  // the FP64 sums a.acc.
+  auto emit = [&](int col, float hi, float lo) {
+    if constexpr (kND) {
+      atomicAdd(a.acc + col, static_cast<double>(hi));
+      atomicAdd(a.acc + col, static_cast<double>(lo));
+    } else {
+      float* part = a.part + static_cast<size_t>(k) * 2 * H;
+      part[col] = hi;
+      part[H + col] = lo;
+    }
+  };
+  if (consumer) {
+    if (G == 1) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          f2 hi[4], lo[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            hi[q] = f2_add(acc[v][q], cmp[v][q]);
+            lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
+          }
+          if constexpr (kND) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              emit(c * 8 + 2 * q, f2_lo(hi[q]), f2_lo(lo[q]));
+              emit(c * 8 + 2 * q + 1, f2_hi(hi[q]), f2_hi(lo[q]));
+            }
+          } else {
+            float* part = a.part + static_cast<size_t>(k) * 2 * H;
+            ulonglong2* ph = reinterpret_cast<ulonglong2*>(part + c * 8);
+            ulonglong2* pl = reinterpret_cast<ulonglong2*>(part + H + c * 8);
+            ph[0] = make_ulonglong2(hi[0].v, hi[1].v);
+            ph[1] = make_ulonglong2(hi[2].v, hi[3].v);
+            pl[0] = make_ulonglong2(lo[0].v, lo[1].v);
+            pl[1] = make_ulonglong2(lo[2].v, lo[3].v);
+          }
+        }
+      }
+    } else {
+      // several row groups: combine them through shared memory in group order.  The ring
+      // is free once every consumer is past its loop: each stage was waited on (full) by
+      // every group that had a row in it before that group finished.
+      named_bar_sync(15, ncons);
+      // cb: [G][2][H] (hi, lo), each H-slab stored as two planes of float4 (columns 0-3
+      // and 4-7 of every vector) so that a warp's stores of one plane are contiguous
+      float* cb = reinterpret_cast<float*>(smem);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int c = lt + v * NTg;
+        if (c < NV) {
+          f2 hi[4], lo[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            hi[q] = f2_add(acc[v][q], cmp[v][q]);
+            lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
+          }
+          ulonglong2* ph = reinterpret_cast<ulonglong2*>(cb + (2 * g) * H);
+          ulonglong2* pl = reinterpret_cast<ulonglong2*>(cb + (2 * g + 1) * H);
+          ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
+          ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
+          pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
+          pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
+        }
+      }
+      named_bar_sync(15, ncons);
+      for (int col = tid; col < H; col += ncons) {
+        const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
+        float sacc = 0.f, e = 0.f;
+        for (int gi = 0; gi < G; ++gi) {
+          float err;
+          sacc = two_sum(sacc, cb[(2 * gi) * H + at], err);
+          e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + at]));
+        }
+        const float hi = __fadd_rn(sacc, e);
+        emit(col, hi, __fsub_rn(e, __fsub_rn(hi, sacc)));
+      }
+    }
+  }
+  if constexpr (kND) {
+    // Every CTA, producer included, takes a ticket once its additions are visible
+    // (fence, then the CTA barrier); the CTA with the last ticket rounds the sums.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      *last_flag = atomicAdd(a.ctl + 1, 1u) == static_cast<uint32_t>(gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_flag) {
+      __threadfence();
+      for (int col = tid; col < H; col += blockDim.x)
+        a.dw[col] = static_cast<float>(ld_cg_f64(a.acc + col));
+    }
+  }
+}
+
+// The kernel build for a launch shape, per (kND, kRc) pair; each pair's translation unit
+// instantiates only its own builds.  (bwd_shape gives 1-vector lanes the narrow class, 2-
+// and 4-vector threads the multi or the wide class, 3-vector threads the multi class.)
+template <bool kND, bool kRc>
+const void* pick_rows_kernel(const Shape& s, bool fp32w, bool dh) {
+  auto fn = [](auto k) { return reinterpret_cast<const void*>(k); };
+#define RMSN_PICK(V, C)                                                              \
+  (fp32w ? (dh ? fn(&rmsn_bwd_rows_kernel<V, C, true, true, kND, kRc>)               \
+               : fn(&rmsn_bwd_rows_kernel<V, C, true, false, kND, kRc>))             \
+         : (dh ? fn(&rmsn_bwd_rows_kernel<V, C, false, true, kND, kRc>)              \
+               : fn(&rmsn_bwd_rows_kernel<V, C, false, false, kND, kRc>)))
+  if (s.vpt == 1) return RMSN_PICK(1, kBwdNarrow);
+  if (s.vpt == 2) return s.cls == kBwdMulti ? RMSN_PICK(2, kBwdMulti) : RMSN_PICK(2, kBwdWide);
+  if (s.vpt == 3) return RMSN_PICK(3, kBwdMulti);
+  return s.cls == kBwdMulti ? RMSN_PICK(4, kBwdMulti) : RMSN_PICK(4, kBwdWide);
+#undef RMSN_PICK
+}
+
+}  // namespace rmsn

@@ -22,7 +22,10 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 //   rs     [stages][rs_stride(rs_rows)] FP32: the staged rows' rstd (backward; forward:
 //          none), from the 16-byte block holding the stage's first row onwards
 //   w      [w_floats] FP32 weight, for builds that keep it in shared memory
-//   abort  CTA abort flag of the bounded waits
+//   abort  CTA abort flag of the bounded waits (word 0); word 1: the backward's
+//          last-CTA flag (one-launch non-deterministic build)
+//   srow   [srow_stages] first row of each staged chunk (builds whose producer takes
+//          chunks dynamically; others: none)
 //
 // Row j's reduction uses buffer j % kRedBufs.  A warp writes buffer j in phase A(j) after
 // finishing B(j-2), which needed every warp's A(j-2), which each warp issues after its
@@ -30,7 +33,7 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 // same ordering keeps each redb barrier within one phase of its waiters.
 constexpr int kRedBufs = 4;
 struct SmemLayout {
-  size_t full, empty, redb, slots, rs, w, abort_flag, total;
+  size_t full, empty, redb, slots, rs, w, abort_flag, srow, total;
 };
 
 // Floats per stage of the staged rstd: the stage's `rows` values start up to 3 floats
@@ -42,7 +45,7 @@ __host__ __device__ constexpr int rs_stride(int rows) { return rows == 0 ? 0 : (
 // `rs_rows` is the number of rstd values staged with each stage (the backward's groups).
 __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int groups, int H,
                                                   int red_groups, int rs_rows,
-                                                  int w_floats = 0) {
+                                                  int w_floats = 0, int srow_stages = 0) {
   SmemLayout L;
   size_t off = static_cast<size_t>(stages) * tensors * groups * H * 2;  // multiple of 16
   L.full = off;
@@ -60,6 +63,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int tensors, int g
   off += 4 * static_cast<size_t>(w_floats);
   L.abort_flag = off;
   off += 16;
+  L.srow = off;
+  off += 4 * ((static_cast<size_t>(srow_stages) + 3) & ~static_cast<size_t>(3));
   L.total = off;
   return L;
 }
@@ -106,6 +111,15 @@ struct BwdArgs {
   const void* w;
   __nv_bfloat16* dx;          // contiguous
   float* part;                // [P][2][H]: compensated dw partial per CTA (hi row, lo row)
+  // one-launch non-deterministic build: ctl[0] next row to hand out, ctl[1] CTAs done;
+  // acc[H] FP64 sums of the CTAs' partials; dw written by the last CTA to finish
+  unsigned* ctl;
+  double* acc;
+  float* dw;
+  // rstd == nullptr: the row pass recomputes rstd (eps as in the forward) and writes it to
+  // rstd_out when that is not null
+  float eps;
+  float* rstd_out;
   RowMapArgs map;
   int32_t R;
   int32_t contig;
@@ -120,8 +134,30 @@ Shape bwd_shape(int H, bool with_dh);
 // Launchers: return the CUDA launch status.  `pdl` opts the launch into programmatic
 // dependent launch (overlap with the previous kernel on the stream).
 cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
+// The row-pass kernel build for a shape: deterministic (fixed chunks, partials to the
+// workspace) or not (rows handed out, FP64 sums), with rstd given or recomputed (rc).
+// One translation unit per (nd, rc) pair: rmsn_bwd.cu, rmsn_bwd_rc.cu, rmsn_bwd_nd.cu,
+// rmsn_bwd_nd_rc.cu.
+const void* bwd_rows_fn(const Shape& s, bool fp32w, bool dh, bool nd, bool rc);
+const void* bwd_rows_fn_det(const Shape& s, bool fp32w, bool dh);
+const void* bwd_rows_fn_det_rc(const Shape& s, bool fp32w, bool dh);
+const void* bwd_rows_fn_nd(const Shape& s, bool fp32w, bool dh);
+const void* bwd_rows_fn_nd_rc(const Shape& s, bool fp32w, bool dh);
+
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
+
+// Non-deterministic backward in one row-pass launch (rmsn_bwd_nd.cu): CTAs take chunks of
+// rows from a counter as they go, and each adds its dw partial into FP64 sums that the
+// last CTA to finish rounds into dw.  Its workspace is the control words and the sums,
+// zeroed on the stream by a one-CTA kernel launched just before the row pass.
+constexpr size_t kNdCtlBytes = 16;
+__host__ __device__ constexpr size_t nd_workspace_bytes(int H) {
+  return kNdCtlBytes + sizeof(double) * static_cast<size_t>(H);
+}
+Shape nd_shape(const Shape& s, int H);  // + the chunk-start slots in shared memory
+int bwd_nd_blocks_per_sm(const Shape& s, bool fp32w, bool rc);
+cudaError_t launch_bwd_nd(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 
 // Small inputs (rmsn_small.cu): the whole backward in one launch of row tasks (dx) and
 // column tasks (dw over every row in a fixed order), no workspace, for R <= kSmallMaxRows.
@@ -131,6 +167,9 @@ constexpr int kSmallSlices = kSmallThreads / kSmallColVecs;   // row slices a co
 constexpr int64_t kSmallMaxRows = 256;
 bool bwd_is_small(int64_t R);
 cudaError_t launch_bwd_small(const BwdArgs& a, float* dw, bool fp32w, cudaStream_t st);
+// rstd of rows [0, R) into `rstd` (one warp a row, the forward's formula), for the small
+// path of the backward that recomputes rstd.
+cudaError_t launch_rstd_rows(const BwdArgs& a, float* rstd, cudaStream_t st);
 
 // Backward shape classes, each its own kernel build:
 //  kBwdNarrow  up to 256 consumers, two CTAs an SM: one-vector lanes (H = 8)
@@ -181,6 +220,5 @@ constexpr int fwd_max_threads(int cls, int vpt) {
 
 // Resident CTAs per SM of the chosen row kernel (cached per device).
 int fwd_blocks_per_sm(const Shape& s, bool fp32w);
-int bwd_blocks_per_sm(const Shape& s, bool fp32w);
 
 }  // namespace rmsn

@@ -228,6 +228,51 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 
 bool bwd_is_small(int64_t R) { return R > 0 && R <= kSmallMaxRows; }
 
+// rstd of rows [0, a.R) for the backward that recomputes it on the one-launch path: one
+// warp a row, the row's 16-byte vectors strided over the lanes, the sum of squares in FP32
+// (BF16 squares are exact; the additions round), then the forward's correctly rounded
+// 1/sqrt(sum/H + eps).
+constexpr int kRstdRowsPerCta = 8;
+__global__ void __launch_bounds__(32 * kRstdRowsPerCta)
+    rmsn_rstd_rows_kernel(const BwdArgs a, float* __restrict__ rstd) {
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+  const int H = a.map.H;
+  const int NV = H >> 3;
+  const int lane = threadIdx.x & 31;
+  const int32_t row = static_cast<int32_t>(blockIdx.x) * kRstdRowsPerCta +
+                      static_cast<int32_t>(threadIdx.x >> 5);
+  if (row >= a.R) return;  // the whole warp
+  const int32_t t = row / a.map.nh;
+  const int32_t hd = row - t * a.map.nh;
+  const __nv_bfloat16* xr = a.x + static_cast<int64_t>(t) * a.map.s_tok +
+                            static_cast<int64_t>(hd) * a.map.s_head;
+  f2 s0 = f2_splat(0.f), s1 = f2_splat(0.f);
+  for (int c = lane; c < NV; c += 32) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + c * 8);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const f2 x2 = bf2_to_f2(u4_get(v, q));
+      if (q & 1)
+        s1 = f2_fma(x2, x2, s1);
+      else
+        s0 = f2_fma(x2, x2, s0);
+    }
+  }
+  const f2 sq = f2_add(s0, s1);
+  const float ss = warp_allsum(f2_lo(sq) + f2_hi(sq));
+  if (lane == 0)
+    rstd[row] = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(H)), a.eps));
+}
+
+cudaError_t launch_rstd_rows(const BwdArgs& a, float* rstd, cudaStream_t st) {
+  const void* fn = reinterpret_cast<const void*>(&rmsn_rstd_rows_kernel);
+  BwdArgs copy = a;
+  void* args[] = {&copy, &rstd};
+  const unsigned grid = static_cast<unsigned>((a.R + kRstdRowsPerCta - 1) / kRstdRowsPerCta);
+  return launch_pdl(fn, dim3(grid), dim3(32 * kRstdRowsPerCta), 0, st, args);
+}
+
 cudaError_t launch_bwd_small(const BwdArgs& a, float* dw, bool fp32w, cudaStream_t st) {
   const int NV = a.map.H / 8;
   const int vpt = (NV + kSmallThreads - 1) / kSmallThreads;  // 1..4 for H <= 8192

@@ -211,3 +211,57 @@ def test_deterministic_workspace_covers_both_dh_plans(lib):
                 P = min(-(-T // p["groups"]), 152 * p["class_blocks_per_sm"])
                 need = max(need, P * 2 * H * 4)
             assert lib.rmsnorm_train_bwd_workspace_bytes(T, 1, H, 1) == need, (H, T)
+
+
+def test_nondeterministic_workspace_is_control_words_and_fp64_sums(lib):
+    # the one-launch non-deterministic backward: 16 bytes of counters + H FP64 sums, for
+    # every row count past the one-launch small path; no device query needed
+    f = lib.rmsnorm_train_bwd_workspace_bytes
+    for H in (8, 256, 1536, 4096, 6144, 8192):
+        assert f(256, 1, H, 0) == 0
+        for T in (257, 4096, 131072):
+            assert f(T, 1, H, 0) == 16 + 8 * H, (H, T)
+    assert f(65536, 24, 256, 0) == 16 + 8 * 256
+    assert f(0, 1, 4096, 0) == 0
+
+
+@pytest.mark.parametrize("op", [2, 3], ids=["bwd", "bwd_dh"])
+def test_nondeterministic_build_fits_shared_memory_at_every_width(lib, op):
+    # the non-deterministic row pass adds one chunk-start word per ring stage (rounded to
+    # 16 bytes) to the deterministic build's shared memory
+    from rmsnorm_fwd_02_gb300 import _native as N
+    for H in range(8, 8193, 8):
+        p = N.rmsnorm_train_launch_plan(H, op)
+        smem = p["smem"] + 4 * ((p["stages"] + 3) // 4 * 4)
+        assert smem <= SMEM_PER_CTA, (H, p)
+        assert p["class_blocks_per_sm"] * (smem + 1024) <= SMEM_PER_SM, (H, p)
+
+
+def test_noalloc_scratch_covers_every_supported_shape(lib):
+    # rmsnorm_train_bwd_noalloc keeps its workspace in a 16 MiB array: the deterministic
+    # partition is at most 152 x (CTAs an SM) partials of 2*H floats, the non-deterministic
+    # workspace 16 + 8*H bytes, so no supported shape reaches the limit
+    f = lib.rmsnorm_train_bwd_workspace_bytes
+    for H in range(8, 8193, 8):
+        for det in (0, 1):
+            assert f(1 << 20, 1, H, det) <= 16 << 20, (H, det)
+
+
+def test_recompute_rejects_before_any_cuda_call(lib):
+    f = lib.rmsnorm_train_bwd_recompute
+    args = dict(x=BAD_PTR, dy=BAD_PTR, dh=None, w=BAD_PTR, wd=0, dx=BAD_PTR2, dw=BAD_PTR2,
+                rs=BAD_PTR2, ws=None, wsb=0, T=300, nh=1, H=4096, st=4096, sh=4096, eps=1e-6,
+                det=1)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["dy"], a["dh"], a["w"], a["wd"], a["dx"], a["dw"], a["rs"], a["ws"],
+                 a["wsb"], a["T"], a["nh"], a["H"], a["st"], a["sh"], a["eps"], a["det"], None)
+
+    assert call(rs=None) == INVALID                  # rstd_out is required
+    assert call(rs=BAD_PTR2 + 2) == INVALID          # and 4-byte aligned
+    assert call(eps=float("nan")) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(H=12, st=12, sh=12) == INVALID
+    assert call(x=None) == INVALID
+    assert call(det=3) == INVALID

@@ -5,7 +5,7 @@ instead of a caller workspace.
 
 Called through the C ABI, it must give what rmsnorm_train_bwd gives with a workspace:
 dx within the 1-BF16-ulp gate and dw within the per-element budget of each other (in
-fact the same kernels run, so the bits match).  Two calls in a row on different shapes
+fact the same kernels run, so dx's bits match, and dw's in the deterministic mode).  Two calls in a row on different shapes
 check that the shared array's leftover contents from the previous call never leak into
 the next one.  This file sorts last so a stop-at-first-failure run has already run
 every other test; it also passes alone in a fresh process.
@@ -35,14 +35,17 @@ def _without_workspace(dc, rstd, det):
     return dx, dw
 
 
-def _agree(a, b):
+def _agree(a, b, det):
     (dx_a, dw_a), (dx_b, dw_b) = a, b
     ba, bb = parity.bits_of(dx_a), parity.bits_of(dx_b)
     assert np.abs(parity.ordinal(ba) - parity.ordinal(bb)).max() <= 1
     wa, wb = dw_a.cpu().numpy().astype(np.float64), dw_b.cpu().numpy().astype(np.float64)
     assert np.all(np.abs(wa - wb) <= parity.DW_ATOL + parity.DW_RTOL * np.abs(wa))
-    # same kernels, same partition: identical bits
-    assert np.array_equal(ba, bb) and np.array_equal(wa, wb)
+    # the same kernels run: dx is identical; so is dw in the deterministic mode (the
+    # non-deterministic one hands rows to its CTAs as they come, so dw's last bits vary)
+    assert np.array_equal(ba, bb)
+    if det:
+        assert np.array_equal(wa, wb)
 
 
 @pytest.mark.parametrize("det", [1, 0])
@@ -55,7 +58,7 @@ def test_noalloc_matches_workspace_backward_on_two_calls_in_a_row(det):
         ref = _with_workspace(dc, rstd, det)
         first = _without_workspace(dc, rstd, det)
         torch.cuda.synchronize()
-        _agree(ref, first)
+        _agree(ref, first, det)
     # and back to the first shape: the array now holds the last shape's partials
     c = cases[0]
     dc = parity.DeviceCase(c)
@@ -63,7 +66,7 @@ def test_noalloc_matches_workspace_backward_on_two_calls_in_a_row(det):
     ref = _with_workspace(dc, rstd, det)
     again = _without_workspace(dc, rstd, det)
     torch.cuda.synchronize()
-    _agree(ref, again)
+    _agree(ref, again, det)
     assert N.rmsnorm_train_device_error(reset=True) == 0
 
 
