@@ -57,11 +57,11 @@ __device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t* bar, uint32_
                                                           volatile int* abort_flag,
                                                           unsigned* err_word, unsigned errbit) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  unsigned long long prev = global_ns(), waited = 0;
   for (;;) {
     if (*abort_flag) return false;
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (wait_expired(prev, waited)) {
       atomicOr(err_word, errbit);
       *abort_flag = 1;
       return false;

@@ -342,41 +342,25 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     return launch_bwd_small(a, dw, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
   }
   const Shape s = bwd_shape(H, dh != nullptr);
-  if (R > 0 && !deterministic) {
-    // one launch: rows handed out as the CTAs go, dw finished by the last CTA
-    if (workspace == nullptr || workspace_bytes < nd_workspace_bytes(H)) return RMSN_ERR_WORKSPACE;
-    const Shape sn = nd_shape(s, H);
-    const int occ = bwd_nd_blocks_per_sm(sn, fp32w, rstd == nullptr);
-    const int64_t per = s.groups;
-    int64_t P = (R + per - 1) / per;
-    const int64_t cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
-    if (P > cap) P = cap;
-    BwdArgs a{};
-    a.x = static_cast<const __nv_bfloat16*>(x);
-    a.dy = static_cast<const __nv_bfloat16*>(dy);
-    a.dh = static_cast<const __nv_bfloat16*>(dh);
-    a.rstd = rstd;
-    a.eps = eps;
-    a.rstd_out = rstd_out;
-    a.w = w;
-    a.dx = static_cast<__nv_bfloat16*>(dx);
-    a.ctl = static_cast<unsigned*>(workspace);
-    a.acc = reinterpret_cast<double*>(static_cast<unsigned char*>(workspace) + kNdCtlBytes);
-    a.dw = dw;
-    a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
-    a.R = static_cast<int32_t>(R);
-    a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
-    a.groups = s.groups;
-    a.ntg = s.ntg;
-    a.stages = s.stages;
-    a.P = static_cast<int32_t>(P);
-    a.err = g_err_ptr[dev];
-    return launch_bwd_nd(a, sn, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
-  }
+  // deterministic: the partials start at the workspace; non-deterministic: after the row
+  // counter
+  const size_t ctl_bytes = deterministic ? 0 : kNdCtlBytes;
+  float* part = workspace ? reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                                     ctl_bytes)
+                          : nullptr;
   int P = 0;
   if (R > 0) {
+    // at most 152 x (CTAs an SM of the class) partials in either mode (the deterministic
+    // partition; the non-deterministic one is also bounded by this GPU's resident CTAs)
     P = det_partials(static_cast<int32_t>(R), s);
-    const size_t need = static_cast<size_t>(P) * 2 * H * sizeof(float);
+    Shape sl = s;
+    if (!deterministic) {
+      sl = nd_shape(s, H);
+      const int occ = bwd_nd_blocks_per_sm(sl, fp32w, rstd == nullptr);
+      const int64_t cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
+      if (P > cap) P = static_cast<int>(cap);
+    }
+    const size_t need = ctl_bytes + static_cast<size_t>(P) * 2 * H * sizeof(float);
     if (workspace == nullptr || workspace_bytes < need) return RMSN_ERR_WORKSPACE;
 
     BwdArgs a{};
@@ -388,7 +372,8 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     a.rstd_out = rstd_out;
     a.w = w;
     a.dx = static_cast<__nv_bfloat16*>(dx);
-    a.part = static_cast<float*>(workspace);
+    a.part = part;
+    a.ctl = static_cast<unsigned*>(workspace);
     a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
     a.R = static_cast<int32_t>(R);
     a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
@@ -397,9 +382,11 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     a.stages = s.stages;
     a.P = P;
     a.err = g_err_ptr[dev];
-    if (launch_bwd_rows(a, s, fp32w, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
+    const cudaError_t e = deterministic ? launch_bwd_rows(a, sl, fp32w, stream_)
+                                        : launch_bwd_nd(a, sl, fp32w, stream_);
+    if (e != cudaSuccess) return RMSN_ERR_CUDA;
   }
-  if (launch_dw_finish(static_cast<const float*>(workspace), dw, P, H, stream_) != cudaSuccess)
+  if (launch_dw_finish(part, dw, P, H, stream_) != cudaSuccess)
     return RMSN_ERR_CUDA;
   return RMSN_OK;
 }
@@ -476,14 +463,12 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
     return 0;
   const int64_t R = T * static_cast<int64_t>(nh);
   if (R == 0 || bwd_is_small(R)) return 0;  // small inputs take the one-launch path
-  // non-deterministic: the control words and the FP64 sums of the one-launch build
-  if (!deterministic) return nd_workspace_bytes(H);
-  // deterministic: P partials; the launch shape (so the partial count) may differ with
-  // and without dh, and one size serves both
+  // P partials (the launch shape, so the partial count, may differ with and without dh:
+  // one size serves both), after the row counter in the non-deterministic mode
   int P = det_partials(static_cast<int32_t>(R), bwd_shape(H, false));
   const int Pd = det_partials(static_cast<int32_t>(R), bwd_shape(H, true));
   if (Pd > P) P = Pd;
-  return static_cast<size_t>(P) * 2 * H * sizeof(float);
+  return (deterministic ? 0 : kNdCtlBytes) + static_cast<size_t>(P) * 2 * H * sizeof(float);
 }
 
 int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float* rstd,

@@ -1,27 +1,24 @@
 // rmsn_bwd_nd.cu -- RMSNorm training backward for sm_103a, non-deterministic builds: the
-// whole backward in one row-pass launch (rmsn_bwd_rows.cuh with kND = true), preceded by a
-// one-CTA kernel that zeroes its control words and FP64 sums.
+// row pass of rmsn_bwd_rows.cuh with kND = true, whose CTAs take chunks of rows from an
+// atomic counter as they go, preceded by a one-CTA kernel that zeroes that counter, and
+// followed by the fixed-order dw finish.
 //
-// flashinfer PR #8827 (description) leaves deterministic=False free to be faster, and the
-// pages' non-deterministic routes are single kernels (PR #8848: "blocked FP32" dw sums in
-// one kernel; PR #8899: the kb programs).  Here the mode buys two things the fixed
-// partition cannot have: rows are handed out as the CTAs go (no CTA idles while another
-// still has a queue of rows), and dw is finished by the last CTA without a second launch
-// and a grid-wide drain in between.  dx is the deterministic build's, bit for bit.
+// flashinfer PR #8827 (description) leaves deterministic=False free to be faster.  What the
+// mode buys here is the partition: with rows handed out as CTAs free up, no CTA idles
+// while another still holds a queue of rows, and all CTAs stream through neighbouring rows
+// together.  dx is the deterministic build's, bit for bit; dw's partials cover rows that
+// vary from run to run, so its last bits may too.
 #include "rmsn_bwd_rows.cuh"
 
 namespace rmsn {
 
-// Zeroes the row counter, the ticket counter and the H FP64 sums of one call.  It lets the
-// row pass be scheduled at once (that grid still waits for this one to finish before it
-// touches the workspace), and waits for the previous grid on the stream, which may be an
-// earlier call still reading the same workspace.
-__global__ void __launch_bounds__(256) rmsn_nd_prep_kernel(unsigned* ctl, double* acc, int H) {
+// Zeroes the row counter of one call.  It lets the row pass be scheduled at once (that
+// grid still waits for this one to finish before it touches the workspace), and waits for
+// the previous grid on the stream, which may be an earlier call still using the counter.
+__global__ void __launch_bounds__(32) rmsn_nd_prep_kernel(unsigned* ctl) {
   pdl_allow_next_grid();
   pdl_wait_prior_grid();
   if (threadIdx.x < kNdCtlBytes / sizeof(unsigned)) ctl[threadIdx.x] = 0u;
-  double2* a2 = reinterpret_cast<double2*>(acc);  // 16-byte aligned: the workspace + 16
-  for (int i = threadIdx.x; i < H / 2; i += blockDim.x) a2[i] = make_double2(0.0, 0.0);
 }
 
 const void* bwd_rows_fn_nd(const Shape& s, bool fp32w, bool dh) {
@@ -42,10 +39,8 @@ cudaError_t launch_bwd_nd(const BwdArgs& a, const Shape& s, bool fp32w, cudaStre
   cudaError_t e = prepare_kernel(fn, s.smem);
   if (e != cudaSuccess) return e;
   unsigned* ctl = a.ctl;
-  double* acc = a.acc;
-  int H = a.map.H;
-  void* pargs[] = {&ctl, &acc, &H};
-  e = launch_pdl(reinterpret_cast<const void*>(&rmsn_nd_prep_kernel), dim3(1), dim3(256), 0, st,
+  void* pargs[] = {&ctl};
+  e = launch_pdl(reinterpret_cast<const void*>(&rmsn_nd_prep_kernel), dim3(1), dim3(32), 0, st,
                  pargs);
   if (e != cudaSuccess) return e;
   BwdArgs copy = a;

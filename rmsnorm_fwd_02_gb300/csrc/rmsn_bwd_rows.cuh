@@ -1,8 +1,8 @@
 // rmsn_bwd_rows.cuh -- the RMSNorm training backward's row pass for sm_103a: dx fused with
 // the compensated dw partial sums.  Included by rmsn_bwd.cu (deterministic builds: a fixed
-// chunk of rows per CTA, partials to a workspace, a separate fixed-order finish) and by
-// rmsn_bwd_nd.cu (non-deterministic builds: rows handed out as the CTAs go, partials added
-// into FP64 sums, dw rounded by the last CTA to finish; one launch).
+// chunk of rows per CTA) and by rmsn_bwd_nd.cu (non-deterministic builds: rows handed out
+// as the CTAs go); both write one dw partial per CTA to the workspace, and the
+// fixed-order finish kernel (rmsn_bwd.cu) adds them.
 //
 // Per normalized row, with r the forward's rstd (flashinfer PR #8827, description: the
 // backward's BF16 dx and FP32 dw; the residual form's combined gradient):
@@ -19,13 +19,11 @@
 // dy*x*rs_lo is 2^-8 smaller.  Each consumer thread keeps per column a running FP32 sum
 // of the exact products and a compensation term that collects each addition's Fast2Sum
 // error plus the small dy*x*rs_lo terms.  A CTA's groups combine into an unevaluated
-// (hi, lo) FP32 pair per column.  Deterministic builds write it as the CTA's partial; the
-// finish kernel adds the P pairs in a fixed order with Knuth's TwoSum, so dw is
-// bit-reproducible whenever P is (the row -> CTA mapping is fixed by (R, P)).
-// Non-deterministic builds add hi and lo, each exact in FP64, into an FP64 sum per column
-// (their order varies run to run, and an FP64 sum of at most a few hundred terms loses
-// nothing at FP32 precision); what remains is the final rounding of dw to FP32.  dx never
-// depends on the partition: it is bit-identical across modes.
+// (hi, lo) FP32 pair per column, written as the CTA's partial; the finish kernel adds the
+// P pairs in a fixed order with Knuth's TwoSum, so dw is bit-reproducible whenever the
+// row -> CTA mapping is (deterministic builds: fixed by (R, P)).  What remains is about the
+// final rounding of dw to FP32.  dx never depends on the partition: it is bit-identical
+// across modes.
 //
 // Split-phase rows (see the consumer loop) keep the row reduction off the critical path.
 // Arithmetic runs on packed FP32 pairs (f32x2): two columns per instruction.
@@ -50,14 +48,6 @@ struct RowSums {
   float dot, ss;
 };
 
-// Loads an FP64 value from global memory at L2 (not through L1): the sums other CTAs
-// update with atomics.
-__device__ __forceinline__ double ld_cg_f64(const double* p) {
-  double v;
-  asm volatile("ld.global.cg.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Launch bounds per shape class (rmsn_launch.h): narrow CTAs of up to 256 consumers, two
 // an SM; multi-group CTAs of up to 480 consumers and wide CTAs (384 consumers with
 // 2-vector threads, 256 with 4-vector threads), one an SM; each + the producer warp.
@@ -65,12 +55,12 @@ __device__ __forceinline__ double ld_cg_f64(const double* p) {
 // kRc = true: the backward is not handed rstd; phase A forms sum_j x_j^2 beside
 // sum_j (dy_j*w_j)*x_j (both through the one reduction) and phase B recomputes
 // rstd = 1/sqrt(sum x^2 / H + eps) as the forward does, writing it to a.rstd_out if given.
-// kND = false: CTA k owns rows [k*R/P, (k+1)*R/P) and writes its dw partial to a.part.
+// kND = false: CTA k owns rows [k*R/P, (k+1)*R/P).
 // kND = true: the producer takes chunks of G rows (one ring stage) from the counter
 // a.ctl[0] as slots free up, one chunk ahead, and passes each chunk's first row to the
-// consumers through shared memory; a chunk start at or past R ends the CTA's work.  At
-// the end every CTA adds its partial into a.acc and takes a ticket from a.ctl[1]; the CTA
-// that takes the last ticket rounds the sums into a.dw.  Nothing waits on another CTA.
+// consumers through shared memory; a chunk start at or past R ends the CTA's work.  A CTA
+// that frees up early takes more rows, so no CTA idles while another still holds a queue.
+// Either way CTA k writes its dw partial to a.part[k].
 template <int VPT, int kCls, bool kFp32W, bool kDh, bool kND, bool kRc>
 __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_per_sm(kCls))
     rmsn_bwd_rows_kernel(const BwdArgs a) {
@@ -94,7 +84,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   float* rs_ring = reinterpret_cast<float*>(smem + L.rs);        // [S][RSP] staged rstd
   const int RSP = rs_stride(G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
-  volatile int* last_flag = abort_flag + 1;
   volatile int32_t* srow = reinterpret_cast<volatile int32_t*>(smem + L.srow);  // [S]
 
   const int tid = threadIdx.x;
@@ -115,7 +104,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     if (red_smem)
       for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
     *abort_flag = 0;
-    *last_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -189,8 +177,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       }
       mbar_drain(full, S, j);
     }
-    if constexpr (!kND) return;
-    __syncwarp();  // the producer warp reconverges before the CTA-wide barriers below
+    return;
   }
 
   // ---- consumers: group g, thread lt owns column vectors c = lt + v*NTg ----
@@ -201,7 +188,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   // the dw contributions.  Across rows a thread keeps only its columns' dw state and
   // weight in registers (the 4-vector multi-group build reads the weight from shared
   // memory instead).
-  const bool consumer = tid < ncons;
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
@@ -212,7 +198,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
     if constexpr (!kWSmem) {
-      if (consumer && c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
+      if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -220,19 +206,17 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       cmp[v][q] = f2_splat(0.f);
     }
   }
-  if (consumer) {
-    if constexpr (kWSmem) {
-      for (int c = tid; c < NV; c += ncons) {
-        f2 p[4];
-        load_w8_pairs<kFp32W>(a.w, c, p);
-        // two planes of float4 (columns 0-3 and 4-7 of each vector), so that a warp's
-        // reads of one plane are contiguous and free of bank conflicts
-        float4* d = reinterpret_cast<float4*>(wsm);
-        d[c] = make_float4(f2_lo(p[0]), f2_hi(p[0]), f2_lo(p[1]), f2_hi(p[1]));
-        d[NV + c] = make_float4(f2_lo(p[2]), f2_hi(p[2]), f2_lo(p[3]), f2_hi(p[3]));
-      }
-      named_bar_sync(14, ncons);
+  if constexpr (kWSmem) {
+    for (int c = tid; c < NV; c += ncons) {
+      f2 p[4];
+      load_w8_pairs<kFp32W>(a.w, c, p);
+      // two planes of float4 (columns 0-3 and 4-7 of each vector), so that a warp's
+      // reads of one plane are contiguous and free of bank conflicts
+      float4* d = reinterpret_cast<float4*>(wsm);
+      d[c] = make_float4(f2_lo(p[0]), f2_hi(p[0]), f2_lo(p[1]), f2_hi(p[1]));
+      d[NV + c] = make_float4(f2_lo(p[2]), f2_hi(p[2]), f2_lo(p[3]), f2_hi(p[3]));
     }
+    named_bar_sync(14, ncons);
   }
   // this thread's weight pairs for column vector c (its v-th)
   auto wvec = [&](int v, int c, f2 (&p)[4]) {
@@ -375,142 +359,103 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
   };
 
-  if (consumer) {
-    if constexpr (kND) {
-      // Stages in the order the producer filled them; a negative chunk start (or an
-      // abort) ends the loop, warp-uniformly (every lane reads the same start).
-      RowSums carry{0.f, 0.f};
-      int32_t ra_prev = 0;
-      for (int32_t j = 0;; ++j) {
+  if constexpr (kND) {
+    // Stages in the order the producer filled them; a negative chunk start (or an
+    // abort) ends the loop, warp-uniformly (every lane reads the same start).
+    RowSums carry{0.f, 0.f};
+    int32_t ra_prev = 0;
+    for (int32_t j = 0;; ++j) {
+      const int s = j % S;
+      const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u,
+                                        abort_flag, a.err, kErrConsumerWait);
+      const int32_t ra = ok ? srow[s] : -1;
+      const bool stop = __any_sync(0xffffffffu, ra < 0);
+      RowSums cur{0.f, 0.f};
+      if (!stop) cur = phase_a(j, s, ra + g < a.R);
+      if (j >= 1) phase_b(j - 1, (j - 1) % S, ra_prev, a.R, carry);
+      if (stop) break;
+      ra_prev = ra;
+      carry = cur;
+    }
+  } else {
+    // Rows of this warp's first group: every lane of a warp runs the same iterations
+    // (the shuffles need them all); groups past the chunk's end skip the row work.
+    const int g0 = red_smem ? g : (tid & ~31) / NTg;
+    const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
+    RowSums carry{0.f, 0.f};  // sub-warp groups: row j-1's sums
+    for (int32_t j = 0; j <= ng; ++j) {
+      RowSums cur{0.f, 0.f};
+      if (j < ng) {
         const int s = j % S;
-        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u,
-                                          abort_flag, a.err, kErrConsumerWait);
-        const int32_t ra = ok ? srow[s] : -1;
-        const bool stop = __any_sync(0xffffffffu, ra < 0);
-        RowSums cur{0.f, 0.f};
-        if (!stop) cur = phase_a(j, s, ra + g < a.R);
-        if (j >= 1) phase_b(j - 1, (j - 1) % S, ra_prev, a.R, carry);
-        if (stop) break;
-        ra_prev = ra;
-        carry = cur;
+        mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
+                          kErrConsumerWait);
+        cur = phase_a(j, s, r0 + j * G + g < r1);
       }
-    } else {
-      // Rows of this warp's first group: every lane of a warp runs the same iterations
-      // (the shuffles need them all); groups past the chunk's end skip the row work.
-      const int g0 = red_smem ? g : (tid & ~31) / NTg;
-      const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
-      RowSums carry{0.f, 0.f};  // sub-warp groups: row j-1's sums
-      for (int32_t j = 0; j <= ng; ++j) {
-        RowSums cur{0.f, 0.f};
-        if (j < ng) {
-          const int s = j % S;
-          mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                            kErrConsumerWait);
-          cur = phase_a(j, s, r0 + j * G + g < r1);
-        }
-        if (j >= 1) phase_b(j - 1, (j - 1) % S, r0 + (j - 1) * G, r1, carry);
-        carry = cur;
-      }
+      if (j >= 1) phase_b(j - 1, (j - 1) % S, r0 + (j - 1) * G, r1, carry);
+      carry = cur;
     }
   }
 
   // ---- this CTA's dw partial: (hi, lo) with hi + lo == acc + cmp exactly ----
-  // Deterministic builds store it to a.part[k]; non-deterministic ones add hi and lo into
-  // the FP64 sums a.acc.
-  auto emit = [&](int col, float hi, float lo) {
-    if constexpr (kND) {
-      atomicAdd(a.acc + col, static_cast<double>(hi));
-      atomicAdd(a.acc + col, static_cast<double>(lo));
-    } else {
-      float* part = a.part + static_cast<size_t>(k) * 2 * H;
-      part[col] = hi;
-      part[H + col] = lo;
+  float* part = a.part + static_cast<size_t>(k) * 2 * H;
+  if (G == 1) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        f2 hi[4], lo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hi[q] = f2_add(acc[v][q], cmp[v][q]);
+          lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
+        }
+        ulonglong2* ph = reinterpret_cast<ulonglong2*>(part + c * 8);
+        ulonglong2* pl = reinterpret_cast<ulonglong2*>(part + H + c * 8);
+        ph[0] = make_ulonglong2(hi[0].v, hi[1].v);
+        ph[1] = make_ulonglong2(hi[2].v, hi[3].v);
+        pl[0] = make_ulonglong2(lo[0].v, lo[1].v);
+        pl[1] = make_ulonglong2(lo[2].v, lo[3].v);
+      }
     }
-  };
-  if (consumer) {
-    if (G == 1) {
+    return;
+  }
+  // several row groups: combine them through shared memory in group order.  The ring is
+  // free once every consumer is past its loop: each stage was waited on (full) by every
+  // group that had a row in it before that group finished.
+  named_bar_sync(15, ncons);
+  // cb: [G][2][H] (hi, lo), each H-slab stored as two planes of float4 (columns 0-3 and
+  // 4-7 of every vector) so that a warp's stores of one plane are contiguous
+  float* cb = reinterpret_cast<float*>(smem);
 #pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = lt + v * NTg;
-        if (c < NV) {
-          f2 hi[4], lo[4];
+  for (int v = 0; v < VPT; ++v) {
+    const int c = lt + v * NTg;
+    if (c < NV) {
+      f2 hi[4], lo[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            hi[q] = f2_add(acc[v][q], cmp[v][q]);
-            lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
-          }
-          if constexpr (kND) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              emit(c * 8 + 2 * q, f2_lo(hi[q]), f2_lo(lo[q]));
-              emit(c * 8 + 2 * q + 1, f2_hi(hi[q]), f2_hi(lo[q]));
-            }
-          } else {
-            float* part = a.part + static_cast<size_t>(k) * 2 * H;
-            ulonglong2* ph = reinterpret_cast<ulonglong2*>(part + c * 8);
-            ulonglong2* pl = reinterpret_cast<ulonglong2*>(part + H + c * 8);
-            ph[0] = make_ulonglong2(hi[0].v, hi[1].v);
-            ph[1] = make_ulonglong2(hi[2].v, hi[3].v);
-            pl[0] = make_ulonglong2(lo[0].v, lo[1].v);
-            pl[1] = make_ulonglong2(lo[2].v, lo[3].v);
-          }
-        }
+      for (int q = 0; q < 4; ++q) {
+        hi[q] = f2_add(acc[v][q], cmp[v][q]);
+        lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
       }
-    } else {
-      // several row groups: combine them through shared memory in group order.  The ring
-      // is free once every consumer is past its loop: each stage was waited on (full) by
-      // every group that had a row in it before that group finished.
-      named_bar_sync(15, ncons);
-      // cb: [G][2][H] (hi, lo), each H-slab stored as two planes of float4 (columns 0-3
-      // and 4-7 of every vector) so that a warp's stores of one plane are contiguous
-      float* cb = reinterpret_cast<float*>(smem);
-#pragma unroll
-      for (int v = 0; v < VPT; ++v) {
-        const int c = lt + v * NTg;
-        if (c < NV) {
-          f2 hi[4], lo[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            hi[q] = f2_add(acc[v][q], cmp[v][q]);
-            lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
-          }
-          ulonglong2* ph = reinterpret_cast<ulonglong2*>(cb + (2 * g) * H);
-          ulonglong2* pl = reinterpret_cast<ulonglong2*>(cb + (2 * g + 1) * H);
-          ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
-          ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
-          pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
-          pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
-        }
-      }
-      named_bar_sync(15, ncons);
-      for (int col = tid; col < H; col += ncons) {
-        const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
-        float sacc = 0.f, e = 0.f;
-        for (int gi = 0; gi < G; ++gi) {
-          float err;
-          sacc = two_sum(sacc, cb[(2 * gi) * H + at], err);
-          e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + at]));
-        }
-        const float hi = __fadd_rn(sacc, e);
-        emit(col, hi, __fsub_rn(e, __fsub_rn(hi, sacc)));
-      }
+      ulonglong2* ph = reinterpret_cast<ulonglong2*>(cb + (2 * g) * H);
+      ulonglong2* pl = reinterpret_cast<ulonglong2*>(cb + (2 * g + 1) * H);
+      ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
+      ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
+      pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
+      pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
     }
   }
-  if constexpr (kND) {
-    // Every CTA, producer included, takes a ticket once its additions are visible
-    // (fence, then the CTA barrier); the CTA with the last ticket rounds the sums.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      *last_flag = atomicAdd(a.ctl + 1, 1u) == static_cast<uint32_t>(gridDim.x - 1) ? 1 : 0;
+  named_bar_sync(15, ncons);
+  for (int col = tid; col < H; col += ncons) {
+    const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
+    float sacc = 0.f, e = 0.f;
+    for (int gi = 0; gi < G; ++gi) {
+      float err;
+      sacc = two_sum(sacc, cb[(2 * gi) * H + at], err);
+      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + at]));
     }
-    __syncthreads();
-    if (*last_flag) {
-      __threadfence();
-      for (int col = tid; col < H; col += blockDim.x)
-        a.dw[col] = static_cast<float>(ld_cg_f64(a.acc + col));
-    }
+    const float hi = __fadd_rn(sacc, e);
+    part[col] = hi;
+    part[H + col] = __fsub_rn(e, __fsub_rn(hi, sacc));
   }
 }
 

@@ -21,8 +21,14 @@ namespace rmsn {
 // Device-side error bits (see rmsnorm_train_device_error in the public header).
 enum : unsigned { kErrConsumerWait = 1u, kErrProducerWait = 2u };
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
+// A bounded wait gives up after this many nanoseconds of %globaltimer spent waiting.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// Waiting time is summed poll by poll; a step between two polls that goes backwards or
+// is longer than this is the timer being set (or the context being off the GPU), not
+// time spent waiting, and is not counted.  Without this, one backward step of the timer
+// would read as a wait of ~2^64 ns and abort a healthy kernel.
+constexpr unsigned long long kWaitStepMaxNs = 1000000ull;  // 1 ms
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -32,6 +38,17 @@ __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Adds the time since the previous poll (`prev`, then updated) to `waited`, skipping
+// steps the timer took outside the wait; true once `waited` passes the limit.
+__device__ __forceinline__ bool wait_expired(unsigned long long& prev,
+                                             unsigned long long& waited) {
+  const unsigned long long now = global_ns();
+  const unsigned long long step = now - prev;  // huge if the timer stepped back
+  prev = now;
+  if (step <= kWaitStepMaxNs) waited += step;
+  return waited > kWaitLimitNs;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -73,11 +90,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   volatile int* abort_flag,
                                                   unsigned* err_word, unsigned errbit) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  unsigned long long prev = global_ns(), waited = 0;
   for (;;) {
     if (*abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (wait_expired(prev, waited)) {
       atomicOr(err_word, errbit);
       *abort_flag = 1;
       return false;
@@ -90,11 +107,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // this CTA's shared memory once it exits -- also after an abort, whose flag it ignores.
 // Bounded by one kWaitLimitNs for the whole drain.
 __device__ __forceinline__ void mbar_drain(uint64_t* full, int S, int32_t issued) {
-  const unsigned long long t0 = global_ns();
+  unsigned long long prev = global_ns(), waited = 0;
   for (int32_t j = issued > S ? issued - S : 0; j < issued; ++j) {
     const uint32_t parity = static_cast<uint32_t>(j / S) & 1u;
     while (!mbar_try_wait(&full[j % S], parity))
-      if (global_ns() - t0 > kWaitLimitNs) return;
+      if (wait_expired(prev, waited)) return;
   }
 }
 

@@ -111,11 +111,8 @@ struct BwdArgs {
   const void* w;
   __nv_bfloat16* dx;          // contiguous
   float* part;                // [P][2][H]: compensated dw partial per CTA (hi row, lo row)
-  // one-launch non-deterministic build: ctl[0] next row to hand out, ctl[1] CTAs done;
-  // acc[H] FP64 sums of the CTAs' partials; dw written by the last CTA to finish
+  // non-deterministic builds: ctl[0] is the next row to hand out (zeroed before the launch)
   unsigned* ctl;
-  double* acc;
-  float* dw;
   // rstd == nullptr: the row pass recomputes rstd (eps as in the forward) and writes it to
   // rstd_out when that is not null
   float eps;
@@ -147,14 +144,11 @@ const void* bwd_rows_fn_nd_rc(const Shape& s, bool fp32w, bool dh);
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
 
-// Non-deterministic backward in one row-pass launch (rmsn_bwd_nd.cu): CTAs take chunks of
-// rows from a counter as they go, and each adds its dw partial into FP64 sums that the
-// last CTA to finish rounds into dw.  Its workspace is the control words and the sums,
-// zeroed on the stream by a one-CTA kernel launched just before the row pass.
+// Non-deterministic backward (rmsn_bwd_nd.cu): CTAs take chunks of rows from a counter as
+// they go.  Its workspace is that counter (16 bytes, zeroed on the stream by a one-CTA
+// kernel launched just before the row pass) followed by the P partials; the fixed-order
+// finish adds them.
 constexpr size_t kNdCtlBytes = 16;
-__host__ __device__ constexpr size_t nd_workspace_bytes(int H) {
-  return kNdCtlBytes + sizeof(double) * static_cast<size_t>(H);
-}
 Shape nd_shape(const Shape& s, int H);  // + the chunk-start slots in shared memory
 int bwd_nd_blocks_per_sm(const Shape& s, bool fp32w, bool rc);
 cudaError_t launch_bwd_nd(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);

@@ -3,7 +3,9 @@
     y, rstd        = rmsnorm_fwd(x, w, eps)                  # x [T, H] or a [T, nh, H] view
     y, rstd, h     = rmsnorm_fwd(x_in, w, eps, residual=res) # fused residual add
     dx, dw         = rmsnorm_bwd(dy, x_or_h, rstd, w, deterministic=True, dh=None)
+    dx, dw, rstd   = rmsnorm_bwd_recompute(dy, x_or_h, w, eps, deterministic=True, dh=None)
     y              = rmsnorm_train(x, w, eps, deterministic=True)   # autograd
+    y              = rmsnorm_train(x, w, eps, recompute_rstd=True)  # saves x only
     y, h           = rmsnorm_train(x_in, w, eps, residual=res)      # autograd, residual form
 
 Inputs: BF16 CUDA activations whose last dimension is contiguous (a [T, nh, H] view may
@@ -76,37 +78,67 @@ def rmsnorm_bwd(dy, x, rstd, w, deterministic=True, dh=None):
     return dx, dw
 
 
+def rmsnorm_bwd_recompute(dy, x, w, eps=EPS, deterministic=True, dh=None):
+    """The backward for a step that kept x but not rstd: rstd is recomputed from x inside
+    the backward (and returned)."""
+    T, nh, H, s_tok, s_head = _view(x)
+    dy = dy.contiguous()
+    if dh is not None:
+        dh = dh.contiguous()
+    w = w.contiguous()
+    dx = torch.empty(dy.shape, dtype=torch.bfloat16, device=dy.device)
+    dw = torch.empty(H, dtype=torch.float32, device=dy.device)
+    rstd = torch.empty(dy.shape[:-1], dtype=torch.float32, device=dy.device)
+    nbytes = N.rmsnorm_train_bwd_workspace_bytes(T, nh, H, deterministic)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dy.device)
+    N.rmsnorm_train_bwd_recompute(x, dy, dh, w, _wdtype(w), dx, dw, rstd, ws, nbytes, T, nh, H,
+                                  s_tok, s_head, float(eps), deterministic)
+    return dx, dw, rstd
+
+
 class RMSNormTrain(torch.autograd.Function):
-    """Autograd wrapper: forward saves x (or h) and rstd; backward runs the CUDA backward."""
+    """Autograd wrapper: forward saves x (or h) and rstd -- or, with recompute_rstd, x (or
+    h) alone, and the backward recomputes rstd; backward runs the CUDA backward."""
 
     @staticmethod
-    def forward(ctx, x, w, eps, residual, deterministic):
+    def forward(ctx, x, w, eps, residual, deterministic, recompute_rstd):
+        ctx.residual = residual is not None
+        ctx.deterministic = deterministic
+        ctx.recompute = recompute_rstd
+        ctx.eps = eps
         if residual is None:
             y, rstd = rmsnorm_fwd(x, w, eps)
-            ctx.save_for_backward(x, rstd, w)
-            ctx.residual = False
-            ctx.deterministic = deterministic
-            return y
-        y, rstd, h = rmsnorm_fwd(x, w, eps, residual=residual)
-        ctx.save_for_backward(h, rstd, w)
-        ctx.residual = True
-        ctx.deterministic = deterministic
-        return y, h
+            xs = x
+        else:
+            y, rstd, xs = rmsnorm_fwd(x, w, eps, residual=residual)
+        if recompute_rstd:
+            ctx.save_for_backward(xs, w)
+        else:
+            ctx.save_for_backward(xs, rstd, w)
+        return y if residual is None else (y, xs)
 
     @staticmethod
     def backward(ctx, *grads):
-        xs, rstd, w = ctx.saved_tensors
+        if ctx.recompute:
+            xs, w = ctx.saved_tensors
+            rstd = None
+        else:
+            xs, rstd, w = ctx.saved_tensors
         dy = grads[0]
         dh = grads[1] if ctx.residual else None
         if dy is None:
             dy = torch.zeros(xs.shape, dtype=torch.bfloat16, device=xs.device)
-        dx, dw = rmsnorm_bwd(dy.to(torch.bfloat16), xs, rstd, w, ctx.deterministic,
-                             dh=None if dh is None else dh.to(torch.bfloat16))
+        dy = dy.to(torch.bfloat16)
+        dh = None if dh is None else dh.to(torch.bfloat16)
+        if rstd is None:
+            dx, dw, _ = rmsnorm_bwd_recompute(dy, xs, w, ctx.eps, ctx.deterministic, dh=dh)
+        else:
+            dx, dw = rmsnorm_bwd(dy, xs, rstd, w, ctx.deterministic, dh=dh)
         dw = dw.to(w.dtype)
         if ctx.residual:
-            return dx, dw, None, dx, None
-        return dx, dw, None, None, None
+            return dx, dw, None, dx, None, None
+        return dx, dw, None, None, None, None
 
 
-def rmsnorm_train(x, w, eps=EPS, residual=None, deterministic=True):
-    return RMSNormTrain.apply(x, w, eps, residual, deterministic)
+def rmsnorm_train(x, w, eps=EPS, residual=None, deterministic=True, recompute_rstd=False):
+    return RMSNormTrain.apply(x, w, eps, residual, deterministic, recompute_rstd)

@@ -11,9 +11,6 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
-    config.addinivalue_line(
-        "markers", "gpu_pending: needs a CUDA GPU; parity tests of kernels not yet run on "
-        "one (select with -m gpu_pending; they join the gpu tests once they pass there)")
 
 
 def pytest_collection_modifyitems(config, items):
@@ -28,5 +25,5 @@ def pytest_collection_modifyitems(config, items):
         return
     skip = pytest.mark.skip(reason="no CUDA device")
     for item in items:
-        if "gpu" in item.keywords or "gpu_pending" in item.keywords:
+        if "gpu" in item.keywords:
             item.add_marker(skip)

@@ -213,15 +213,15 @@ def test_deterministic_workspace_covers_both_dh_plans(lib):
             assert lib.rmsnorm_train_bwd_workspace_bytes(T, 1, H, 1) == need, (H, T)
 
 
-def test_nondeterministic_workspace_is_control_words_and_fp64_sums(lib):
-    # the one-launch non-deterministic backward: 16 bytes of counters + H FP64 sums, for
-    # every row count past the one-launch small path; no device query needed
+def test_nondeterministic_workspace_is_row_counter_and_partials(lib):
+    # non-deterministic: a 16-byte row counter before the deterministic mode's partials;
+    # no device query needed
     f = lib.rmsnorm_train_bwd_workspace_bytes
     for H in (8, 256, 1536, 4096, 6144, 8192):
         assert f(256, 1, H, 0) == 0
         for T in (257, 4096, 131072):
-            assert f(T, 1, H, 0) == 16 + 8 * H, (H, T)
-    assert f(65536, 24, 256, 0) == 16 + 8 * 256
+            assert f(T, 1, H, 0) == 16 + f(T, 1, H, 1), (H, T)
+    assert f(65536, 24, 256, 0) == 16 + 152 * 2 * 256 * 4
     assert f(0, 1, 4096, 0) == 0
 
 
@@ -238,9 +238,9 @@ def test_nondeterministic_build_fits_shared_memory_at_every_width(lib, op):
 
 
 def test_noalloc_scratch_covers_every_supported_shape(lib):
-    # rmsnorm_train_bwd_noalloc keeps its workspace in a 16 MiB array: the deterministic
-    # partition is at most 152 x (CTAs an SM) partials of 2*H floats, the non-deterministic
-    # workspace 16 + 8*H bytes, so no supported shape reaches the limit
+    # rmsnorm_train_bwd_noalloc keeps its workspace in a 16 MiB array: the partition is at
+    # most 152 x (CTAs an SM) partials of 2*H floats (+ a 16-byte counter in the
+    # non-deterministic mode), so no supported shape reaches the limit
     f = lib.rmsnorm_train_bwd_workspace_bytes
     for H in range(8, 8193, 8):
         for det in (0, 1):

@@ -70,3 +70,20 @@ def test_recompute_rejects_missing_rstd_out():
         N.rmsnorm_train_bwd_recompute(dc.x, dc.dy, None, dc.w, N.RMSN_W_BF16, dx, dw, None,
                                       None, 0, c.T, 1, c.H, c.H, c.H, 1e-6, True)
     assert ei.value.status == 1
+
+
+def test_autograd_recompute_rstd_matches_direct_calls():
+    import rmsnorm_fwd_02_gb300 as R
+    c = synth.plain(300)
+    dc = parity.DeviceCase(c)
+    x = dc.x.view(c.T, c.H).clone().requires_grad_(True)
+    w = dc.w.clone().requires_grad_(True)
+    y = R.rmsnorm_train(x, w, c.eps, deterministic=True, recompute_rstd=True)
+    dy = dc.dy.view(c.T, c.H)
+    y.backward(dy)
+    dx0, dw0, rs0 = R.rmsnorm_bwd_recompute(dy, dc.x.view(c.T, c.H), dc.w, c.eps, True)
+    _, rstd = R.rmsnorm_fwd(dc.x.view(c.T, c.H), dc.w, c.eps)
+    assert torch.equal(x.grad, dx0)
+    assert torch.equal(w.grad, dw0.to(w.dtype))
+    rel = ((rs0 - rstd).abs() / rstd).max().item()
+    assert rel <= 2.0**-22, rel

@@ -18,7 +18,6 @@ The backward is fed FP32(mean64) and FP32(rstd64) -- the oracle's own forward st
 rounded -- and the oracle's backward uses the same values widened, so no oracle input
 comes from the CUDA path.
 
-Marked gpu_pending until these kernels have passed on a GPU.
 """
 from __future__ import annotations
 
@@ -32,7 +31,7 @@ from rmsnorm_fwd_02_gb300 import _native as N
 from rmsnorm_fwd_02_gb300 import synth as S
 from rmsnorm_fwd_02_gb300.layernorm import layernorm_bwd, layernorm_fwd, layernorm_train
 
-pytestmark = pytest.mark.gpu_pending
+pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 
