@@ -793,6 +793,25 @@ def time_cell(env, cell, reps, ckpt=False, once=False, only=None):
                     bwd(i)
 
                 ops.append(("2xfwd+bwd_det", step, 2 * fwd_b + bwd_b))
+
+                # the backward that recomputes rstd (writing it to the set's rstd), and the
+                # checkpointed step with it in place of the second forward
+                def bwd_rc(i, ws=ws, nws=nws):
+                    q = sets[i]
+                    xs = q["h"] if res else q["x"]
+                    st = lib.rmsnorm_train_bwd_recompute(xs.data_ptr(), q["dy"].data_ptr(), None,
+                                                         w.data_ptr(), wd, q["dx"].data_ptr(),
+                                                         q["dw"].data_ptr(), q["rstd"].data_ptr(),
+                                                         ws.data_ptr(), nws, T, nh, H, s_tok,
+                                                         s_head, 1e-6, 1, cur["sh"])
+                    assert st == 0, st
+
+                def step_rc(i, bwd_rc=bwd_rc):
+                    fwd(i)
+                    bwd_rc(i)
+
+                ops.append(("bwd_det_rc", bwd_rc, bwd_b))
+                ops.append(("fwd+bwd_det_rc", step_rc, fwd_b + bwd_b))
     timed, timed_stream, timed_graph = _cell_timers(torch, stream, flush)
     out = []
     if only:
@@ -1015,7 +1034,8 @@ def main(argv=None):
                          "(filter entries as layernorm_M_H)")
     ap.add_argument("--sweep-ops", default="",
                     help="with --sweep: only these ops (comma-separated: fwd, bwd_det, "
-                         "bwd_nondet, bwd_det+dh, bwd_nondet+dh, 2xfwd+bwd_det, ...)")
+                         "bwd_nondet, bwd_det+dh, bwd_nondet+dh, 2xfwd+bwd_det, bwd_det_rc, "
+                         "fwd+bwd_det_rc)")
     ap.add_argument("--sweep-once", action="store_true",
                     help="with --sweep: run each op of each selected workload once, untimed "
                          "(one launch of each kernel, for a profiler)")

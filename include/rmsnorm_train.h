@@ -14,10 +14,11 @@
  * Two backward modes share one forward: deterministic != 0 gives bit-identical dw run to
  * run and across GPUs of any SM count (the row -> partial mapping depends on T, nh, H and
  * whether dh is given, never on the GPU; a second kernel adds the partials in a fixed
- * order); deterministic == 0 hands rows to the CTAs as they free up (no CTA idles while
- * another still has a queue of rows), so each CTA's dw partial covers rows that vary from
- * run to run and dw may differ between runs in its last bits (both modes keep dw within
- * the same budget).  dx is the same in both modes, bit for bit.
+ * order); deterministic == 0 gives each CTA a fixed prefix of rows and hands the last
+ * rows out to the CTAs as they free up (no CTA idles while another still has a queue of
+ * rows), so a CTA's dw partial covers rows that vary from run to run and dw may differ
+ * between runs in its last bits (both modes keep dw within the same budget).  dx is the
+ * same in both modes, bit for bit.
  *
  * Rows and views (same PR, description: per-head views [T,24,256] strided and [T,4,256]
  * contiguous with a shared w[256]).  A normalized row is a pair (token t, head h),
@@ -86,8 +87,8 @@ int rmsnorm_train_fwd(const void* x, const void* residual, const void* w, int w_
  * T*nh <= 256 rows (done in one launch without a workspace) and for T*nh == 0.  Above
  * that, P partials of 2*H floats (P <= 152 per CTA an SM the launch shape keeps
  * resident, a function of (T, nh, H) only), and for deterministic == 0 a 16-byte row
- * counter before them.  Returns 0 on invalid sizes.  Host-only computation: no device
- * access.
+ * counter slot before them.  Returns 0 on invalid sizes.  Host-only computation: no
+ * device access.
  */
 size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int deterministic);
 
@@ -108,9 +109,9 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
  *   dw         FP32 [H] out, overwritten (not accumulated); zero-filled when T*nh == 0
  *   workspace  device scratch of >= rmsnorm_train_bwd_workspace_bytes(...) bytes,
  *              16-byte aligned, no initial contents required (the non-deterministic
- *              mode zeroes its row counter on the stream first); clobbered by the call
- *              (may be NULL when that size is 0).  Two calls that may overlap on the GPU
- *              need separate workspaces.
+ *              mode's row counter is opened by each call, under a per-call tag); clobbered
+ *              by the call (may be NULL when that size is 0).  Two calls that may overlap
+ *              on the GPU need separate workspaces.
  *   deterministic  0 or 1 (see the top of this file)
  */
 int rmsnorm_train_bwd(const void* x, const void* dy, const void* dh, const float* rstd,

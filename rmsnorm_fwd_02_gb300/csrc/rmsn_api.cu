@@ -1,6 +1,7 @@
 // rmsn_api.cu -- the C ABI (include/rmsnorm_train.h): argument checks, launch planning,
 // and kernel launches.  Never allocates, frees or synchronizes (except the diagnostic
 // rmsnorm_train_device_error); every launch goes on the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -129,6 +130,17 @@ int device_setup(int dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tag of a non-deterministic backward call: nonzero, and different from the last 2^32 - 2
+// calls' (the row counter it marks is cleared by each call's finish).
+std::atomic<uint32_t> g_call_tag{0};
+uint32_t next_call_tag() {
+  uint32_t t;
+  do {
+    t = g_call_tag.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  } while (t == 0u);
+  return t;
+}
+
 // Checks shared by both directions; view strides apply to the strided input only.
 int check_view(int64_t T, int32_t nh, int32_t H, int64_t s_tok, int64_t s_head, int w_dtype) {
   if (T < 0 || nh < 1) return RMSN_ERR_INVALID_ARG;
@@ -245,7 +257,7 @@ Shape bwd_shape(int H, bool with_dh) {
 Shape nd_shape(const Shape& s, int H) {
   Shape n = s;
   n.smem = smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0, s.groups,
-                       bwd_w_in_smem(s.cls, s.vpt) ? H : 0, s.stages)
+                       bwd_w_in_smem(s.cls, s.vpt) ? H : 0, 2 * s.stages)
                .total;
   return n;
 }
@@ -373,7 +385,8 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     a.w = w;
     a.dx = static_cast<__nv_bfloat16*>(dx);
     a.part = part;
-    a.ctl = static_cast<unsigned*>(workspace);
+    a.ctl = deterministic ? nullptr : static_cast<unsigned*>(workspace);
+    a.tag = next_call_tag();
     a.map = RowMapArgs{nh, H, s_tok, nh > 1 ? s_head : 0};
     a.R = static_cast<int32_t>(R);
     a.contig = is_contig(nh, H, s_tok, s_head) ? 1 : 0;
@@ -386,7 +399,8 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
                                         : launch_bwd_nd(a, sl, fp32w, stream_);
     if (e != cudaSuccess) return RMSN_ERR_CUDA;
   }
-  if (launch_dw_finish(part, dw, P, H, stream_) != cudaSuccess)
+  unsigned* ctl = (deterministic || R == 0) ? nullptr : static_cast<unsigned*>(workspace);
+  if (launch_dw_finish(part, dw, P, H, ctl, stream_) != cudaSuccess)
     return RMSN_ERR_CUDA;
   return RMSN_OK;
 }

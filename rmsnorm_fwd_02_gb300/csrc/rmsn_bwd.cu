@@ -11,11 +11,15 @@ namespace rmsn {
 // halving).  TwoSum carries the error terms throughout.  Each thread walks only ~P/32
 // partials with four loads in flight, so the kernel is a short tail.
 __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
-    rmsn_dw_finish_kernel(const float* __restrict__ part, float* __restrict__ dw, int P, int H) {
+    rmsn_dw_finish_kernel(const float* __restrict__ part, float* __restrict__ dw, int P, int H,
+                          unsigned* ctl) {
   __shared__ float sh[kFinishSlices][kFinishCols];
   __shared__ float se[kFinishSlices][kFinishCols];
   pdl_wait_prior_grid();
   pdl_allow_next_grid();
+  // the row pass that used the non-deterministic pool is complete: clear its words, so
+  // that a replay of this call (same tag) finds the pool closed until its CTA 0 opens it
+  if (ctl != nullptr && blockIdx.x == 0 && threadIdx.x < 2) ctl[threadIdx.x] = 0u;
   const int cl = threadIdx.x % kFinishCols;
   const int sl = threadIdx.x / kFinishCols;
   const int col = blockIdx.x * kFinishCols + cl;
@@ -85,9 +89,10 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaSt
                     s.smem, st, args);
 }
 
-cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st) {
+cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, unsigned* ctl,
+                             cudaStream_t st) {
   const void* fn = reinterpret_cast<const void*>(&rmsn_dw_finish_kernel);
-  void* args[] = {&part, &dw, &P, &H};
+  void* args[] = {&part, &dw, &P, &H, &ctl};
   const unsigned grid = static_cast<unsigned>((H + kFinishCols - 1) / kFinishCols);
   return launch_pdl(fn, dim3(grid), dim3(kFinishCols * kFinishSlices), 0, st, args);
 }

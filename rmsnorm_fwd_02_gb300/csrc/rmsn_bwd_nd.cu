@@ -1,7 +1,7 @@
 // rmsn_bwd_nd.cu -- RMSNorm training backward for sm_103a, non-deterministic builds: the
 // row pass of rmsn_bwd_rows.cuh with kND = true, whose CTAs take chunks of rows from an
-// atomic counter as they go, preceded by a one-CTA kernel that zeroes that counter, and
-// followed by the fixed-order dw finish.
+// atomic counter as they go, followed by the fixed-order dw finish (which also clears the
+// counter).
 //
 // flashinfer PR #8827 (description) leaves deterministic=False free to be faster.  What the
 // mode buys here is the partition: with rows handed out as CTAs free up, no CTA idles
@@ -11,15 +11,6 @@
 #include "rmsn_bwd_rows.cuh"
 
 namespace rmsn {
-
-// Zeroes the row counter of one call.  It lets the row pass be scheduled at once (that
-// grid still waits for this one to finish before it touches the workspace), and waits for
-// the previous grid on the stream, which may be an earlier call still using the counter.
-__global__ void __launch_bounds__(32) rmsn_nd_prep_kernel(unsigned* ctl) {
-  pdl_allow_next_grid();
-  pdl_wait_prior_grid();
-  if (threadIdx.x < kNdCtlBytes / sizeof(unsigned)) ctl[threadIdx.x] = 0u;
-}
 
 const void* bwd_rows_fn_nd(const Shape& s, bool fp32w, bool dh) {
   return pick_rows_kernel<true, false>(s, fp32w, dh);
@@ -37,11 +28,6 @@ int bwd_nd_blocks_per_sm(const Shape& s, bool fp32w, bool rc) {
 cudaError_t launch_bwd_nd(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st) {
   const void* fn = bwd_rows_fn(s, fp32w, a.dh != nullptr, true, a.rstd == nullptr);
   cudaError_t e = prepare_kernel(fn, s.smem);
-  if (e != cudaSuccess) return e;
-  unsigned* ctl = a.ctl;
-  void* pargs[] = {&ctl};
-  e = launch_pdl(reinterpret_cast<const void*>(&rmsn_nd_prep_kernel), dim3(1), dim3(32), 0, st,
-                 pargs);
   if (e != cudaSuccess) return e;
   BwdArgs copy = a;
   void* args[] = {&copy};

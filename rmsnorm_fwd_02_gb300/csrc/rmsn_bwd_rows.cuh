@@ -43,6 +43,22 @@ __device__ __forceinline__ float two_sum(float a, float b, float& err) {
   return s;
 }
 
+// The non-deterministic row counter's two words: ctl[0] the tag of the call that opened
+// the pool of tail rows (a nonzero per-call number), ctl[1] the next tail row.
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// First row of CTA k's chunk in the deterministic partition of R rows over P CTAs.
+__device__ __forceinline__ int32_t r0_det(int32_t k, int32_t R, int32_t P) {
+  return static_cast<int32_t>((static_cast<int64_t>(k) * R) / P);
+}
+
 // A row's two reduced sums: (dy*w)*x, and x^2 (builds that recompute rstd).
 struct RowSums {
   float dot, ss;
@@ -56,10 +72,15 @@ struct RowSums {
 // sum_j (dy_j*w_j)*x_j (both through the one reduction) and phase B recomputes
 // rstd = 1/sqrt(sum x^2 / H + eps) as the forward does, writing it to a.rstd_out if given.
 // kND = false: CTA k owns rows [k*R/P, (k+1)*R/P).
-// kND = true: the producer takes chunks of G rows (one ring stage) from the counter
-// a.ctl[0] as slots free up, one chunk ahead, and passes each chunk's first row to the
-// consumers through shared memory; a chunk start at or past R ends the CTA's work.  A CTA
-// that frees up early takes more rows, so no CTA idles while another still holds a queue.
+// kND = true: CTA k owns a fixed prefix of Ns stages, rows [k*Ns*G, (k+1)*Ns*G), and the
+// last ~2 stages' worth of rows a CTA would own, rows [P*Ns*G, R), form a pool handed out
+// G rows at a time by the counter a.ctl[1]: a CTA that is done with its prefix early takes
+// more of the tail, so none idles while another still holds a queue.  CTA 0 opens the
+// pool (sets the counter, then publishes the call's tag in a.ctl[0]) before its own rows;
+// a CTA that reaches the pool before it is open takes nothing from it, and CTA 0 itself
+// always drains it, so no CTA ever waits on another.  (Below 4 stages a CTA the prefix
+// is the deterministic chunk and the pool is empty.)  The producer passes each stage's
+// first row to the consumers through shared memory; a negative start ends the CTA's work.
 // Either way CTA k writes its dw partial to a.part[k].
 template <int VPT, int kCls, bool kFp32W, bool kDh, bool kND, bool kRc>
 __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_per_sm(kCls))
@@ -74,7 +95,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
   constexpr bool kWSmem = bwd_w_in_smem(kCls, VPT);
   const SmemLayout L =
-      smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0, kND ? S : 0);
+      smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0, kND ? 2 * S : 0);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -84,15 +105,16 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   float* rs_ring = reinterpret_cast<float*>(smem + L.rs);        // [S][RSP] staged rstd
   const int RSP = rs_stride(G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
-  volatile int32_t* srow = reinterpret_cast<volatile int32_t*>(smem + L.srow);  // [S]
+  // [S][2]: each staged chunk's rows [start, end)
+  volatile int32_t* srow = reinterpret_cast<volatile int32_t*>(smem + L.srow);
 
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
   const int32_t k = blockIdx.x;
   int32_t r0 = 0, r1 = 0, nstage = 0;
   if constexpr (!kND) {
-    r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
-    r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
+    r0 = r0_det(k, a.R, a.P);
+    r1 = r0_det(k + 1, a.R, a.P);
     nstage = (r1 - r0 + G - 1) / G;
   }
 
@@ -144,25 +166,54 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       int32_t j = 0;  // stages whose full barrier has been armed
       if constexpr (kND) {
         const uint32_t R = static_cast<uint32_t>(a.R);
-        uint32_t next = atomicAdd(a.ctl, static_cast<uint32_t>(G));
+        const uint32_t per = static_cast<uint32_t>(a.P) * static_cast<uint32_t>(G);
+        const uint32_t nfull = R / per;          // whole stages every CTA could own
+        uint32_t pa, pb, pool;                   // this CTA's prefix [pa, pb), pool start
+        if (nfull >= 4) {
+          const uint32_t Ns = nfull - 2;
+          pa = static_cast<uint32_t>(k) * Ns * G;
+          pb = pa + Ns * G;
+          pool = per * Ns;
+        } else {
+          pa = static_cast<uint32_t>(r0_det(k, a.R, a.P));
+          pb = static_cast<uint32_t>(r0_det(k + 1, a.R, a.P));
+          pool = R;
+        }
+        if (k == 0 && pool < R) {  // open the pool: the counter first, then the tag
+          a.ctl[1] = pool;
+          __threadfence();
+          st_release_u32(a.ctl, a.tag);
+        }
+        bool tail = false;
+        uint32_t next = pa;
+        uint32_t first_tail = R;  // the first pool chunk, taken while the prefix's last
+                                  // stage is issued (so its round trip is hidden too)
         for (;; ++j) {
           const int s = j % S;
           if (j >= S &&
               !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
                                  a.err, kErrProducerWait))
             break;
+          if (!tail && next >= pb) {  // prefix done: on to the pool
+            tail = true;
+            next = first_tail;
+          }
           const uint32_t ra = next;
           if (ra >= R) {  // no rows left: an empty stage tells the consumers to stop
-            srow[s] = -1;
+            srow[2 * s] = -1;
             mbar_arrive(&full[s]);
             ++j;
             break;
           }
-          // the next chunk is taken now, so the atomic's round trip overlaps the wait
+          // the next tail chunk is taken now, so the atomic's round trip overlaps the wait
           // for the next free slot
-          next = atomicAdd(a.ctl, static_cast<uint32_t>(G));
-          srow[s] = static_cast<int32_t>(ra);  // published by the arrival in issue()
-          issue(s, static_cast<int32_t>(ra), static_cast<int32_t>(min(ra + G, R)));
+          const uint32_t rb = tail ? min(ra + G, R) : min(ra + G, pb);
+          if (!tail && rb >= pb && pool < R && ld_acquire_u32(a.ctl) == a.tag)
+            first_tail = atomicAdd(a.ctl + 1, G);  // the pool is open: reserve a chunk
+          next = tail ? atomicAdd(a.ctl + 1, G) : rb;
+          srow[2 * s] = static_cast<int32_t>(ra);  // published by the arrival in issue()
+          srow[2 * s + 1] = static_cast<int32_t>(rb);
+          issue(s, static_cast<int32_t>(ra), static_cast<int32_t>(rb));
         }
       } else {
         for (; j < nstage; ++j) {
@@ -363,18 +414,20 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     // Stages in the order the producer filled them; a negative chunk start (or an
     // abort) ends the loop, warp-uniformly (every lane reads the same start).
     RowSums carry{0.f, 0.f};
-    int32_t ra_prev = 0;
+    int32_t ra_prev = 0, rb_prev = 0;
     for (int32_t j = 0;; ++j) {
       const int s = j % S;
       const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u,
                                         abort_flag, a.err, kErrConsumerWait);
-      const int32_t ra = ok ? srow[s] : -1;
+      const int32_t ra = ok ? srow[2 * s] : -1;
+      const int32_t rb = ok ? srow[2 * s + 1] : -1;
       const bool stop = __any_sync(0xffffffffu, ra < 0);
       RowSums cur{0.f, 0.f};
-      if (!stop) cur = phase_a(j, s, ra + g < a.R);
-      if (j >= 1) phase_b(j - 1, (j - 1) % S, ra_prev, a.R, carry);
+      if (!stop) cur = phase_a(j, s, ra + g < rb);
+      if (j >= 1) phase_b(j - 1, (j - 1) % S, ra_prev, rb_prev, carry);
       if (stop) break;
       ra_prev = ra;
+      rb_prev = rb;
       carry = cur;
     }
   } else {

@@ -24,8 +24,8 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 //   w      [w_floats] FP32 weight, for builds that keep it in shared memory
 //   abort  CTA abort flag of the bounded waits (word 0); word 1: the backward's
 //          last-CTA flag (one-launch non-deterministic build)
-//   srow   [srow_stages] first row of each staged chunk (builds whose producer takes
-//          chunks dynamically; others: none)
+//   srow   [srow_stages] int32: the first and end row of each staged chunk (builds
+//          whose producer decides its chunks as it goes: 2 per stage; others: none)
 //
 // Row j's reduction uses buffer j % kRedBufs.  A warp writes buffer j in phase A(j) after
 // finishing B(j-2), which needed every warp's A(j-2), which each warp issues after its
@@ -111,8 +111,11 @@ struct BwdArgs {
   const void* w;
   __nv_bfloat16* dx;          // contiguous
   float* part;                // [P][2][H]: compensated dw partial per CTA (hi row, lo row)
-  // non-deterministic builds: ctl[0] is the next row to hand out (zeroed before the launch)
+  // non-deterministic builds: ctl[0] the tag of the call that opened the tail-row pool,
+  // ctl[1] the next pool row; tag is nonzero and differs from call to call (a CUDA graph
+  // replays its call's tag, and the finish clears ctl[0] between calls)
   unsigned* ctl;
+  uint32_t tag;
   // rstd == nullptr: the row pass recomputes rstd (eps as in the forward) and writes it to
   // rstd_out when that is not null
   float eps;
@@ -142,12 +145,15 @@ const void* bwd_rows_fn_nd(const Shape& s, bool fp32w, bool dh);
 const void* bwd_rows_fn_nd_rc(const Shape& s, bool fp32w, bool dh);
 
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
-cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, cudaStream_t st);
+// ctl: the non-deterministic pool words to clear once the partials are summed, or null.
+cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, unsigned* ctl,
+                             cudaStream_t st);
 
-// Non-deterministic backward (rmsn_bwd_nd.cu): CTAs take chunks of rows from a counter as
-// they go.  Its workspace is that counter (16 bytes, zeroed on the stream by a one-CTA
-// kernel launched just before the row pass) followed by the P partials; the fixed-order
-// finish adds them.
+// Non-deterministic backward (rmsn_bwd_nd.cu): each CTA's fixed prefix of rows, then a pool
+// of tail rows taken from a counter as CTAs free up.  Its workspace is the pool's two
+// words (a 16-byte slot) followed by the P partials; the fixed-order finish adds them and
+// clears the words.  They need no initial value: the pool is open to a call only once
+// its CTA 0 has published the call's tag there.
 constexpr size_t kNdCtlBytes = 16;
 Shape nd_shape(const Shape& s, int H);  // + the chunk-start slots in shared memory
 int bwd_nd_blocks_per_sm(const Shape& s, bool fp32w, bool rc);
