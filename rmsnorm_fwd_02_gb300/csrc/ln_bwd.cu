@@ -48,7 +48,8 @@ __device__ __forceinline__ void comp_add(f2& acc, f2& cmp, f2 p) {
 
 }  // namespace
 
-// Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdWide up to
+// Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdQuad up to
+// 256, kLnBwdWide up to
 // 352; each + the producer warp, one CTA an SM.  kPair: the CTA is one of a cluster of two
 // that share each row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp
 // row groups only); both CTAs add the row sums of both halves in the same order.
@@ -451,13 +452,15 @@ const void* ln_bwd_ptr_v(bool fp32w) {
                : reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, false, kPair>);
 }
 
-// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3; the pair builds
+// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3, kLnBwdQuad for 4;
+// the pair builds
 // (half-rows of 4100..8192 columns) for 2 (multi) and 3 (wide).
 const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
   if (s.pair)
     return s.cls == kLnBwdWide ? ln_bwd_ptr_v<3, kLnBwdWide, true>(fp32w)
                                : ln_bwd_ptr_v<2, kLnBwdMulti, true>(fp32w);
   if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide, false>(fp32w);
+  if (s.cls == kLnBwdQuad) return ln_bwd_ptr_v<4, kLnBwdQuad, false>(fp32w);
   return s.vpt == 1 ? ln_bwd_ptr_v<1, kLnBwdMulti, false>(fp32w)
                     : ln_bwd_ptr_v<2, kLnBwdMulti, false>(fp32w);
 }

@@ -27,9 +27,12 @@ constexpr int kLnMaxWarpsPerGroup = 16;
 //               the dw and db running sums and their compensations take 32 registers a
 //               column vector
 //  kLnFwdPair   forward of one CTA of a pair, up to 256 consumers (9 warps: 168 registers)
-enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3 };
+//  kLnBwdQuad   backward with 4-vector threads, up to 256 consumers (9 warps: 168
+//               registers, a few spilled): two 128-thread rows in flight at H = 4096,
+//               where the other classes fit one
+enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3, kLnBwdQuad = 4 };
 constexpr int ln_consumers(int cls) {
-  return cls == kLnBwdWide ? 352 : (cls == kLnFwdPair ? 256 : 480);
+  return cls == kLnBwdWide ? 352 : ((cls == kLnFwdPair || cls == kLnBwdQuad) ? 256 : 480);
 }
 constexpr int ln_max_threads(int cls) { return ln_consumers(cls) + kLnProducerThreads; }
 
@@ -98,7 +101,7 @@ struct LnShape {
   int tensors;  // BF16 tensors staged per row (1 forward, 2 backward)
   int threads;  // groups * ntg + producer warp
   size_t smem;  // dynamic shared memory bytes
-  int cls;      // kLnFwd, kLnBwdMulti or kLnBwdWide
+  int cls;      // kLnFwd, kLnBwdMulti, kLnBwdWide, kLnFwdPair or kLnBwdQuad
   int pair;     // 1: a CTA pair per row chunk, each CTA owning half the columns
 };
 

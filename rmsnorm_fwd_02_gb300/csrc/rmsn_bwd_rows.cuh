@@ -301,16 +301,16 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
           const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
           f2 wl[4];
           wvec(v, c, wl);
+          // (dy*x)*w: dy*x exact from the BF16 words, one rounding in the fma with w
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wl[q]);
-            const f2 x2 = bf2_to_f2(u4_get(xv, q));
+            const f2 dyx = bf2_mul_exact(u4_get(dv, q), u4_get(xv, q));
             if (q & 1) {
-              dot1 = f2_fma(gw, x2, dot1);
-              if constexpr (kRc) ss1 = f2_fma(x2, x2, ss1);
+              dot1 = f2_fma(dyx, wl[q], dot1);
+              if constexpr (kRc) ss1 = bf2_sq_acc(u4_get(xv, q), ss1);
             } else {
-              dot0 = f2_fma(gw, x2, dot0);
-              if constexpr (kRc) ss0 = f2_fma(x2, x2, ss0);
+              dot0 = f2_fma(dyx, wl[q], dot0);
+              if constexpr (kRc) ss0 = bf2_sq_acc(u4_get(xv, q), ss0);
             }
           }
         }

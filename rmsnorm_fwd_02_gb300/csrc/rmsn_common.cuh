@@ -214,6 +214,33 @@ __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
 __device__ __forceinline__ f2 bf2_to_f2(uint32_t u) {
   return f2_make(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
+// The two elementwise products of two words of two BF16 each, as an FP32 pair: exact (a
+// product of two 8-bit significands fits FP32's 24), formed by the mixed-precision fma
+// (BF16 sources, FP32 accumulator) with no conversion of either word.
+__device__ __forceinline__ f2 bf2_mul_exact(uint32_t a, uint32_t b) {
+  f2 r;
+  asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t.reg .f32 p0, p1;\n\t"
+      "mov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+      "fma.rn.f32.bf16 p0, a0, b0, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 p1, a1, b1, 0f80000000;\n\t"
+      "mov.b64 %0, {p0, p1};\n\t}"
+      : "=l"(r.v)
+      : "r"(a), "r"(b));
+  return r;
+}
+// c + a*a per lane for the two BF16 of word a (one rounding each: the square is exact).
+__device__ __forceinline__ f2 bf2_sq_acc(uint32_t a, f2 c) {
+  f2 r;
+  asm("{\n\t.reg .b16 a0, a1;\n\t.reg .f32 c0, c1, p0, p1;\n\t"
+      "mov.b32 {a0, a1}, %1;\n\tmov.b64 {c0, c1}, %2;\n\t"
+      "fma.rn.f32.bf16 p0, a0, a0, c0;\n\t"
+      "fma.rn.f32.bf16 p1, a1, a1, c1;\n\t"
+      "mov.b64 %0, {p0, p1};\n\t}"
+      : "=l"(r.v)
+      : "r"(a), "l"(c.v));
+  return r;
+}
+
 // The pair rounded to two BF16 (nearest even), element 2i in the low half.
 __device__ __forceinline__ uint32_t f2_to_bf2(f2 a) {
   float lo, hi;

@@ -79,12 +79,12 @@ __global__ void __launch_bounds__(kSmallThreads)
           dv[v] = *reinterpret_cast<const uint4*>(a.dy + static_cast<size_t>(row) * H + c * 8);
           load_w8_pairs<kFp32W>(a.w, c, wv[v]);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const f2 gw = f2_mul(bf2_to_f2(u4_get(dv[v], q)), wv[v][q]);
+          for (int q = 0; q < 4; ++q) {  // (dy*x)*w, dy*x exact, as the row pass forms it
+            const f2 dyx = bf2_mul_exact(u4_get(dv[v], q), u4_get(xv[v], q));
             if (q & 1)
-              dot1 = f2_fma(gw, bf2_to_f2(u4_get(xv[v], q)), dot1);
+              dot1 = f2_fma(dyx, wv[v][q], dot1);
             else
-              dot0 = f2_fma(gw, bf2_to_f2(u4_get(xv[v], q)), dot0);
+              dot0 = f2_fma(dyx, wv[v][q], dot0);
           }
         }
       }

@@ -126,8 +126,10 @@ def test_layernorm_plan_fits_its_kernel_build_at_every_width(lib, op):
                 assert p["cls"] == 0 and p["vpt"] in (1, 2, 4), ctx
                 assert p["class_max_threads"] == 512, ctx
         else:
-            assert (p["cls"], p["vpt"]) in ((1, 1), (1, 2), (2, 3)), ctx
-            assert p["class_max_threads"] == (512 if p["cls"] == 1 else 384), ctx
+            assert (p["cls"], p["vpt"]) in ((1, 1), (1, 2), (2, 3), (4, 4)), ctx
+            assert p["class_max_threads"] == {1: 512, 2: 384, 4: 288}[p["cls"]], ctx
+            if pair:
+                assert p["cls"] != 4, ctx              # no pair build of the 4-vector class
             ring = p["stages"] * tensors * p["groups"] * Hc * 2
             assert ring >= 8 * p["groups"] * Hc, ctx   # the end-of-kernel combine buffer
 
