@@ -171,7 +171,9 @@ int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, con
 /*
  * The launch plan the library uses for one op at width H: for tests and diagnostics.
  * No device access; the result depends on H and op only.
- *   op     RMSN_PLAN_FWD, RMSN_PLAN_FWD_RESIDUAL, RMSN_PLAN_BWD or RMSN_PLAN_BWD_DH
+ *   op     RMSN_PLAN_FWD, RMSN_PLAN_FWD_RESIDUAL, RMSN_PLAN_BWD or RMSN_PLAN_BWD_DH (the
+ *          deterministic backward without / with dh), RMSN_PLAN_BWD_ND or
+ *          RMSN_PLAN_BWD_ND_DH (the non-deterministic backward)
  *   out    host array receiving min(n_out, RMSN_PLAN_FIELDS) values, in this order:
  *            [0] 16-byte column vectors (8 columns) per consumer thread
  *            [1] threads per row group (8 or 16: sub-warp groups; else whole warps)
@@ -180,7 +182,8 @@ int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, con
  *            [4] threads per CTA (the row groups + one producer warp)
  *            [5] dynamic shared memory bytes per CTA
  *            [6] shape class (forward: 0 two CTAs an SM, 1 one CTA an SM; backward:
- *                0 narrow, 1 several row groups, 2 wide)
+ *                0 narrow, 1 several row groups, 2 wide, 3 several row groups with the dw
+ *                sums in tensor memory)
  *            [7] most threads a CTA of that class's kernel build may have
  *            [8] CTAs per SM that class's kernel build is made for
  * Returns RMSN_OK; RMSN_ERR_INVALID_ARG for an unknown op, out == NULL, n_out < 0 or H
@@ -190,6 +193,8 @@ int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, con
 #define RMSN_PLAN_FWD_RESIDUAL 1
 #define RMSN_PLAN_BWD 2
 #define RMSN_PLAN_BWD_DH 3
+#define RMSN_PLAN_BWD_ND 4
+#define RMSN_PLAN_BWD_ND_DH 5
 #define RMSN_PLAN_FIELDS 9
 int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out);
 

@@ -45,7 +45,7 @@ SIGNATURES = {
     "layernorm_train_device_error": (_int, [C.POINTER(C.c_uint), _int]),
 }
 
-PLAN_FWD, PLAN_FWD_RESIDUAL, PLAN_BWD, PLAN_BWD_DH = 0, 1, 2, 3
+PLAN_FWD, PLAN_FWD_RESIDUAL, PLAN_BWD, PLAN_BWD_DH, PLAN_BWD_ND, PLAN_BWD_ND_DH = 0, 1, 2, 3, 4, 5
 LN_PLAN_FWD, LN_PLAN_BWD = 0, 1
 PLAN_FIELDS = ("vpt", "group_threads", "groups", "stages", "threads", "smem", "cls",
                "class_max_threads", "class_blocks_per_sm")

@@ -24,12 +24,15 @@ constexpr int64_t kMaxRows = (int64_t{1} << 31) - (int64_t{1} << 16);
 // each; "wide" kernels, one CTA an SM, take twice that.
 constexpr size_t kRingTarget = 96 * 1024;
 constexpr size_t kRingTargetWide = 192 * 1024;
+// the tensor-memory class: three stages of its larger row count within this ring
+constexpr size_t kRingTargetTm = 200 * 1024;
 constexpr size_t kRingTargetSmall = 64 * 1024;
 // Forward rows whose group has at least this many threads run one CTA an SM (kFwdSolo).
 constexpr int kFwdSoloMinGroup = 64;
 // Largest row group of the backward's multi-group class (a multiple of 32, <= 480 / 2).
 constexpr int kMultiMaxGroup = 240;
 constexpr int kMaxStages = 12;
+constexpr size_t kMaxSmemBytes = 227 * 1024;  // dynamic shared memory a CTA may take
 // Deterministic backward: at most kDetSMs x (the CTAs an SM the kernel is built to keep
 // resident) dw partials -- a function of the shape only, so the same on every device
 // whatever its SM count.  152 is GB300's SM count: there the partition is one wave.
@@ -56,7 +59,8 @@ size_t shared_bytes(const Shape& s, int H, bool bwd) {
                      bwd ? s.groups : 0, bwd && bwd_w_in_smem(s.cls, s.vpt) ? H : 0).total;
 }
 
-Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true) {
+Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true,
+                 bool tm = false, int tm_min_stages = 3) {
   Shape s{};
   const int nv = H / 8;
   s.vpt = vpt;
@@ -69,7 +73,9 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true)
     s.ntg = ((per + 31) / 32) * 32;
   }
   if (bwd) {
-    if (allow_multi && vpt >= 2 && s.ntg <= kMultiMaxGroup)
+    if (tm)
+      s.cls = kBwdTm;
+    else if (allow_multi && vpt >= 2 && s.ntg <= kMultiMaxGroup)
       s.cls = kBwdMulti;
     else if (vpt >= 2 && s.ntg >= 32)
       s.cls = kBwdWide;
@@ -86,9 +92,20 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true)
   int budget = kMaxConsumerThreads / 2;
   if (!bwd && s.cls == kFwdSolo) budget = fwd_solo_consumers(vpt);
   if (bwd && s.cls == kBwdMulti) budget = kMultiConsumers;
+  if (bwd && s.cls == kBwdTm) budget = kTmConsumers;
   s.groups = s.ntg >= budget ? 1 : budget / s.ntg;
   // whole-warp groups: at most 16 (their reduction slots in shared memory)
   if (s.ntg >= 32 && s.groups > 16) s.groups = 16;
+  if (bwd && s.cls == kBwdTm) {
+    // whole warps of consumers, and as many groups as leave tm_min_stages stages in the
+    // ring
+    const int step = s.ntg < 32 ? 32 / s.ntg : 1;
+    s.groups -= s.groups % step;
+    while (s.groups > step &&
+           kRingTargetTm / (static_cast<size_t>(tensors) * s.groups * H * 2) <
+               static_cast<size_t>(tm_min_stages))
+      s.groups -= step;
+  }
   s.tensors = tensors;
   s.threads = s.groups * s.ntg + kProducerThreads;
   const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * H * 2;
@@ -96,7 +113,8 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true)
   // take a 64 KB ring so that three share an SM when that still leaves four or more
   // stages; the rest take 96 KB (two CTAs an SM)
   const bool one_cta = bwd ? s.cls != kBwdNarrow : s.cls == kFwdSolo;
-  size_t target = one_cta ? kRingTargetWide : kRingTarget;
+  size_t target = one_cta ? (s.cls == kBwdTm && bwd ? kRingTargetTm : kRingTargetWide)
+                          : kRingTarget;
   if (!bwd && !one_cta && s.threads <= 192 && kRingTargetSmall / stage_bytes >= 4)
     target = kRingTargetSmall;
   int st = static_cast<int>(target / stage_bytes);
@@ -212,7 +230,7 @@ Shape fwd_shape(int H, bool residual) {
   return best.vpt != 0 ? best : any;
 }
 
-Shape bwd_shape(int H, bool with_dh) {
+Shape bwd_shape(int H, bool with_dh, bool nd) {
   const int nv = H / 8;
   // rows that 240 threads cover with 2 to 4 vectors each (narrow rows in 8- or 16-lane
   // groups): several row groups in one CTA (kBwdMulti); wider rows: see below; H = 8:
@@ -238,11 +256,34 @@ Shape bwd_shape(int H, bool with_dh) {
       return groups(u) != groups(v) ? groups(u) > groups(v) : busy(u) > busy(v);
     };
     const int v = better(3, 2) ? 3 : 2;
+    Shape best = make_shape(H, tensors, v, true);
     if (groups(4) > 0 && better(4, v)) {
       const Shape s4 = make_shape(H, tensors, 4, true);
-      if (s4.stages >= 3) return s4;
+      if (s4.stages >= 3) best = s4;
     }
-    return make_shape(H, tensors, v, true);
+    // the tensor-memory class where it keeps more rows in flight (its dw state leaves
+    // the registers, so 20 warps fit), the fewest vectors a thread among equals
+    Shape det = best;
+    for (int u = 2; u <= 4; ++u) {
+      if (group(u) > kMultiMaxGroup) continue;
+      const Shape t = make_shape(H, tensors, u, true, true, /*tm=*/true);
+      if (t.stages >= 3 && t.smem <= kMaxSmemBytes && t.groups > det.groups) det = t;
+    }
+    if (!nd || det.cls != kBwdTm || det.stages >= best.stages) return det;
+    // The non-deterministic build keeps the multi class's ring depth: its producer takes
+    // the tail rows from a global counter, whose round trips a shallower ring exposes
+    // (measured: 9 rows in 3 stages ran 5 % behind 7 rows in 4 at H = 1536, where the
+    // deterministic build gained 4 %).  It keeps the deterministic build's row layout
+    // (vectors a thread, group threads), so that dx is bit-identical across the modes;
+    // only the rows a stage may differ.
+    if (best.vpt == det.vpt && best.ntg == det.ntg) {
+      const Shape t = make_shape(H, tensors, det.vpt, true, true, true, best.stages);
+      return (t.stages >= best.stages && t.smem <= kMaxSmemBytes && t.groups > best.groups)
+                 ? t
+                 : best;
+    }
+    const Shape t = make_shape(H, tensors, det.vpt, true, true, true, best.stages);
+    return (t.ntg == det.ntg && t.stages >= best.stages && t.smem <= kMaxSmemBytes) ? t : det;
   }
   // past 3 x 240 vectors: 4-vector threads in two row groups of up to 240 (H up to 7680)
   // while the ring still holds three stages of them (measured: with two stages the ring
@@ -272,7 +313,7 @@ cudaError_t prepare_kernel(const void* fn, size_t smem) {
     if (g_prepared.count(k)) return cudaSuccess;
   }
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(227 * 1024));
+                           static_cast<int>(kMaxSmemBytes));
   if (e != cudaSuccess) return e;
   (void)smem;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -353,7 +394,7 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     }
     return launch_bwd_small(a, dw, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
   }
-  const Shape s = bwd_shape(H, dh != nullptr);
+  const Shape s = bwd_shape(H, dh != nullptr, !deterministic);
   // deterministic: the partials start at the workspace; non-deterministic: after the row
   // counter
   const size_t ctl_bytes = deterministic ? 0 : kNdCtlBytes;
@@ -479,8 +520,9 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
   if (R == 0 || bwd_is_small(R)) return 0;  // small inputs take the one-launch path
   // P partials (the launch shape, so the partial count, may differ with and without dh:
   // one size serves both), after the row counter in the non-deterministic mode
-  int P = det_partials(static_cast<int32_t>(R), bwd_shape(H, false));
-  const int Pd = det_partials(static_cast<int32_t>(R), bwd_shape(H, true));
+  const bool nd = !deterministic;
+  int P = det_partials(static_cast<int32_t>(R), bwd_shape(H, false, nd));
+  const int Pd = det_partials(static_cast<int32_t>(R), bwd_shape(H, true, nd));
   if (Pd > P) P = Pd;
   return (deterministic ? 0 : kNdCtlBytes) + static_cast<size_t>(P) * 2 * H * sizeof(float);
 }
@@ -506,11 +548,13 @@ int rmsnorm_train_bwd_recompute(const void* x, const void* dy, const void* dh, c
 }
 
 int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out) {
-  if (!out || n_out < 0 || op < RMSN_PLAN_FWD || op > RMSN_PLAN_BWD_DH) return RMSN_ERR_INVALID_ARG;
+  if (!out || n_out < 0 || op < RMSN_PLAN_FWD || op > RMSN_PLAN_BWD_ND_DH)
+    return RMSN_ERR_INVALID_ARG;
   if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
   if (H > kMaxH) return RMSN_ERR_UNSUPPORTED;
   const bool bwd = op >= RMSN_PLAN_BWD;
-  const Shape s = bwd ? bwd_shape(H, op == RMSN_PLAN_BWD_DH)
+  const Shape s = bwd ? bwd_shape(H, op == RMSN_PLAN_BWD_DH || op == RMSN_PLAN_BWD_ND_DH,
+                                 op >= RMSN_PLAN_BWD_ND)
                       : fwd_shape(H, op == RMSN_PLAN_FWD_RESIDUAL);
   const int64_t v[RMSN_PLAN_FIELDS] = {
       s.vpt, s.ntg, s.groups, s.stages, s.threads, static_cast<int64_t>(s.smem), s.cls,

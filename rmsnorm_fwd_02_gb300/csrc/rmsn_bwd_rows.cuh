@@ -31,6 +31,7 @@
 
 #include "rmsn_common.cuh"
 #include "rmsn_launch.h"
+#include "rmsn_tmem.cuh"
 
 namespace rmsn {
 
@@ -94,6 +95,9 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const size_t stage_elems = static_cast<size_t>(NT) * G * H;
   const bool red_smem = NTg >= 32;  // else sub-warp groups: shuffles only
   constexpr bool kWSmem = bwd_w_in_smem(kCls, VPT);
+  // kTm: each consumer thread's dw sums and compensation terms live in tensor memory (16
+  // columns of its lane a vector) and come to registers one vector at a time
+  constexpr bool kTm = kCls == kBwdTm;
   const SmemLayout L =
       smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0, kND ? 2 * S : 0);
 
@@ -111,6 +115,8 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
   const int32_t k = blockIdx.x;
+  uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + L.abort_flag) + 2;
+  const uint32_t tm_ncols = kTm ? tmem_alloc_cols(bwd_tm_cols(ncons / 32, VPT)) : 0u;
   int32_t r0 = 0, r1 = 0, nstage = 0;
   if constexpr (!kND) {
     r0 = r0_det(k, a.R, a.P);
@@ -127,6 +133,15 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if constexpr (kTm) {
+    // consumer warp 0 takes the columns (one CTA an SM: nothing else holds them); the
+    // address reaches the other warps through shared memory
+    if (tid < 32) {
+      __syncwarp();  // the .sync.aligned tcgen05 forms want the whole warp converged
+      tmem_alloc_warp(tm_slot, tm_ncols);
+      tmem_fence_before_sync();
+    }
   }
   __syncthreads();
   pdl_wait_prior_grid();
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
   f2 wv[kWSmem ? 1 : VPT][4];  // the weight of this thread's columns (registers)
-  f2 acc[VPT][4], cmp[VPT][4];
+  f2 acc[VPT][4], cmp[VPT][4];  // (kTm: filled from tensor memory after the loop)
   float* wsm = reinterpret_cast<float*>(smem + L.w);  // or FP32 in shared memory
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
@@ -251,11 +266,27 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     if constexpr (!kWSmem) {
       if (c < NV) load_w8_pairs<kFp32W>(a.w, c, wv[v]);
     }
+    if constexpr (!kTm) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      acc[v][q] = f2_splat(0.f);
-      cmp[v][q] = f2_splat(0.f);
+      for (int q = 0; q < 4; ++q) {
+        acc[v][q] = f2_splat(0.f);
+        cmp[v][q] = f2_splat(0.f);
+      }
     }
+  }
+  // this thread's cells: vector v's 8 sums at columns tm + 16v .. +7, its 8 compensation
+  // terms at +8 .. +15 (warps sharing a lane quadrant side by side)
+  uint32_t tm = 0;
+  if constexpr (kTm) {
+    __syncwarp();
+    tmem_fence_after_sync();
+    const uint32_t w = static_cast<uint32_t>(tid >> 5);
+    tm = tmem_warp_addr(*tm_slot, w, (w >> 2) * 16u * VPT);
+    float z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) tmem_st16(tm + 16u * v, z);
   }
   if constexpr (kWSmem) {
     for (int c = tid; c < NV; c += ncons) {
@@ -352,15 +383,20 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       dot = slot_sum(slots + rb * 32, NW);
       if constexpr (kRc) ss = slot_sum(slots + rb * 32 + 16, NW);
     }
-    if (row < row_end) {
+    const bool rv = row < row_end;
+    // (kTm: every thread of the warp takes part in the tensor-memory traffic, with or
+    // without a row)
+    if (kTm || rv) {
       // this row's rstd: staged with the row (the stage is held until phase B ends), or
       // (kRc) recomputed from the row's sum of squares the way the forward forms it
-      float rs;
-      if constexpr (kRc) {
-        rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
-        if (a.rstd_out != nullptr && lt == 0) a.rstd_out[row] = rs;
-      } else {
-        rs = rs_ring[s * RSP + (row - (stage_ra & ~3))];
+      float rs = 0.f;
+      if (rv) {
+        if constexpr (kRc) {
+          rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, hf), a.eps));
+          if (a.rstd_out != nullptr && lt == 0) a.rstd_out[row] = rs;
+        } else {
+          rs = rs_ring[s * RSP + (row - (stage_ra & ~3))];
+        }
       }
       // rstd = rs_hi + rs_lo with rs_hi holding rstd's top 8 significant bits: dy*x has
       // at most 16 significant bits (two BF16 significands), so dy*x*rs_hi is exact in
@@ -374,10 +410,18 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       const f2 ncr2 = f2_splat(-(dot * (rs * inv_h)) * rs);
       const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
       const size_t out_row = static_cast<size_t>(row) * H;
+      if constexpr (kTm) {
+        __syncwarp();
+        tmem_wait_st();  // the previous row's sums are stored before they are loaded
+      }
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
         const int c = lt + v * NTg;
-        if (c < NV) {
+        const bool live = rv && c < NV;
+        float tv[16];  // kTm: this vector's sums [0, 8) and compensation terms [8, 16)
+        if constexpr (kTm) tmem_ld16(tm + 16u * v, tv);
+        f2 dyx[4];
+        if (live) {
           const uint4 xv = lds128(st + c * 8);
           const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
           uint4 hv = make_uint4(0u, 0u, 0u, 0u);
@@ -393,16 +437,39 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
             f2 d = f2_mul(f2_fma(x2, ncr2, gw), rs2);  // (g - xhat*c) * rstd
             if constexpr (kDh) d = f2_add(d, bf2_to_f2(u4_get(hv, q)));
             o[q] = f2_to_bf2(d);
-            // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
-            // compensation term, which also collects dy*x*rs_lo
-            const f2 dyx = f2_mul(d2, x2);
-            const f2 p = f2_mul(dyx, rh2);
-            const f2 t = f2_add(acc[v][q], p);
-            const f2 e = f2_add(f2_sub(acc[v][q], t), p);
-            cmp[v][q] = f2_fma(dyx, rl2, f2_add(cmp[v][q], e));
-            acc[v][q] = t;
+            dyx[q] = f2_mul(d2, x2);
+            if constexpr (!kTm) {
+              // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
+              // compensation term, which also collects dy*x*rs_lo
+              const f2 p = f2_mul(dyx[q], rh2);
+              const f2 t = f2_add(acc[v][q], p);
+              const f2 e = f2_add(f2_sub(acc[v][q], t), p);
+              cmp[v][q] = f2_fma(dyx[q], rl2, f2_add(cmp[v][q], e));
+              acc[v][q] = t;
+            }
           }
           stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        if constexpr (kTm) {
+          __syncwarp();
+          tmem_wait_ld();
+          if (live) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // the same update, on the loaded cells
+              const f2 av = f2_make(tv[2 * q], tv[2 * q + 1]);
+              const f2 p = f2_mul(dyx[q], rh2);
+              const f2 t = f2_add(av, p);
+              const f2 e = f2_add(f2_sub(av, t), p);
+              const f2 cv = f2_fma(dyx[q], rl2,
+                                   f2_add(f2_make(tv[8 + 2 * q], tv[9 + 2 * q]), e));
+              tv[2 * q] = f2_lo(t);
+              tv[2 * q + 1] = f2_hi(t);
+              tv[8 + 2 * q] = f2_lo(cv);
+              tv[9 + 2 * q] = f2_hi(cv);
+            }
+          }
+          __syncwarp();
+          tmem_st16(tm + 16u * v, tv);
         }
       }
     }
@@ -415,20 +482,27 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     // abort) ends the loop, warp-uniformly (every lane reads the same start).
     RowSums carry{0.f, 0.f};
     int32_t ra_prev = 0, rb_prev = 0;
+    // slot and parity of stage j, and the slot of stage j-1, kept by increments (no
+    // division by the runtime ring depth on the per-row path)
+    int s = 0, s_prev = 0;
+    uint32_t ph = 0;
     for (int32_t j = 0;; ++j) {
-      const int s = j % S;
-      const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u,
-                                        abort_flag, a.err, kErrConsumerWait);
+      const bool ok = mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
       const int32_t ra = ok ? srow[2 * s] : -1;
       const int32_t rb = ok ? srow[2 * s + 1] : -1;
       const bool stop = __any_sync(0xffffffffu, ra < 0);
       RowSums cur{0.f, 0.f};
       if (!stop) cur = phase_a(j, s, ra + g < rb);
-      if (j >= 1) phase_b(j - 1, (j - 1) % S, ra_prev, rb_prev, carry);
+      if (j >= 1) phase_b(j - 1, s_prev, ra_prev, rb_prev, carry);
       if (stop) break;
       ra_prev = ra;
       rb_prev = rb;
       carry = cur;
+      s_prev = s;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
   } else {
     // Rows of this warp's first group: every lane of a warp runs the same iterations
@@ -436,16 +510,46 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     const int g0 = red_smem ? g : (tid & ~31) / NTg;
     const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
     RowSums carry{0.f, 0.f};  // sub-warp groups: row j-1's sums
+    int s = 0, s_prev = 0;     // slot and parity of stage j, slot of stage j-1
+    uint32_t ph = 0;
     for (int32_t j = 0; j <= ng; ++j) {
       RowSums cur{0.f, 0.f};
       if (j < ng) {
-        const int s = j % S;
-        mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                          kErrConsumerWait);
+        mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
         cur = phase_a(j, s, r0 + j * G + g < r1);
       }
-      if (j >= 1) phase_b(j - 1, (j - 1) % S, r0 + (j - 1) * G, r1, carry);
+      if (j >= 1) phase_b(j - 1, s_prev, r0 + (j - 1) * G, r1, carry);
       carry = cur;
+      s_prev = s;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+
+  if constexpr (kTm) {
+    // the sums come back to registers, and warp 0 frees the columns once every consumer
+    // has loaded its own
+    __syncwarp();
+    tmem_wait_st();
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      float tv[16];
+      tmem_ld16(tm + 16u * v, tv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[v][q] = f2_make(tv[2 * q], tv[2 * q + 1]);
+        cmp[v][q] = f2_make(tv[8 + 2 * q], tv[9 + 2 * q]);
+      }
+    }
+    tmem_fence_before_sync();
+    named_bar_sync(13, ncons);
+    if (tid < 32) {
+      __syncwarp();
+      tmem_fence_after_sync();
+      tmem_dealloc_warp(*tm_slot, tm_ncols);
     }
   }
 
@@ -523,6 +627,9 @@ const void* pick_rows_kernel(const Shape& s, bool fp32w, bool dh) {
                : fn(&rmsn_bwd_rows_kernel<V, C, true, false, kND, kRc>))             \
          : (dh ? fn(&rmsn_bwd_rows_kernel<V, C, false, true, kND, kRc>)              \
                : fn(&rmsn_bwd_rows_kernel<V, C, false, false, kND, kRc>)))
+  if (s.cls == kBwdTm)
+    return s.vpt == 2 ? RMSN_PICK(2, kBwdTm)
+                      : (s.vpt == 3 ? RMSN_PICK(3, kBwdTm) : RMSN_PICK(4, kBwdTm));
   if (s.vpt == 1) return RMSN_PICK(1, kBwdNarrow);
   if (s.vpt == 2) return s.cls == kBwdMulti ? RMSN_PICK(2, kBwdMulti) : RMSN_PICK(2, kBwdWide);
   if (s.vpt == 3) return RMSN_PICK(3, kBwdMulti);

@@ -22,8 +22,8 @@ constexpr int kFinishSlices = 32;          // partition slices per finishing CTA
 //   rs     [stages][rs_stride(rs_rows)] FP32: the staged rows' rstd (backward; forward:
 //          none), from the 16-byte block holding the stage's first row onwards
 //   w      [w_floats] FP32 weight, for builds that keep it in shared memory
-//   abort  CTA abort flag of the bounded waits (word 0); word 1: the backward's
-//          last-CTA flag (one-launch non-deterministic build)
+//   abort  CTA abort flag of the bounded waits (word 0); word 2: the tensor-memory
+//          address of the backward builds that keep their dw sums there
 //   srow   [srow_stages] int32: the first and end row of each staged chunk (builds
 //          whose producer decides its chunks as it goes: 2 per stage; others: none)
 //
@@ -78,7 +78,8 @@ struct Shape {
   int tensors;   // BF16 tensors staged per row
   int threads;   // groups * ntg + producer warp
   size_t smem;   // dynamic shared memory bytes
-  int cls;       // shape class: kFwdPair / kFwdSolo, or kBwdNarrow / kBwdMulti / kBwdWide
+  int cls;       // shape class: kFwdPair / kFwdSolo, or kBwdNarrow / kBwdMulti / kBwdWide /
+                 // kBwdTm
 };
 
 struct RowMapArgs {
@@ -129,7 +130,7 @@ struct BwdArgs {
 
 // Shape of the forward / backward row kernels for width H.
 Shape fwd_shape(int H, bool residual);
-Shape bwd_shape(int H, bool with_dh);
+Shape bwd_shape(int H, bool with_dh, bool nd);  // nd: the non-deterministic build's shape
 
 // Launchers: return the CUDA launch status.  `pdl` opts the launch into programmatic
 // dependent launch (overlap with the previous kernel on the stream).
@@ -182,13 +183,25 @@ cudaError_t launch_rstd_rows(const BwdArgs& a, float* rstd, cudaStream_t st);
 //              and cap every thread at 96, too few for the dw state without spills)
 //  kBwdWide    one row group of more than 240 threads (2-vector, H up to 6144) or
 //              4-vector threads (H above 6144), one CTA an SM
-enum { kBwdNarrow = 0, kBwdMulti = 1, kBwdWide = 2 };
+//  kBwdTm      the multi-group class with each thread's dw sums and compensation in
+//              tensor memory instead of registers, and the weight in shared memory: up
+//              to 608 consumers (20 warps with the producer, 96 registers a thread), so
+//              more rows in flight where the multi class's registers run out
+enum { kBwdNarrow = 0, kBwdMulti = 1, kBwdWide = 2, kBwdTm = 3 };
 constexpr int kMultiConsumers = 480;
+constexpr int kTmConsumers = 608;
 
 // Backward builds that keep the weight in shared memory (FP32, H floats) instead of
-// registers: 4-vector threads of the multi-group class.
+// registers: 4-vector threads of the multi-group class, and the tensor-memory class.
 __host__ __device__ constexpr bool bwd_w_in_smem(int cls, int vpt) {
-  return cls == kBwdMulti && vpt == 4;
+  return cls == kBwdTm || (cls == kBwdMulti && vpt == 4);
+}
+
+// Tensor-memory columns a kBwdTm CTA of `cons_warps` consumer warps allocates: per thread
+// 16 columns a vector (8 sums, then 8 compensation terms), the warps that share a lane
+// quadrant side by side.
+__host__ __device__ constexpr int bwd_tm_cols(int cons_warps, int vpt) {
+  return ((cons_warps + 3) / 4) * 16 * vpt;
 }
 
 // CTAs per SM the backward row kernel is built to keep resident (its launch bounds'
@@ -198,7 +211,9 @@ constexpr int bwd_design_blocks_per_sm(int cls) { return cls == kBwdNarrow ? 2 :
 // Threads a backward CTA of the class may have (its launch bounds' maximum).
 constexpr int bwd_max_threads(int cls, int vpt) {
   return kProducerThreads +
-         (cls == kBwdMulti ? kMultiConsumers : (cls == kBwdWide && vpt == 2 ? 384 : 256));
+         (cls == kBwdMulti ? kMultiConsumers
+                           : (cls == kBwdTm ? kTmConsumers
+                                            : (cls == kBwdWide && vpt == 2 ? 384 : 256)));
 }
 
 // Forward shape classes:

@@ -128,10 +128,10 @@ def test_deterministic_workspace_size_depends_on_shape_only(lib):
     assert f(257, 1, 4096, 1) == 129 * 2 * 4096 * 4
     # H = 6144: 384 consumers, one CTA an SM -> at most 152
     assert f(65536, 1, 6144, 1) == 152 * 2 * 6144 * 4
-    # H = 256: 60 eight-lane groups without dh, 30 sixteen-lane groups with (30 rows a
-    # stage), one CTA an SM -> at most 152
-    assert f(300, 1, 256, 1) == 10 * 2 * 256 * 4
-    assert f(301, 1, 256, 1) == 11 * 2 * 256 * 4
+    # H = 256: 64 eight-lane groups without dh, 44 with (the tensor-memory class; 44 rows
+    # a stage sets the size), one CTA an SM -> at most 152
+    assert f(300, 1, 256, 1) == 7 * 2 * 256 * 4
+    assert f(309, 1, 256, 1) == 8 * 2 * 256 * 4
     assert f(65536, 24, 256, 1) == 152 * 2 * 256 * 4
     # H = 8192: 4-vector threads, one CTA an SM
     assert f(131072, 1, 8192, 1) == 152 * 2 * 8192 * 4
@@ -148,13 +148,14 @@ SMEM_PER_SM = 228 * 1024      # GB300 shared memory per SM, of which 1 KB per CT
 SMEM_PER_CTA = 227 * 1024
 
 
-@pytest.mark.parametrize("op", [0, 1, 2, 3], ids=["fwd", "fwd_res", "bwd", "bwd_dh"])
+@pytest.mark.parametrize("op", [0, 1, 2, 3, 4, 5],
+                         ids=["fwd", "fwd_res", "bwd", "bwd_dh", "bwd_nd", "bwd_nd_dh"])
 def test_launch_plan_fits_its_kernel_build_at_every_width(lib, op):
     # Every supported width: the CTA fits the launch bounds of the kernel build it selects,
     # the ring and barriers fit shared memory at the build's CTAs per SM, the row groups
     # cover the row, and (backward) the ring can hold the end-of-kernel dw combine buffer.
     from rmsnorm_fwd_02_gb300 import _native as N
-    tensors = {0: 1, 1: 2, 2: 2, 3: 3}[op]
+    tensors = {0: 1, 1: 2, 2: 2, 3: 3, 4: 2, 5: 3}[op]
     for H in range(8, 8193, 8):
         p = N.rmsnorm_train_launch_plan(H, op)
         ctx = f"H={H} {p}"
@@ -173,7 +174,15 @@ def test_launch_plan_fits_its_kernel_build_at_every_width(lib, op):
             assert ring >= 8 * p["groups"] * H, ctx
             assert p["vpt"] in (1, 2, 3, 4), ctx
             if p["vpt"] == 3:
-                assert p["cls"] == 1, ctx      # 3-vector rows only in the multi-group build
+                assert p["cls"] in (1, 3), ctx  # 3-vector rows: the multi-group builds only
+            if p["cls"] == 3:
+                # the tensor-memory class: 608 consumers at most, whole warps, and each
+                # thread's 16 columns a vector, four warps a lane quadrant, in 512 columns
+                assert p["class_max_threads"] == 640, ctx
+                warps = (p["threads"] - 32) // 32
+                assert (p["threads"] - 32) % 32 == 0, ctx
+                assert -(-warps // 4) * 16 * p["vpt"] <= 512, ctx
+                assert p["stages"] >= 3, ctx
         else:
             if p["cls"] == 1:
                 assert p["vpt"] in (2, 3, 4, 6), ctx   # the one-CTA forward's builds
@@ -184,7 +193,7 @@ def test_launch_plan_fits_its_kernel_build_at_every_width(lib, op):
 
 def test_launch_plan_rejects_bad_arguments(lib):
     out = (C.c_int64 * 9)()
-    assert lib.rmsnorm_train_launch_plan(4096, 4, out, 9) == INVALID
+    assert lib.rmsnorm_train_launch_plan(4096, 6, out, 9) == INVALID
     assert lib.rmsnorm_train_launch_plan(4096, -1, out, 9) == INVALID
     assert lib.rmsnorm_train_launch_plan(4100, 0, out, 9) == INVALID
     assert lib.rmsnorm_train_launch_plan(0, 0, out, 9) == INVALID
@@ -214,18 +223,38 @@ def test_deterministic_workspace_covers_both_dh_plans(lib):
 
 
 def test_nondeterministic_workspace_is_row_counter_and_partials(lib):
-    # non-deterministic: a 16-byte row counter before the deterministic mode's partials;
-    # no device query needed
+    # non-deterministic: a 16-byte row counter before the partials of its own plans (which
+    # may keep fewer rows a stage than the deterministic ones); no device query needed
+    from rmsnorm_fwd_02_gb300 import _native as N
     f = lib.rmsnorm_train_bwd_workspace_bytes
-    for H in (8, 256, 1536, 4096, 6144, 8192):
+    for H in (8, 256, 1024, 1536, 4096, 6144, 8192):
         assert f(256, 1, H, 0) == 0
         for T in (257, 4096, 131072):
-            assert f(T, 1, H, 0) == 16 + f(T, 1, H, 1), (H, T)
+            need = 0
+            for op in (4, 5):
+                p = N.rmsnorm_train_launch_plan(H, op)
+                P = min(-(-T // p["groups"]), 152 * p["class_blocks_per_sm"])
+                need = max(need, P * 2 * H * 4)
+            assert f(T, 1, H, 0) == 16 + need, (H, T)
+            if T == 131072:
+                assert f(T, 1, H, 0) == 16 + f(T, 1, H, 1), (H, T)
     assert f(65536, 24, 256, 0) == 16 + 152 * 2 * 256 * 4
     assert f(0, 1, 4096, 0) == 0
 
 
-@pytest.mark.parametrize("op", [2, 3], ids=["bwd", "bwd_dh"])
+@pytest.mark.parametrize("dh", [False, True], ids=["plain", "dh"])
+def test_both_modes_share_the_row_layout_at_every_width(lib, dh):
+    # dx is bit-identical across the modes only if each row is reduced the same way: the
+    # two plans may differ in rows a stage and ring depth, never in vectors a thread or
+    # threads a row group
+    from rmsnorm_fwd_02_gb300 import _native as N
+    for H in range(8, 8193, 8):
+        a = N.rmsnorm_train_launch_plan(H, 3 if dh else 2)
+        b = N.rmsnorm_train_launch_plan(H, 5 if dh else 4)
+        assert (a["vpt"], a["group_threads"]) == (b["vpt"], b["group_threads"]), (H, a, b)
+
+
+@pytest.mark.parametrize("op", [4, 5], ids=["bwd_nd", "bwd_nd_dh"])
 def test_nondeterministic_build_fits_shared_memory_at_every_width(lib, op):
     # the non-deterministic row pass adds two words per ring stage (each chunk's first and
     # end row, rounded to 16 bytes) to the deterministic build's shared memory
