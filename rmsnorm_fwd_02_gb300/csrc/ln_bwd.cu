@@ -179,14 +179,15 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
   float sg_carry = 0.f, sgd_carry = 0.f;  // sub-warp groups: row j-1's two sums
+  int s_cur = 0, s_prev = 0;  // slot and parity of stage j, slot of stage j-1 (increments,
+  uint32_t ph = 0;            // no division by the runtime ring depth)
   for (int32_t j = 0; j <= ng; ++j) {
     float sg_new = 0.f, sgd_new = 0.f;
     // ---- phase A, row j: partials of sum g and sum g*d ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
-      const int s = j % S;
-      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                        kErrConsumerWait);
+      const int s = s_cur;
+      mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
       f2 ga = f2_splat(0.f), gb = f2_splat(0.f), da = f2_splat(0.f), db2 = f2_splat(0.f);
       if (row < r1) {
         const float mu = stat[s * 2 * SP + (row - ((r0 + j * G) & ~3))];
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     if (j >= 1) {
       const int32_t jj = j - 1;
       const int32_t row = r0 + jj * G + g;
-      const int s = jj % S;
+      const int s = s_prev;
       float SG = sg_carry, SGD = sgd_carry;
       if (red_smem) {
         const int rb = (jj % kLnRedBufs) * G + g;
@@ -295,6 +296,11 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     }
     sg_carry = sg_new;
     sgd_carry = sgd_new;
+    s_prev = s_cur;
+    if (++s_cur == S) {
+      s_cur = 0;
+      ph ^= 1u;
+    }
   }
 
   // ---- this CTA's partials: per column (hi, lo) with hi + lo == acc + cmp exactly ----

@@ -212,14 +212,15 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
   const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
   float s_carry = 0.f, m_carry = 0.f;  // sub-warp groups: row j-1's merged statistics
+  int s_cur = 0, s_prev = 0;  // slot and parity of stage j, slot of stage j-1 (increments,
+  uint32_t ph = 0;            // no division by the runtime ring depth)
   for (int32_t j = 0; j <= ng; ++j) {
     float St = 0.f, Mt = 0.f;
     // ---- phase A, row j: this thread's sum and sum of squared deviations ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
-      const int s = j % S;
-      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                        kErrConsumerWait);
+      const int s = s_cur;
+      mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
       if (row < r1) {
         const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
         // statistics of x - K, K the row's first element (one value for the whole group,
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
     if (j >= 1) {
       const int32_t jj = j - 1;
       const int32_t row = r0 + jj * G + g;
-      const int s = jj % S;
+      const int s = s_prev;
       const bool valid = row < r1;
       const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
       uint4 hv[VPT];
@@ -346,6 +347,11 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
     }
     s_carry = St;
     m_carry = Mt;
+    s_prev = s_cur;
+    if (++s_cur == S) {
+      s_cur = 0;
+      ph ^= 1u;
+    }
   }
   if constexpr (kPair) {
     __syncwarp();

@@ -32,6 +32,12 @@ constexpr int kFwdSoloMinGroup = 64;
 // Largest row group of the backward's multi-group class (a multiple of 32, <= 480 / 2).
 constexpr int kMultiMaxGroup = 240;
 constexpr int kMaxStages = 12;
+// The forward keeps at most three stages in flight a CTA: its consumers outrun HBM, so
+// every free stage is an outstanding load, and fewer streams per SM make better use of
+// the DRAM (measured, one CTA an SM, H = 1536..6144: 3 stages 1-6 % ahead of 6 at large
+// T and in the back-to-back clock at T = 16384, 2 stages 10-20 % behind; two CTAs an SM,
+// [T,24,256] of 32 heads: 3 stages 8 % ahead of 6).
+constexpr int kFwdMaxStages = 3;
 constexpr size_t kMaxSmemBytes = 227 * 1024;  // dynamic shared memory a CTA may take
 // Deterministic backward: at most kDetSMs x (the CTAs an SM the kernel is built to keep
 // resident) dw partials -- a function of the shape only, so the same on every device
@@ -119,6 +125,7 @@ Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true,
     target = kRingTargetSmall;
   int st = static_cast<int>(target / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
+  if (!bwd && s.stages > kFwdMaxStages) s.stages = kFwdMaxStages;
   s.smem = shared_bytes(s, H, bwd);
   return s;
 }

@@ -132,14 +132,15 @@ __global__ void __launch_bounds__(fwd_max_threads(kCls, VPT), fwd_design_blocks_
   const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
 
   float ss_carry = 0.f;  // sub-warp groups: row j-1's sum of squares
+  int s_cur = 0, s_prev = 0;  // slot and parity of stage j, slot of stage j-1 (increments,
+  uint32_t ph = 0;            // no division by the runtime ring depth)
   for (int32_t j = 0; j <= ng; ++j) {
     float part = 0.f;
     // ---- phase A, row j: this thread's partial sum of squares (and h, residual form) ----
     if (j < ng) {
       const int32_t row = r0 + j * G + g;
-      const int s = j % S;
-      mbar_wait_bounded(&full[s], static_cast<uint32_t>(j / S) & 1u, abort_flag, a.err,
-                        kErrConsumerWait);
+      const int s = s_cur;
+      mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
       const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
       f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);  // two chains, fixed combine order
       if (row < r1) {
@@ -152,12 +153,12 @@ __global__ void __launch_bounds__(fwd_max_threads(kCls, VPT), fwd_design_blocks_
               u = residual_sum8(u, lds128(xs + static_cast<size_t>(G) * H + c * 8));
               stg128(a.h + static_cast<size_t>(row) * H + c * 8, u);
             }
-            const f2 e0 = bf2_to_f2(u.x), e1 = bf2_to_f2(u.y);
-            const f2 e2 = bf2_to_f2(u.z), e3 = bf2_to_f2(u.w);
-            ss0 = f2_fma(e0, e0, ss0);
-            ss1 = f2_fma(e1, e1, ss1);
-            ss0 = f2_fma(e2, e2, ss0);
-            ss1 = f2_fma(e3, e3, ss1);
+            // x^2 + ss per element straight from the BF16 words (the square is exact, so
+            // this rounds exactly as converting first and using an FP32 fma would)
+            ss0 = bf2_sq_acc(u.x, ss0);
+            ss1 = bf2_sq_acc(u.y, ss1);
+            ss0 = bf2_sq_acc(u.z, ss0);
+            ss1 = bf2_sq_acc(u.w, ss1);
           }
         }
       }
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(fwd_max_threads(kCls, VPT), fwd_design_blocks_
     if (j >= 1) {
       const int32_t jj = j - 1;
       const int32_t row = r0 + jj * G + g;
-      const int s = jj % S;
+      const int s = s_prev;
       const bool valid = row < r1;
       const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
       uint4 hv[VPT];
@@ -223,6 +224,11 @@ __global__ void __launch_bounds__(fwd_max_threads(kCls, VPT), fwd_design_blocks_
       mbar_arrive(&redb[(j % kRedBufs) * G + g]);
     }
     ss_carry = red_j;
+    s_prev = s_cur;
+    if (++s_cur == S) {
+      s_cur = 0;
+      ph ^= 1u;
+    }
   }
 }
 
