@@ -173,7 +173,8 @@ int rmsnorm_train_bwd_noalloc(const void* x, const void* dy, const void* dh, con
  * No device access; the result depends on H and op only.
  *   op     RMSN_PLAN_FWD, RMSN_PLAN_FWD_RESIDUAL, RMSN_PLAN_BWD or RMSN_PLAN_BWD_DH (the
  *          deterministic backward without / with dh), RMSN_PLAN_BWD_ND or
- *          RMSN_PLAN_BWD_ND_DH (the non-deterministic backward)
+ *          RMSN_PLAN_BWD_ND_DH (the non-deterministic backward: the same plans, as both
+ *          modes run one row-pass program on one launch shape)
  *   out    host array receiving min(n_out, RMSN_PLAN_FIELDS) values, in this order:
  *            [0] 16-byte column vectors (8 columns) per consumer thread
  *            [1] threads per row group (8 or 16: sub-warp groups; else whole warps)

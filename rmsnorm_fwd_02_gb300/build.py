@@ -18,8 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librmsnorm_train.so")
-SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_bwd_rc.cu", "rmsn_bwd_nd.cu",
-           "rmsn_bwd_nd_rc.cu", "rmsn_small.cu",
+SOURCES = ["rmsn_api.cu", "rmsn_fwd.cu", "rmsn_bwd.cu", "rmsn_bwd_rc.cu", "rmsn_small.cu",
            "ln_api.cu", "ln_fwd.cu", "ln_bwd.cu"]
 HEADERS = ["rmsn_common.cuh", "rmsn_launch.h", "rmsn_bwd_rows.cuh", "rmsn_tmem.cuh", "ln_launch.h",
            "ln_common.cuh"]

@@ -62,7 +62,9 @@ uint64_t key(int dev, const void* fn, uint64_t extra) {
 
 size_t shared_bytes(const Shape& s, int H, bool bwd) {
   return smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0,
-                     bwd ? s.groups : 0, bwd && bwd_w_in_smem(s.cls, s.vpt) ? H : 0).total;
+                     bwd ? s.groups : 0, bwd && bwd_w_in_smem(s.cls, s.vpt) ? H : 0,
+                     bwd ? 2 * s.stages : 0)
+      .total;
 }
 
 Shape make_shape(int H, int tensors, int vpt, bool bwd, bool allow_multi = true,
@@ -237,7 +239,7 @@ Shape fwd_shape(int H, bool residual) {
   return best.vpt != 0 ? best : any;
 }
 
-Shape bwd_shape(int H, bool with_dh, bool nd) {
+Shape bwd_shape(int H, bool with_dh) {
   const int nv = H / 8;
   // rows that 240 threads cover with 2 to 4 vectors each (narrow rows in 8- or 16-lane
   // groups): several row groups in one CTA (kBwdMulti); wider rows: see below; H = 8:
@@ -268,29 +270,25 @@ Shape bwd_shape(int H, bool with_dh, bool nd) {
       const Shape s4 = make_shape(H, tensors, 4, true);
       if (s4.stages >= 3) best = s4;
     }
-    // the tensor-memory class where it keeps more rows in flight (its dw state leaves
-    // the registers, so 20 warps fit), the fewest vectors a thread among equals
-    Shape det = best;
+    // The tensor-memory class where it keeps more rows in flight (its dw state leaves
+    // the registers, so 20 warps fit): the vector count with the most rows a stage at
+    // three stages (the fewest vectors among equals), then as many rows as keep the
+    // multi class's ring depth -- the non-deterministic pool's counter round trips want
+    // the deeper ring, and both modes run one program on one shape (measured at H = 1536:
+    // 8 rows in 4 stages 4 % ahead of 9 in 3, and of 7 in 4 in the multi class).
+    int tv = 0, tg = best.groups;
     for (int u = 2; u <= 4; ++u) {
       if (group(u) > kMultiMaxGroup) continue;
       const Shape t = make_shape(H, tensors, u, true, true, /*tm=*/true);
-      if (t.stages >= 3 && t.smem <= kMaxSmemBytes && t.groups > det.groups) det = t;
+      if (t.stages >= 3 && t.smem <= kMaxSmemBytes && t.groups > tg) {
+        tv = u;
+        tg = t.groups;
+      }
     }
-    if (!nd || det.cls != kBwdTm || det.stages >= best.stages) return det;
-    // The non-deterministic build keeps the multi class's ring depth: its producer takes
-    // the tail rows from a global counter, whose round trips a shallower ring exposes
-    // (measured: 9 rows in 3 stages ran 5 % behind 7 rows in 4 at H = 1536, where the
-    // deterministic build gained 4 %).  It keeps the deterministic build's row layout
-    // (vectors a thread, group threads), so that dx is bit-identical across the modes;
-    // only the rows a stage may differ.
-    if (best.vpt == det.vpt && best.ntg == det.ntg) {
-      const Shape t = make_shape(H, tensors, det.vpt, true, true, true, best.stages);
-      return (t.stages >= best.stages && t.smem <= kMaxSmemBytes && t.groups > best.groups)
-                 ? t
-                 : best;
-    }
-    const Shape t = make_shape(H, tensors, det.vpt, true, true, true, best.stages);
-    return (t.ntg == det.ntg && t.stages >= best.stages && t.smem <= kMaxSmemBytes) ? t : det;
+    if (tv == 0) return best;
+    const int depth = best.stages > 3 ? best.stages : 3;
+    const Shape t = make_shape(H, tensors, tv, true, true, true, depth);
+    return (t.stages >= depth && t.smem <= kMaxSmemBytes && t.groups > best.groups) ? t : best;
   }
   // past 3 x 240 vectors: 4-vector threads in two row groups of up to 240 (H up to 7680)
   // while the ring still holds three stages of them (measured: with two stages the ring
@@ -300,14 +298,6 @@ Shape bwd_shape(int H, bool with_dh, bool nd) {
     if (s.stages >= 3) return s;
   }
   return make_shape(H, tensors, nv <= 768 ? 2 : 4, true, /*allow_multi=*/false);
-}
-
-Shape nd_shape(const Shape& s, int H) {
-  Shape n = s;
-  n.smem = smem_layout(s.stages, s.tensors, s.groups, H, s.ntg >= 32 ? s.groups : 0, s.groups,
-                       bwd_w_in_smem(s.cls, s.vpt) ? H : 0, 2 * s.stages)
-               .total;
-  return n;
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem) {
@@ -401,7 +391,7 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     }
     return launch_bwd_small(a, dw, fp32w, stream_) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
   }
-  const Shape s = bwd_shape(H, dh != nullptr, !deterministic);
+  const Shape s = bwd_shape(H, dh != nullptr);
   // deterministic: the partials start at the workspace; non-deterministic: after the row
   // counter
   const size_t ctl_bytes = deterministic ? 0 : kNdCtlBytes;
@@ -413,10 +403,8 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     // at most 152 x (CTAs an SM of the class) partials in either mode (the deterministic
     // partition; the non-deterministic one is also bounded by this GPU's resident CTAs)
     P = det_partials(static_cast<int32_t>(R), s);
-    Shape sl = s;
     if (!deterministic) {
-      sl = nd_shape(s, H);
-      const int occ = bwd_nd_blocks_per_sm(sl, fp32w, rstd == nullptr);
+      const int occ = bwd_blocks_per_sm(s, fp32w, rstd == nullptr);
       const int64_t cap = static_cast<int64_t>(g_sms[dev]) * (occ > 0 ? occ : 1);
       if (P > cap) P = static_cast<int>(cap);
     }
@@ -443,9 +431,7 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     a.stages = s.stages;
     a.P = P;
     a.err = g_err_ptr[dev];
-    const cudaError_t e = deterministic ? launch_bwd_rows(a, sl, fp32w, stream_)
-                                        : launch_bwd_nd(a, sl, fp32w, stream_);
-    if (e != cudaSuccess) return RMSN_ERR_CUDA;
+    if (launch_bwd_rows(a, s, fp32w, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
   }
   unsigned* ctl = (deterministic || R == 0) ? nullptr : static_cast<unsigned*>(workspace);
   if (launch_dw_finish(part, dw, P, H, ctl, stream_) != cudaSuccess)
@@ -527,9 +513,8 @@ size_t rmsnorm_train_bwd_workspace_bytes(int64_t T, int32_t nh, int32_t H, int d
   if (R == 0 || bwd_is_small(R)) return 0;  // small inputs take the one-launch path
   // P partials (the launch shape, so the partial count, may differ with and without dh:
   // one size serves both), after the row counter in the non-deterministic mode
-  const bool nd = !deterministic;
-  int P = det_partials(static_cast<int32_t>(R), bwd_shape(H, false, nd));
-  const int Pd = det_partials(static_cast<int32_t>(R), bwd_shape(H, true, nd));
+  int P = det_partials(static_cast<int32_t>(R), bwd_shape(H, false));
+  const int Pd = det_partials(static_cast<int32_t>(R), bwd_shape(H, true));
   if (Pd > P) P = Pd;
   return (deterministic ? 0 : kNdCtlBytes) + static_cast<size_t>(P) * 2 * H * sizeof(float);
 }
@@ -560,8 +545,7 @@ int rmsnorm_train_launch_plan(int32_t H, int op, int64_t* out, int n_out) {
   if (H <= 0 || (H % 8) != 0) return RMSN_ERR_INVALID_ARG;
   if (H > kMaxH) return RMSN_ERR_UNSUPPORTED;
   const bool bwd = op >= RMSN_PLAN_BWD;
-  const Shape s = bwd ? bwd_shape(H, op == RMSN_PLAN_BWD_DH || op == RMSN_PLAN_BWD_ND_DH,
-                                 op >= RMSN_PLAN_BWD_ND)
+  const Shape s = bwd ? bwd_shape(H, op == RMSN_PLAN_BWD_DH || op == RMSN_PLAN_BWD_ND_DH)
                       : fwd_shape(H, op == RMSN_PLAN_FWD_RESIDUAL);
   const int64_t v[RMSN_PLAN_FIELDS] = {
       s.vpt, s.ntg, s.groups, s.stages, s.threads, static_cast<int64_t>(s.smem), s.cls,

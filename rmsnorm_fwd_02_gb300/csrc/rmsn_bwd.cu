@@ -1,6 +1,13 @@
-// rmsn_bwd.cu -- RMSNorm training backward for sm_103a, deterministic builds: the row
-// pass (rmsn_bwd_rows.cuh) with a fixed chunk of rows per CTA writing its compensated dw
-// partial to the workspace, and the fixed-order dw finish.
+// rmsn_bwd.cu -- RMSNorm training backward for sm_103a: the row pass (rmsn_bwd_rows.cuh;
+// its builds that read rstd -- those that recompute it are in rmsn_bwd_rc.cu), each CTA
+// writing its compensated dw partial to the workspace, and the fixed-order dw finish.
+//
+// One row-pass program serves both modes.  deterministic=1: CTA k owns a fixed chunk of
+// rows, a function of (R, P) only.  deterministic=0 (flashinfer PR #8827, description:
+// free to be faster): each CTA owns a fixed prefix and the last rows are handed out from a
+// counter in the workspace as CTAs free up, so no CTA idles while another still holds a
+// queue of rows; dw's partials then cover rows that vary from run to run, so its last bits
+// may too.  dx never depends on the partition: it is bit-identical across the modes.
 #include "rmsn_bwd_rows.cuh"
 
 namespace rmsn {
@@ -65,13 +72,12 @@ __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
   if (sl == 0 && col < H) dw[col] = __fadd_rn(sh[0][cl], se[0][cl]);
 }
 
-const void* bwd_rows_fn_det(const Shape& s, bool fp32w, bool dh) {
-  return pick_rows_kernel<false, false>(s, fp32w, dh);
+const void* bwd_rows_fn_rs(const Shape& s, bool fp32w, bool dh) {
+  return pick_rows_kernel<false>(s, fp32w, dh);
 }
 
-const void* bwd_rows_fn(const Shape& s, bool fp32w, bool dh, bool nd, bool rc) {
-  if (nd) return rc ? bwd_rows_fn_nd_rc(s, fp32w, dh) : bwd_rows_fn_nd(s, fp32w, dh);
-  return rc ? bwd_rows_fn_det_rc(s, fp32w, dh) : bwd_rows_fn_det(s, fp32w, dh);
+const void* bwd_rows_fn(const Shape& s, bool fp32w, bool dh, bool rc) {
+  return rc ? bwd_rows_fn_rc(s, fp32w, dh) : bwd_rows_fn_rs(s, fp32w, dh);
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem);
@@ -79,8 +85,12 @@ int blocks_per_sm(const void* fn, int threads, size_t smem);
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        void** args);
 
+int bwd_blocks_per_sm(const Shape& s, bool fp32w, bool rc) {
+  return blocks_per_sm(bwd_rows_fn(s, fp32w, s.tensors == 3, rc), s.threads, s.smem);
+}
+
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st) {
-  const void* fn = bwd_rows_fn(s, fp32w, a.dh != nullptr, false, a.rstd == nullptr);
+  const void* fn = bwd_rows_fn(s, fp32w, a.dh != nullptr, a.rstd == nullptr);
   cudaError_t e = prepare_kernel(fn, s.smem);
   if (e != cudaSuccess) return e;
   BwdArgs copy = a;

@@ -1,8 +1,9 @@
 // rmsn_bwd_rows.cuh -- the RMSNorm training backward's row pass for sm_103a: dx fused with
-// the compensated dw partial sums.  Included by rmsn_bwd.cu (deterministic builds: a fixed
-// chunk of rows per CTA) and by rmsn_bwd_nd.cu (non-deterministic builds: rows handed out
-// as the CTAs go); both write one dw partial per CTA to the workspace, and the
-// fixed-order finish kernel (rmsn_bwd.cu) adds them.
+// the compensated dw partial sums, one program for both modes (the partition is chosen at
+// run time: a fixed chunk of rows per CTA, or a fixed prefix plus rows handed out from a
+// counter).  Included by rmsn_bwd.cu (builds that read rstd) and rmsn_bwd_rc.cu (builds
+// that recompute it); each CTA writes one dw partial to the workspace, and the fixed-order
+// finish kernel (rmsn_bwd.cu) adds them.
 //
 // Per normalized row, with r the forward's rstd (flashinfer PR #8827, description: the
 // backward's BF16 dx and FP32 dw; the residual form's combined gradient):
@@ -72,18 +73,23 @@ struct RowSums {
 // kRc = true: the backward is not handed rstd; phase A forms sum_j x_j^2 beside
 // sum_j (dy_j*w_j)*x_j (both through the one reduction) and phase B recomputes
 // rstd = 1/sqrt(sum x^2 / H + eps) as the forward does, writing it to a.rstd_out if given.
-// kND = false: CTA k owns rows [k*R/P, (k+1)*R/P).
-// kND = true: CTA k owns a fixed prefix of Ns stages, rows [k*Ns*G, (k+1)*Ns*G), and the
-// last ~2 stages' worth of rows a CTA would own, rows [P*Ns*G, R), form a pool handed out
-// G rows at a time by the counter a.ctl[1]: a CTA that is done with its prefix early takes
-// more of the tail, so none idles while another still holds a queue.  CTA 0 opens the
-// pool (sets the counter, then publishes the call's tag in a.ctl[0]) before its own rows;
-// a CTA that reaches the pool before it is open takes nothing from it, and CTA 0 itself
-// always drains it, so no CTA ever waits on another.  (Below 4 stages a CTA the prefix
-// is the deterministic chunk and the pool is empty.)  The producer passes each stage's
-// first row to the consumers through shared memory; a negative start ends the CTA's work.
-// Either way CTA k writes its dw partial to a.part[k].
-template <int VPT, int kCls, bool kFp32W, bool kDh, bool kND, bool kRc>
+// The rows a CTA takes (the producer decides them stage by stage and passes each stage's
+// rows [start, end) to the consumers through shared memory; a negative start ends the
+// CTA's work):
+//  a.ctl == nullptr (deterministic): CTA k owns rows [k*R/P, (k+1)*R/P), a function of
+//    (R, P) only, so its partial -- and the fixed-order finish -- are bit-reproducible.
+//  a.ctl != nullptr (non-deterministic): CTA k owns a fixed prefix of Ns stages, rows
+//    [k*Ns*G, (k+1)*Ns*G), and the last ~2 stages' worth of rows a CTA would own, rows
+//    [P*Ns*G, R), form a pool handed out G rows at a time by the counter a.ctl[1]: a CTA
+//    that is done with its prefix early takes more of the tail, so none idles while
+//    another still holds a queue.  CTA 0 opens the pool (sets the counter, then publishes
+//    the call's tag in a.ctl[0]) before its own rows; a CTA that reaches the pool before
+//    it is open takes nothing from it, and CTA 0 itself always drains it, so no CTA ever
+//    waits on another.  (Below 4 stages a CTA the prefix is the deterministic chunk and
+//    the pool is empty.)
+// Either way CTA k writes its dw partial to a.part[k], and dx does not depend on the
+// partition.
+template <int VPT, int kCls, bool kFp32W, bool kDh, bool kRc>
 __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_per_sm(kCls))
     rmsn_bwd_rows_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -99,7 +105,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   // columns of its lane a vector) and come to registers one vector at a time
   constexpr bool kTm = kCls == kBwdTm;
   const SmemLayout L =
-      smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0, kND ? 2 * S : 0);
+      smem_layout(S, NT, G, H, red_smem ? G : 0, G, kWSmem ? H : 0, 2 * S);
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -117,12 +123,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   const int32_t k = blockIdx.x;
   uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + L.abort_flag) + 2;
   const uint32_t tm_ncols = kTm ? tmem_alloc_cols(bwd_tm_cols(ncons / 32, VPT)) : 0u;
-  int32_t r0 = 0, r1 = 0, nstage = 0;
-  if constexpr (!kND) {
-    r0 = r0_det(k, a.R, a.P);
-    r1 = r0_det(k + 1, a.R, a.P);
-    nstage = (r1 - r0 + G - 1) / G;
-  }
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -179,67 +179,55 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
         if constexpr (kDh) copy_rows_contig(dst + 2 * G * H, a.dh, H, ra, rb, &full[s], pol);
       };
       int32_t j = 0;  // stages whose full barrier has been armed
-      if constexpr (kND) {
-        const uint32_t R = static_cast<uint32_t>(a.R);
-        const uint32_t per = static_cast<uint32_t>(a.P) * static_cast<uint32_t>(G);
-        const uint32_t nfull = R / per;          // whole stages every CTA could own
-        uint32_t pa, pb, pool;                   // this CTA's prefix [pa, pb), pool start
-        if (nfull >= 4) {
-          const uint32_t Ns = nfull - 2;
-          pa = static_cast<uint32_t>(k) * Ns * G;
-          pb = pa + Ns * G;
-          pool = per * Ns;
-        } else {
-          pa = static_cast<uint32_t>(r0_det(k, a.R, a.P));
-          pb = static_cast<uint32_t>(r0_det(k + 1, a.R, a.P));
-          pool = R;
-        }
-        if (k == 0 && pool < R) {  // open the pool: the counter first, then the tag
-          a.ctl[1] = pool;
-          __threadfence();
-          st_release_u32(a.ctl, a.tag);
-        }
-        bool tail = false;
-        uint32_t next = pa;
-        uint32_t first_tail = R;  // the first pool chunk, taken while the prefix's last
-                                  // stage is issued (so its round trip is hidden too)
-        for (;; ++j) {
-          const int s = j % S;
-          if (j >= S &&
-              !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
-                                 a.err, kErrProducerWait))
-            break;
-          if (!tail && next >= pb) {  // prefix done: on to the pool
-            tail = true;
-            next = first_tail;
-          }
-          const uint32_t ra = next;
-          if (ra >= R) {  // no rows left: an empty stage tells the consumers to stop
-            srow[2 * s] = -1;
-            mbar_arrive(&full[s]);
-            ++j;
-            break;
-          }
-          // the next tail chunk is taken now, so the atomic's round trip overlaps the wait
-          // for the next free slot
-          const uint32_t rb = tail ? min(ra + G, R) : min(ra + G, pb);
-          if (!tail && rb >= pb && pool < R && ld_acquire_u32(a.ctl) == a.tag)
-            first_tail = atomicAdd(a.ctl + 1, G);  // the pool is open: reserve a chunk
-          next = tail ? atomicAdd(a.ctl + 1, G) : rb;
-          srow[2 * s] = static_cast<int32_t>(ra);  // published by the arrival in issue()
-          srow[2 * s + 1] = static_cast<int32_t>(rb);
-          issue(s, static_cast<int32_t>(ra), static_cast<int32_t>(rb));
-        }
+      const uint32_t R = static_cast<uint32_t>(a.R);
+      const uint32_t per = static_cast<uint32_t>(a.P) * static_cast<uint32_t>(G);
+      const uint32_t nfull = R / per;          // whole stages every CTA could own
+      uint32_t pa, pb, pool;                   // this CTA's own rows [pa, pb), pool start
+      if (nfull >= 4 && a.ctl != nullptr) {  // non-deterministic: prefix and pool
+        const uint32_t Ns = nfull - 2;
+        pa = static_cast<uint32_t>(k) * Ns * G;
+        pb = pa + Ns * G;
+        pool = per * Ns;
       } else {
-        for (; j < nstage; ++j) {
-          const int s = j % S;
-          if (j >= S &&
-              !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
-                                 a.err, kErrProducerWait))
-            break;
-          const int32_t ra = r0 + j * G;
-          issue(s, ra, min(ra + G, r1));
+        pa = static_cast<uint32_t>(r0_det(k, a.R, a.P));
+        pb = static_cast<uint32_t>(r0_det(k + 1, a.R, a.P));
+        pool = R;
+      }
+      if (k == 0 && pool < R) {  // open the pool: the counter first, then the tag
+        a.ctl[1] = pool;
+        __threadfence();
+        st_release_u32(a.ctl, a.tag);
+      }
+      bool tail = false;
+      uint32_t next = pa;
+      uint32_t first_tail = R;  // the first pool chunk, taken while the prefix's last
+                                // stage is issued (so its round trip is hidden too)
+      for (;; ++j) {
+        const int s = j % S;
+        if (j >= S &&
+            !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((j / S) - 1) & 1u, abort_flag,
+                               a.err, kErrProducerWait))
+          break;
+        if (!tail && next >= pb) {  // prefix done: on to the pool
+          tail = true;
+          next = first_tail;
         }
+        const uint32_t ra = next;
+        if (ra >= R) {  // no rows left: an empty stage tells the consumers to stop
+          srow[2 * s] = -1;
+          mbar_arrive(&full[s]);
+          ++j;
+          break;
+        }
+        // the next tail chunk is taken now, so the atomic's round trip overlaps the wait
+        // for the next free slot
+        const uint32_t rb = tail ? min(ra + G, R) : min(ra + G, pb);
+        if (!tail && rb >= pb && pool < R && ld_acquire_u32(a.ctl) == a.tag)
+          first_tail = atomicAdd(a.ctl + 1, G);  // the pool is open: reserve a chunk
+        next = tail ? atomicAdd(a.ctl + 1, G) : rb;
+        srow[2 * s] = static_cast<int32_t>(ra);  // published by the arrival in issue()
+        srow[2 * s + 1] = static_cast<int32_t>(rb);
+        issue(s, static_cast<int32_t>(ra), static_cast<int32_t>(rb));
       }
       mbar_drain(full, S, j);
     }
@@ -477,54 +465,30 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the stage
   };
 
-  if constexpr (kND) {
-    // Stages in the order the producer filled them; a negative chunk start (or an
-    // abort) ends the loop, warp-uniformly (every lane reads the same start).
-    RowSums carry{0.f, 0.f};
-    int32_t ra_prev = 0, rb_prev = 0;
-    // slot and parity of stage j, and the slot of stage j-1, kept by increments (no
-    // division by the runtime ring depth on the per-row path)
-    int s = 0, s_prev = 0;
-    uint32_t ph = 0;
-    for (int32_t j = 0;; ++j) {
-      const bool ok = mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
-      const int32_t ra = ok ? srow[2 * s] : -1;
-      const int32_t rb = ok ? srow[2 * s + 1] : -1;
-      const bool stop = __any_sync(0xffffffffu, ra < 0);
-      RowSums cur{0.f, 0.f};
-      if (!stop) cur = phase_a(j, s, ra + g < rb);
-      if (j >= 1) phase_b(j - 1, s_prev, ra_prev, rb_prev, carry);
-      if (stop) break;
-      ra_prev = ra;
-      rb_prev = rb;
-      carry = cur;
-      s_prev = s;
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-  } else {
-    // Rows of this warp's first group: every lane of a warp runs the same iterations
-    // (the shuffles need them all); groups past the chunk's end skip the row work.
-    const int g0 = red_smem ? g : (tid & ~31) / NTg;
-    const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
-    RowSums carry{0.f, 0.f};  // sub-warp groups: row j-1's sums
-    int s = 0, s_prev = 0;     // slot and parity of stage j, slot of stage j-1
-    uint32_t ph = 0;
-    for (int32_t j = 0; j <= ng; ++j) {
-      RowSums cur{0.f, 0.f};
-      if (j < ng) {
-        mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
-        cur = phase_a(j, s, r0 + j * G + g < r1);
-      }
-      if (j >= 1) phase_b(j - 1, s_prev, r0 + (j - 1) * G, r1, carry);
-      carry = cur;
-      s_prev = s;
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
+  // Stages in the order the producer filled them; a negative chunk start (or an
+  // abort) ends the loop, warp-uniformly (every lane reads the same start).
+  RowSums carry{0.f, 0.f};
+  int32_t ra_prev = 0, rb_prev = 0;
+  // slot and parity of stage j, and the slot of stage j-1, kept by increments (no
+  // division by the runtime ring depth on the per-row path)
+  int s = 0, s_prev = 0;
+  uint32_t ph = 0;
+  for (int32_t j = 0;; ++j) {
+    const bool ok = mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
+    const int32_t ra = ok ? srow[2 * s] : -1;
+    const int32_t rb = ok ? srow[2 * s + 1] : -1;
+    const bool stop = __any_sync(0xffffffffu, ra < 0);
+    RowSums cur{0.f, 0.f};
+    if (!stop) cur = phase_a(j, s, ra + g < rb);
+    if (j >= 1) phase_b(j - 1, s_prev, ra_prev, rb_prev, carry);
+    if (stop) break;
+    ra_prev = ra;
+    rb_prev = rb;
+    carry = cur;
+    s_prev = s;
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
     }
   }
 
@@ -616,17 +580,18 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   }
 }
 
-// The kernel build for a launch shape, per (kND, kRc) pair; each pair's translation unit
+// The kernel build for a launch shape (both modes), per kRc; each value's translation unit
 // instantiates only its own builds.  (bwd_shape gives 1-vector lanes the narrow class, 2-
-// and 4-vector threads the multi or the wide class, 3-vector threads the multi class.)
-template <bool kND, bool kRc>
+// and 4-vector threads the multi, tensor-memory or wide class, 3-vector threads the multi
+// or tensor-memory class.)
+template <bool kRc>
 const void* pick_rows_kernel(const Shape& s, bool fp32w, bool dh) {
   auto fn = [](auto k) { return reinterpret_cast<const void*>(k); };
-#define RMSN_PICK(V, C)                                                              \
-  (fp32w ? (dh ? fn(&rmsn_bwd_rows_kernel<V, C, true, true, kND, kRc>)               \
-               : fn(&rmsn_bwd_rows_kernel<V, C, true, false, kND, kRc>))             \
-         : (dh ? fn(&rmsn_bwd_rows_kernel<V, C, false, true, kND, kRc>)              \
-               : fn(&rmsn_bwd_rows_kernel<V, C, false, false, kND, kRc>)))
+#define RMSN_PICK(V, C)                                                               \
+  (fp32w ? (dh ? fn(&rmsn_bwd_rows_kernel<V, C, true, true, kRc>)                     \
+               : fn(&rmsn_bwd_rows_kernel<V, C, true, false, kRc>))                   \
+         : (dh ? fn(&rmsn_bwd_rows_kernel<V, C, false, true, kRc>)                    \
+               : fn(&rmsn_bwd_rows_kernel<V, C, false, false, kRc>)))
   if (s.cls == kBwdTm)
     return s.vpt == 2 ? RMSN_PICK(2, kBwdTm)
                       : (s.vpt == 3 ? RMSN_PICK(3, kBwdTm) : RMSN_PICK(4, kBwdTm));

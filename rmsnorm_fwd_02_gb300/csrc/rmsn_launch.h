@@ -130,35 +130,30 @@ struct BwdArgs {
 
 // Shape of the forward / backward row kernels for width H.
 Shape fwd_shape(int H, bool residual);
-Shape bwd_shape(int H, bool with_dh, bool nd);  // nd: the non-deterministic build's shape
+Shape bwd_shape(int H, bool with_dh);  // both modes
 
 // Launchers: return the CUDA launch status.  `pdl` opts the launch into programmatic
 // dependent launch (overlap with the previous kernel on the stream).
 cudaError_t launch_fwd(const FwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
-// The row-pass kernel build for a shape: deterministic (fixed chunks, partials to the
-// workspace) or not (rows handed out, FP64 sums), with rstd given or recomputed (rc).
-// One translation unit per (nd, rc) pair: rmsn_bwd.cu, rmsn_bwd_rc.cu, rmsn_bwd_nd.cu,
-// rmsn_bwd_nd_rc.cu.
-const void* bwd_rows_fn(const Shape& s, bool fp32w, bool dh, bool nd, bool rc);
-const void* bwd_rows_fn_det(const Shape& s, bool fp32w, bool dh);
-const void* bwd_rows_fn_det_rc(const Shape& s, bool fp32w, bool dh);
-const void* bwd_rows_fn_nd(const Shape& s, bool fp32w, bool dh);
-const void* bwd_rows_fn_nd_rc(const Shape& s, bool fp32w, bool dh);
+// The row-pass kernel build for a shape (one program for both modes), with rstd given or
+// recomputed (rc): rmsn_bwd.cu and rmsn_bwd_rc.cu.
+const void* bwd_rows_fn(const Shape& s, bool fp32w, bool dh, bool rc);
+const void* bwd_rows_fn_rs(const Shape& s, bool fp32w, bool dh);
+const void* bwd_rows_fn_rc(const Shape& s, bool fp32w, bool dh);
+int bwd_blocks_per_sm(const Shape& s, bool fp32w, bool rc);
 
+// The row pass, either mode: a.ctl null (deterministic: fixed chunks) or the
+// non-deterministic pool's words.
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 // ctl: the non-deterministic pool words to clear once the partials are summed, or null.
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, unsigned* ctl,
                              cudaStream_t st);
 
-// Non-deterministic backward (rmsn_bwd_nd.cu): each CTA's fixed prefix of rows, then a pool
-// of tail rows taken from a counter as CTAs free up.  Its workspace is the pool's two
-// words (a 16-byte slot) followed by the P partials; the fixed-order finish adds them and
-// clears the words.  They need no initial value: the pool is open to a call only once
-// its CTA 0 has published the call's tag there.
+// The non-deterministic workspace starts with the pool's two words (a 16-byte slot),
+// followed by the P partials; the fixed-order finish adds the partials and clears the
+// words.  They need no initial value: the pool is open to a call only once its CTA 0 has
+// published the call's tag there.
 constexpr size_t kNdCtlBytes = 16;
-Shape nd_shape(const Shape& s, int H);  // + the chunk-start slots in shared memory
-int bwd_nd_blocks_per_sm(const Shape& s, bool fp32w, bool rc);
-cudaError_t launch_bwd_nd(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
 
 // Small inputs (rmsn_small.cu): the whole backward in one launch of row tasks (dx) and
 // column tasks (dw over every row in a fixed order), no workspace, for R <= kSmallMaxRows.
