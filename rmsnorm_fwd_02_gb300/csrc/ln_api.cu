@@ -20,6 +20,7 @@ constexpr size_t kLnRingTarget = 192 * 1024;  // one CTA an SM
 // At most four stages in flight a CTA (measured: the backward at H = 4096 3 % faster than
 // with six, the rest unchanged; three slowed the backward at H = 1024 and 8192).
 constexpr int kLnMaxStages = 4;
+constexpr int kTmemColumns = 512;  // tensor-memory columns of an SM
 // Deterministic backward: at most kLnDetSMs partials (the row kernels run one CTA an SM),
 // a function of the shape only.  152 is GB300's SM count: there the partition is one wave.
 constexpr int kLnDetSMs = 152;
@@ -94,11 +95,19 @@ LnShape make_shape(int H, int tensors, int vpt, int cls, bool pair) {
   if (pair && s.ntg < 32) return s;  // a pair exchanges whole warps' partials
   s.groups = budget / s.ntg;  // sub-warp groups: a whole number of warps (budget % 32 == 0)
   if (s.ntg >= 32 && s.groups > kLnMaxWarpsPerGroup) s.groups = kLnMaxWarpsPerGroup;
+  if (cls == kLnBwdTm) {
+    // the CTA's cells fit the SM's 512 tensor-memory columns (whole warps of consumers)
+    const int step = s.ntg < 32 ? 32 / s.ntg : 1;
+    while (s.groups > step && ln_bwd_tm_cols(s.groups * s.ntg / 32, vpt) > kTmemColumns)
+      s.groups -= step;
+    if (ln_bwd_tm_cols(s.groups * s.ntg / 32, vpt) > kTmemColumns) s.groups = 0;
+    if (s.groups == 0) return s;
+  }
   s.threads = s.groups * s.ntg + kLnProducerThreads;
   const size_t stage_bytes = static_cast<size_t>(tensors) * s.groups * Hc * 2;
   const int st = static_cast<int>(kLnRingTarget / stage_bytes);
   s.stages = st < 2 ? 2 : (st > kLnMaxStages ? kLnMaxStages : st);
-  s.smem = ln_shape_layout(s.stages, tensors, s.groups, H, s.ntg, pair).total;
+  s.smem = ln_shape_layout(s.stages, tensors, s.groups, H, s.ntg, pair, cls == kLnBwdTm).total;
   return s;
 }
 
@@ -170,16 +179,22 @@ cudaError_t ln_launch_pair(const void* fn, unsigned pairs, unsigned threads, siz
 
 LnShape ln_bwd_shape(int H) {
   static const int cand[][2] = {{1, kLnBwdMulti}, {2, kLnBwdMulti}, {3, kLnBwdWide}};
-  const LnShape s = pick_shape(H, 2, cand, 3);
+  LnShape s = pick_shape(H, 2, cand, 3);
+  if (H > kLnMaxH) return s;  // pair widths keep the multi and wide pair builds
   // The 4-vector class only where the others keep a single row in flight and it keeps two
   // (H in (3840, 4096]): measured 3 % faster there, and up to 2x slower at narrow widths,
   // where the other classes already keep many rows in flight with fewer registers a
-  // thread.  Pair widths (past kLnMaxH) keep the multi and wide pair builds.
-  if (H <= kLnMaxH && s.groups == 1) {
+  // thread.
+  if (s.groups == 1) {
     static const int quad[][2] = {{4, kLnBwdQuad}};
     const LnShape q = pick_shape(H, 2, quad, 1);
-    if (q.groups > 1 && q.stages >= 3) return q;
+    if (q.groups > 1 && q.stages >= 3) s = q;
   }
+  // the tensor-memory class where it keeps more rows in flight (its column sums leave the
+  // registers, so 20 warps fit)
+  static const int tmc[][2] = {{2, kLnBwdTm}, {3, kLnBwdTm}, {4, kLnBwdTm}};
+  const LnShape t = pick_shape(H, 2, tmc, 3);
+  if (t.groups > s.groups && t.stages >= 3) return t;
   return s;
 }
 

@@ -48,8 +48,8 @@ __device__ __forceinline__ void comp_add(f2& acc, f2& cmp, f2 p) {
 
 }  // namespace
 
-// Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdQuad up to
-// 256, kLnBwdWide up to
+// Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdTm up to
+// 608, kLnBwdQuad up to 256, kLnBwdWide up to
 // 352; each + the producer warp, one CTA an SM.  kPair: the CTA is one of a cluster of two
 // that share each row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp
 // row groups only); both CTAs add the row sums of both halves in the same order.
@@ -68,7 +68,11 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   const int SF = kPair ? kLnSlotFloatsPair : kLnSlotFloats;
   const size_t stage_elems = static_cast<size_t>(2) * G * Hc;  // x rows, then dy rows
   const bool red_smem = NTg >= 32;
-  const LnSmem L = ln_shape_layout(S, 2, G, H, NTg, kPair);
+  // kTm: each consumer thread's dw sums, compensations and db sums live in tensor memory
+  // and come to registers one column vector at a time; the weight sits in shared memory
+  constexpr bool kTm = kCls == kLnBwdTm;
+  const LnSmem L = ln_shape_layout(S, 2, G, H, NTg, kPair, kTm);
+  static_assert(!(kTm && kPair), "the tensor-memory class has no pair build");
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -81,6 +85,8 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 
   const int tid = threadIdx.x;
   const int ncons = G * NTg;
+  uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + L.abort_flag) + 2;
+  const uint32_t tm_ncols = kTm ? tmem_alloc_cols(ln_bwd_tm_cols(ncons / 32, VPT)) : 0u;
   const int32_t k = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : blockIdx.x;
   const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(k) * a.R) / a.P);
   const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
@@ -95,6 +101,15 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       for (int i = 0; i < kLnRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NWt));
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if constexpr (kTm) {
+    // consumer warp 0 takes the columns (one CTA an SM); the address reaches the other
+    // warps through shared memory
+    if (tid < 32) {
+      __syncwarp();
+      tmem_alloc_warp(tm_slot, tm_ncols);
+      tmem_fence_before_sync();
+    }
   }
   __syncthreads();
   if constexpr (kPair) cluster_sync_all();  // the peer's barriers exist before any remote use
@@ -160,18 +175,50 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
-  Param8<kFp32W> wv[VPT];
+  Param8<kFp32W> wv[kTm ? 1 : VPT];  // (kTm: the weight is read from shared memory)
   f2 aw[VPT][4], cw[VPT][4], ab[VPT][4];  // dw: sum and compensation; db: sum
+  unsigned char* wsm = smem + L.w;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
     // the weights of the row's column vector col0/8 + c (a pair: this CTA's half)
-    if (c < NV) load_param8<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
+    if constexpr (!kTm) {
+      if (c < NV) load_param8<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
+    }
+    if constexpr (!kTm) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      aw[v][q] = f2_splat(0.f);
-      cw[v][q] = f2_splat(0.f);
-      ab[v][q] = f2_splat(0.f);
+      for (int q = 0; q < 4; ++q) {
+        aw[v][q] = f2_splat(0.f);
+        cw[v][q] = f2_splat(0.f);
+        ab[v][q] = f2_splat(0.f);
+      }
+    }
+  }
+  // kTm: vector v's cells at columns tm + 32v: dw sums [0, 8), compensations [8, 16), db
+  // sums [16, 24)
+  uint32_t tm = 0;
+  if constexpr (kTm) {
+    // the weight into shared memory as given (16 bytes a BF16 vector, 32 an FP32 one)
+    constexpr int kWB = kFp32W ? 32 : 16;
+    for (int c = tid; c < NV; c += ncons) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.w) +
+                                                        static_cast<size_t>(c) * kWB);
+      uint4* dst = reinterpret_cast<uint4*>(wsm + static_cast<size_t>(c) * kWB);
+      dst[0] = __ldg(src);
+      if constexpr (kFp32W) dst[1] = __ldg(src + 1);
+    }
+    named_bar_sync(14, ncons);
+    __syncwarp();
+    tmem_fence_after_sync();
+    const uint32_t w = static_cast<uint32_t>(tid >> 5);
+    tm = tmem_warp_addr(*tm_slot, w, (w >> 2) * 32u * VPT);
+    float z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      tmem_st16(tm + 32u * v, z);
+      tmem_st16(tm + 32u * v + 16u, z);
     }
   }
   const float inv_h = 1.0f / static_cast<float>(H);
@@ -199,9 +246,10 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
           if (c < NV) {
             const uint4 xv = lds128(st + c * 8);
             const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
+            const Param8<kFp32W> wl = kTm ? smem_param8<kFp32W>(wsm, c) : wv[kTm ? 0 : v];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), param_pair<kFp32W>(wv[v], q));
+              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), param_pair<kFp32W>(wl, q));
               const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
               if (q & 1) {
                 gb = f2_add(gb, gw);
@@ -259,10 +307,13 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
           SGD += p.y;
         }
       }
-      if (row < r1) {
+      const bool rv = row < r1;
+      // (kTm: every thread of the warp takes part in the tensor-memory traffic, with or
+      // without a row)
+      if (kTm || rv) {
         const int base = (r0 + jj * G) & ~3;
-        const float mu = stat[s * 2 * SP + (row - base)];
-        const float rs = stat[s * 2 * SP + SP + (row - base)];
+        const float mu = rv ? stat[s * 2 * SP + (row - base)] : 0.f;
+        const float rs = rv ? stat[s * 2 * SP + SP + (row - base)] : 0.f;
         const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
         const f2 c1 = f2_splat(SG * inv_h);
         // xhat*c2 = d * (r^2 SGD / H): one product of d, so the cancelling terms meet in
@@ -270,24 +321,55 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
         const f2 ncr2 = f2_splat(-(SGD * (rs * inv_h)) * rs);
         const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
         const size_t out_row = static_cast<size_t>(row) * H + col0;
+        if constexpr (kTm) {
+          __syncwarp();
+          tmem_wait_st();  // the previous row's sums are stored before they are loaded
+        }
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
-          if (c < NV) {
+          const bool live = rv && c < NV;
+          float tw[16], tb[8];  // kTm: this vector's dw sums and compensations; db sums
+          if constexpr (kTm) {
+            tmem_ld16(tm + 32u * v, tw);
+            tmem_ld8(tm + 32u * v + 16u, tb);
+            tmem_wait_ld();
+          }
+          if (live) {
             const uint4 xv = lds128(st + c * 8);
             const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
+            const Param8<kFp32W> wl = kTm ? smem_param8<kFp32W>(wsm, c) : wv[kTm ? 0 : v];
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const f2 d2 = bf2_to_f2(u4_get(dv, q));
               const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
-              const f2 gw = f2_mul(d2, param_pair<kFp32W>(wv[v], q));
+              const f2 gw = f2_mul(d2, param_pair<kFp32W>(wl, q));
               const f2 t = f2_fma(dd, ncr2, f2_sub(gw, c1));  // g - c1 - xhat*c2, over r
               o[q] = f2_to_bf2(f2_mul(t, rs2));
-              comp_add(aw[v][q], cw[v][q], f2_mul(f2_mul(d2, dd), rs2));  // dy * xhat
-              ab[v][q] = f2_add(ab[v][q], d2);                             // dy
+              const f2 p = f2_mul(f2_mul(d2, dd), rs2);  // dy * xhat
+              if constexpr (kTm) {
+                f2 av = f2_make(tw[2 * q], tw[2 * q + 1]);
+                f2 cv = f2_make(tw[8 + 2 * q], tw[9 + 2 * q]);
+                comp_add(av, cv, p);
+                const f2 bv2 = f2_add(f2_make(tb[2 * q], tb[2 * q + 1]), d2);  // dy
+                tw[2 * q] = f2_lo(av);
+                tw[2 * q + 1] = f2_hi(av);
+                tw[8 + 2 * q] = f2_lo(cv);
+                tw[9 + 2 * q] = f2_hi(cv);
+                tb[2 * q] = f2_lo(bv2);
+                tb[2 * q + 1] = f2_hi(bv2);
+              } else {
+                comp_add(aw[v][q], cw[v][q], p);
+                ab[v][q] = f2_add(ab[v][q], d2);  // dy
+              }
             }
             stg128(a.dx + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
+          }
+          if constexpr (kTm) {
+            __syncwarp();
+            tmem_st16(tm + 32u * v, tw);
+            tmem_st8(tm + 32u * v + 16u, tb);
           }
         }
       }
@@ -300,6 +382,33 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     if (++s_cur == S) {
       s_cur = 0;
       ph ^= 1u;
+    }
+  }
+
+  if constexpr (kTm) {
+    // the sums come back to registers, and warp 0 frees the columns once every consumer
+    // has loaded its own
+    __syncwarp();
+    tmem_wait_st();
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      float tw[16], tb[8];
+      tmem_ld16(tm + 32u * v, tw);
+      tmem_ld8(tm + 32u * v + 16u, tb);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        aw[v][q] = f2_make(tw[2 * q], tw[2 * q + 1]);
+        cw[v][q] = f2_make(tw[8 + 2 * q], tw[9 + 2 * q]);
+        ab[v][q] = f2_make(tb[2 * q], tb[2 * q + 1]);
+      }
+    }
+    tmem_fence_before_sync();
+    named_bar_sync(13, ncons);
+    if (tid < 32) {
+      __syncwarp();
+      tmem_fence_after_sync();
+      tmem_dealloc_warp(*tm_slot, tm_ncols);
     }
   }
 
@@ -458,8 +567,8 @@ const void* ln_bwd_ptr_v(bool fp32w) {
                : reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, false, kPair>);
 }
 
-// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3, kLnBwdQuad for 4;
-// the pair builds
+// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3, kLnBwdQuad for 4,
+// kLnBwdTm for 2, 3 and 4; the pair builds
 // (half-rows of 4100..8192 columns) for 2 (multi) and 3 (wide).
 const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
   if (s.pair)
@@ -467,6 +576,10 @@ const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
                                : ln_bwd_ptr_v<2, kLnBwdMulti, true>(fp32w);
   if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide, false>(fp32w);
   if (s.cls == kLnBwdQuad) return ln_bwd_ptr_v<4, kLnBwdQuad, false>(fp32w);
+  if (s.cls == kLnBwdTm)
+    return s.vpt == 2 ? ln_bwd_ptr_v<2, kLnBwdTm, false>(fp32w)
+                      : (s.vpt == 3 ? ln_bwd_ptr_v<3, kLnBwdTm, false>(fp32w)
+                                    : ln_bwd_ptr_v<4, kLnBwdTm, false>(fp32w));
   return s.vpt == 1 ? ln_bwd_ptr_v<1, kLnBwdMulti, false>(fp32w)
                     : ln_bwd_ptr_v<2, kLnBwdMulti, false>(fp32w);
 }

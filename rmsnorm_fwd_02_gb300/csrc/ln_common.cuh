@@ -10,6 +10,7 @@
 #pragma once
 
 #include "rmsn_common.cuh"
+#include "rmsn_tmem.cuh"
 
 namespace lnorm {
 
@@ -112,6 +113,21 @@ __device__ __forceinline__ void load_param8(const void* p, int c, Param8<kFp32>&
   }
 }
 
+// Column vector c of a parameter array copied to shared memory as given (16 bytes a BF16
+// vector, 32 an FP32 one).
+template <bool kFp32>
+__device__ __forceinline__ Param8<kFp32> smem_param8(const unsigned char* p, int c) {
+  Param8<kFp32> out;
+  if constexpr (kFp32) {
+    const float4* q = reinterpret_cast<const float4*>(p) + 2 * c;
+    out.a = q[0];
+    out.b = q[1];
+  } else {
+    out.u = reinterpret_cast<const uint4*>(p)[c];
+  }
+  return out;
+}
+
 // Elements 2q and 2q+1 of a column vector's parameters, as an FP32 pair (q a constant
 // after unrolling).
 template <bool kFp32>
@@ -123,6 +139,22 @@ __device__ __forceinline__ f2 param_pair(const Param8<kFp32>& p, int q) {
   } else {
     return bf2_to_f2(u4_get(p.u, q));
   }
+}
+
+// 8 consecutive tensor-memory columns of this thread's lane <-> r[0..7] (the 32x32b
+// shape, as rmsn_tmem.cuh's 16-column forms; whole warp, .sync.aligned).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+                 "=f"(r[6]), "=f"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"r"(taddr), "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]),
+               "f"(r[6]), "f"(r[7])
+               : "memory");
 }
 
 }  // namespace lnorm

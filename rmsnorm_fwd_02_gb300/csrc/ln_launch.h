@@ -30,9 +30,22 @@ constexpr int kLnMaxWarpsPerGroup = 16;
 //  kLnBwdQuad   backward with 4-vector threads, up to 256 consumers (9 warps: 168
 //               registers, a few spilled): two 128-thread rows in flight at H = 4096,
 //               where the other classes fit one
-enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3, kLnBwdQuad = 4 };
+//  kLnBwdTm     backward with each thread's dw sums, their compensations and the db sums
+//               in tensor memory (32 columns of its lane a column vector), up to 608
+//               consumers (20 warps with the producer: 96 registers); single CTAs only
+enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3, kLnBwdQuad = 4,
+       kLnBwdTm = 5 };
 constexpr int ln_consumers(int cls) {
-  return cls == kLnBwdWide ? 352 : ((cls == kLnFwdPair || cls == kLnBwdQuad) ? 256 : 480);
+  return cls == kLnBwdWide ? 352
+                           : ((cls == kLnFwdPair || cls == kLnBwdQuad)
+                                  ? 256
+                                  : (cls == kLnBwdTm ? 608 : 480));
+}
+// Tensor-memory columns a kLnBwdTm CTA of `cons_warps` consumer warps uses: 32 a column
+// vector a thread (dw sums [0, 8), their compensations [8, 16), db sums [16, 24)), the
+// warps sharing a lane quadrant side by side.
+__host__ __device__ constexpr int ln_bwd_tm_cols(int cons_warps, int vpt) {
+  return ((cons_warps + 3) / 4) * 32 * vpt;
 }
 constexpr int ln_max_threads(int cls) { return ln_consumers(cls) + kLnProducerThreads; }
 
@@ -62,14 +75,18 @@ constexpr int kLnWtab = 32;  // entries per row of the forward's warp-merge tabl
 //          first element, the shift both CTAs use)
 //   wtab   [3][kLnWtab] FP32 per-warp counts, prefix counts and combine factors of the
 //          forward's variance merge
-//   abort  the CTA's abort flag of the bounded waits
+//   w      [Hc] the weight as given (BF16 or FP32; room for FP32), for the backward builds
+//          that keep it in shared memory (kLnBwdTm)
+//   abort  the CTA's abort flag of the bounded waits (word 0); word 2: the tensor-memory
+//          address of the kLnBwdTm builds
 struct LnSmem {
-  size_t full, empty, redb, slots, stat, head, wtab, abort_flag, total;
+  size_t full, empty, redb, slots, stat, head, wtab, w, abort_flag, total;
 };
 
 __host__ __device__ inline LnSmem ln_smem_layout(int stages, int tensors, int groups, int Hc,
                                                  int red_groups, int stat_rows,
-                                                 int slot_floats, int head_rows) {
+                                                 int slot_floats, int head_rows,
+                                                 int w_floats = 0) {
   LnSmem L;
   size_t off = static_cast<size_t>(stages) * tensors * groups * Hc * 2;  // multiple of 16
   L.full = off;
@@ -87,6 +104,8 @@ __host__ __device__ inline LnSmem ln_smem_layout(int stages, int tensors, int gr
   off += 16 * static_cast<size_t>(stages) * head_rows;
   L.wtab = off;  // 16-byte aligned
   off += 4 * 3 * kLnWtab;
+  L.w = off;  // 16-byte aligned
+  off += 4 * static_cast<size_t>(w_floats);
   L.abort_flag = off;
   off += 16;
   L.total = off;
@@ -101,7 +120,7 @@ struct LnShape {
   int tensors;  // BF16 tensors staged per row (1 forward, 2 backward)
   int threads;  // groups * ntg + producer warp
   size_t smem;  // dynamic shared memory bytes
-  int cls;      // kLnFwd, kLnBwdMulti, kLnBwdWide, kLnFwdPair or kLnBwdQuad
+  int cls;      // kLnFwd, kLnBwdMulti, kLnBwdWide, kLnFwdPair, kLnBwdQuad or kLnBwdTm
   int pair;     // 1: a CTA pair per row chunk, each CTA owning half the columns
 };
 
@@ -136,11 +155,11 @@ LnShape ln_bwd_shape(int H);
 
 // Shared memory of a shape (host and kernels agree through ln_smem_layout).
 __host__ __device__ inline LnSmem ln_shape_layout(int stages, int tensors, int groups, int H,
-                                                  int ntg, bool pair) {
+                                                  int ntg, bool pair, bool w_smem = false) {
   const int Hc = pair ? H / 2 : H;
   return ln_smem_layout(stages, tensors, groups, Hc, ntg >= 32 ? groups : 0,
                         tensors == 2 ? groups : 0, pair ? kLnSlotFloatsPair : kLnSlotFloats,
-                        pair && tensors == 1 ? groups : 0);
+                        pair && tensors == 1 ? groups : 0, w_smem ? Hc : 0);
 }
 
 cudaError_t ln_launch_fwd(const LnFwdArgs& a, const LnShape& s, bool fp32w, cudaStream_t st);

@@ -126,10 +126,18 @@ def test_layernorm_plan_fits_its_kernel_build_at_every_width(lib, op):
                 assert p["cls"] == 0 and p["vpt"] in (1, 2, 4), ctx
                 assert p["class_max_threads"] == 512, ctx
         else:
-            assert (p["cls"], p["vpt"]) in ((1, 1), (1, 2), (2, 3), (4, 4)), ctx
-            assert p["class_max_threads"] == {1: 512, 2: 384, 4: 288}[p["cls"]], ctx
+            assert (p["cls"], p["vpt"]) in ((1, 1), (1, 2), (2, 3), (4, 4), (5, 2), (5, 3),
+                                            (5, 4)), ctx
+            assert p["class_max_threads"] == {1: 512, 2: 384, 4: 288, 5: 640}[p["cls"]], ctx
             if pair:
-                assert p["cls"] != 4, ctx              # no pair build of the 4-vector class
+                assert p["cls"] not in (4, 5), ctx     # no pair build of these classes
+            if p["cls"] == 5:
+                # the tensor-memory class: whole consumer warps, 32 columns of a thread's
+                # lane a column vector, four warps a lane quadrant, within 512 columns
+                cons = p["threads"] - 32
+                assert cons % 32 == 0, ctx
+                assert -(-(cons // 32) // 4) * 32 * p["vpt"] <= 512, ctx
+                assert p["stages"] >= 3, ctx
             ring = p["stages"] * tensors * p["groups"] * Hc * 2
             assert ring >= 8 * p["groups"] * Hc, ctx   # the end-of-kernel combine buffer
 
