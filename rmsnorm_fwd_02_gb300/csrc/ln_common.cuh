@@ -113,6 +113,21 @@ __device__ __forceinline__ void load_param8(const void* p, int c, Param8<kFp32>&
   }
 }
 
+// x - k for the two BF16 of word u, as an FP32 pair, each rounded once (the same bits as
+// converting x and subtracting in FP32): the mixed-precision fma x*1 + (-k), which reads
+// the BF16 halves of the word with no conversion.  nk = -k.
+__device__ __forceinline__ f2 bf2_minus(uint32_t u, float nk) {
+  f2 r;
+  asm("{\n\t.reg .b16 a0, a1, one;\n\t.reg .f32 p0, p1;\n\t"
+      "mov.b32 {a0, a1}, %1;\n\tmov.b16 one, 0x3F80;\n\t"
+      "fma.rn.f32.bf16 p0, a0, one, %2;\n\t"
+      "fma.rn.f32.bf16 p1, a1, one, %2;\n\t"
+      "mov.b64 %0, {p0, p1};\n\t}"
+      : "=l"(r.v)
+      : "r"(u), "f"(nk));
+  return r;
+}
+
 // Column vector c of a parameter array copied to shared memory as given (16 bytes a BF16
 // vector, 32 an FP32 one).
 template <bool kFp32>

@@ -77,8 +77,8 @@ __device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, floa
 
 }  // namespace
 
-// One build per vector count and parameter dtype; one CTA an SM, up to 480 consumers +
-// the producer warp (16 warps: 128 registers a thread).  kPair (class kLnFwdPair, up to
+// One build per vector count and parameter dtype; one CTA an SM, up to 608 consumers +
+// the producer warp (20 warps: 96 registers a thread).  kPair (class kLnFwdPair, up to
 // 256 consumers, 4-vector threads): the CTA is one of a cluster of two that share each
 // row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp row groups only);
 // the two CTAs merge both halves' warp statistics in the same order, so they compute the
@@ -189,15 +189,29 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
   const int g = tid / NTg;
   const int lt = tid - g * NTg;
   const int wg = lt >> 5, lane = tid & 31;
-  Param8<kFp32W> wv[VPT], bv[VPT];
+  // w and b of this CTA's columns in shared memory as FP32, four planes of float4 (w
+  // columns 0-3 and 4-7 of every vector, then b's), read per use: conflict-free, and no
+  // registers held across rows
+  float4* wb = reinterpret_cast<float4*>(smem + L.w);
+  for (int c = tid; c < NV; c += ncons) {
+    Param8<kFp32W> pw, pb;
+    load_param8<kFp32W>(a.w, (col0 >> 3) + c, pw);
+    load_param8<kFp32W>(a.b, (col0 >> 3) + c, pb);
+    const f2 w0 = param_pair<kFp32W>(pw, 0), w1 = param_pair<kFp32W>(pw, 1);
+    const f2 w2 = param_pair<kFp32W>(pw, 2), w3 = param_pair<kFp32W>(pw, 3);
+    const f2 b0 = param_pair<kFp32W>(pb, 0), b1 = param_pair<kFp32W>(pb, 1);
+    const f2 b2 = param_pair<kFp32W>(pb, 2), b3 = param_pair<kFp32W>(pb, 3);
+    wb[c] = make_float4(f2_lo(w0), f2_hi(w0), f2_lo(w1), f2_hi(w1));
+    wb[NV + c] = make_float4(f2_lo(w2), f2_hi(w2), f2_lo(w3), f2_hi(w3));
+    wb[2 * NV + c] = make_float4(f2_lo(b0), f2_hi(b0), f2_lo(b1), f2_hi(b1));
+    wb[3 * NV + c] = make_float4(f2_lo(b2), f2_hi(b2), f2_lo(b3), f2_hi(b3));
+  }
+  named_bar_sync(14, ncons);
   int nvec = 0;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = lt + v * NTg;
     if (c < NV) {
-      // the parameters of the row's column vector col0/8 + c (a pair: this CTA's half)
-      load_param8<kFp32W>(a.w, (col0 >> 3) + c, wv[v]);
-      load_param8<kFp32W>(a.b, (col0 >> 3) + c, bv[v]);
       ++nvec;
     }
   }
@@ -225,7 +239,8 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
         const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
         // statistics of x - K, K the row's first element (one value for the whole group,
         // and for both CTAs of a pair)
-        const f2 K2 = f2_splat(kPair ? head_shift(&head[s * G + g]) : row_shift(xs));
+        // (x - K: the mixed-precision fma reads the staged BF16 words directly)
+        const float nK = -(kPair ? head_shift(&head[s * G + g]) : row_shift(xs));
         uint4 xr[VPT];
         f2 s0 = f2_splat(0.f), s1 = f2_splat(0.f);
 #pragma unroll
@@ -234,10 +249,10 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
           xr[v] = make_uint4(0u, 0u, 0u, 0u);
           if (c < NV) {
             xr[v] = lds128(xs + c * 8);
-            s0 = f2_add(s0, f2_sub(bf2_to_f2(xr[v].x), K2));
-            s1 = f2_add(s1, f2_sub(bf2_to_f2(xr[v].y), K2));
-            s0 = f2_add(s0, f2_sub(bf2_to_f2(xr[v].z), K2));
-            s1 = f2_add(s1, f2_sub(bf2_to_f2(xr[v].w), K2));
+            s0 = f2_add(s0, bf2_minus(xr[v].x, nK));
+            s1 = f2_add(s1, bf2_minus(xr[v].y, nK));
+            s0 = f2_add(s0, bf2_minus(xr[v].z, nK));
+            s1 = f2_add(s1, bf2_minus(xr[v].w, nK));
           }
         }
         const f2 sp = f2_add(s0, s1);
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
           if (c < NV) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const f2 e = f2_sub(f2_sub(bf2_to_f2(u4_get(xr[v], q)), K2), m2);
+              const f2 e = f2_sub(bf2_minus(u4_get(xr[v], q), nK), m2);
               if (q & 1)
                 q1a = f2_fma(e, e, q1a);
               else
@@ -308,18 +323,23 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
       if (valid) {
         const float mean = __fadd_rn(K, __fdiv_rn(Sg, hf));
         const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(Mg, hf), a.eps));
-        const f2 mu2 = f2_splat(mean), rs2 = f2_splat(rs);
+        const float nmean = -mean;
+        const f2 rs2 = f2_splat(rs);
         const size_t out_row = static_cast<size_t>(row) * H + col0;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
           if (c < NV) {
+            const float4 wa = wb[c], wc = wb[NV + c], ba = wb[2 * NV + c], bc = wb[3 * NV + c];
+            const f2 wq[4] = {f2_make(wa.x, wa.y), f2_make(wa.z, wa.w), f2_make(wc.x, wc.y),
+                              f2_make(wc.z, wc.w)};
+            const f2 bq[4] = {f2_make(ba.x, ba.y), f2_make(ba.z, ba.w), f2_make(bc.x, bc.y),
+                              f2_make(bc.z, bc.w)};
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const f2 xh = f2_mul(f2_sub(bf2_to_f2(u4_get(hv[v], q)), mu2), rs2);
-              o[q] = f2_to_bf2(f2_fma(xh, param_pair<kFp32W>(wv[v], q),
-                                      param_pair<kFp32W>(bv[v], q)));
+              const f2 xh = f2_mul(bf2_minus(u4_get(hv[v], q), nmean), rs2);
+              o[q] = f2_to_bf2(f2_fma(xh, wq[q], bq[q]));
             }
             stg128(a.y + out_row + c * 8, make_uint4(o[0], o[1], o[2], o[3]));
           }

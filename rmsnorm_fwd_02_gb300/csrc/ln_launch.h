@@ -20,7 +20,8 @@ constexpr int kLnMaxWarpsPerGroup = 16;
 
 // Shape classes, each its own kernel build (and a CTA-pair build of each for widths past
 // kLnMaxH) (launch bounds = consumers + producer warp):
-//  kLnFwd       forward, up to 480 consumers, one CTA an SM (16 warps: 128 registers)
+//  kLnFwd       forward, up to 608 consumers, one CTA an SM (20 warps: 96 registers, which
+//               the builds fit with w and b in shared memory)
 //  kLnBwdMulti  backward with 1- or 2-vector threads, up to 480 consumers (128 registers)
 //  kLnBwdWide   backward with 3-vector threads, up to 352 consumers (12 warps, three on a
 //               scheduler partition: 168 registers), for rows past 480 2-vector threads;
@@ -39,7 +40,7 @@ constexpr int ln_consumers(int cls) {
   return cls == kLnBwdWide ? 352
                            : ((cls == kLnFwdPair || cls == kLnBwdQuad)
                                   ? 256
-                                  : (cls == kLnBwdTm ? 608 : 480));
+                                  : ((cls == kLnBwdTm || cls == kLnFwd) ? 608 : 480));
 }
 // Tensor-memory columns a kLnBwdTm CTA of `cons_warps` consumer warps uses: 32 a column
 // vector a thread (dw sums [0, 8), their compensations [8, 16), db sums [16, 24)), the
@@ -75,8 +76,9 @@ constexpr int kLnWtab = 32;  // entries per row of the forward's warp-merge tabl
 //          first element, the shift both CTAs use)
 //   wtab   [3][kLnWtab] FP32 per-warp counts, prefix counts and combine factors of the
 //          forward's variance merge
-//   w      [Hc] the weight as given (BF16 or FP32; room for FP32), for the backward builds
-//          that keep it in shared memory (kLnBwdTm)
+//   w      the parameters in shared memory: the forward's w and b as FP32 (four planes of
+//          float4: w columns 0-3, w 4-7, b 0-3, b 4-7 of every vector; 2*Hc floats), the
+//          kLnBwdTm backward's w as given (BF16 or FP32; room for Hc floats)
 //   abort  the CTA's abort flag of the bounded waits (word 0); word 2: the tensor-memory
 //          address of the kLnBwdTm builds
 struct LnSmem {
@@ -155,11 +157,12 @@ LnShape ln_bwd_shape(int H);
 
 // Shared memory of a shape (host and kernels agree through ln_smem_layout).
 __host__ __device__ inline LnSmem ln_shape_layout(int stages, int tensors, int groups, int H,
-                                                  int ntg, bool pair, bool w_smem = false) {
+                                                  int ntg, bool pair, bool bwd_w_smem = false) {
   const int Hc = pair ? H / 2 : H;
+  const int w_floats = tensors == 1 ? 2 * Hc : (bwd_w_smem ? Hc : 0);
   return ln_smem_layout(stages, tensors, groups, Hc, ntg >= 32 ? groups : 0,
                         tensors == 2 ? groups : 0, pair ? kLnSlotFloatsPair : kLnSlotFloats,
-                        pair && tensors == 1 ? groups : 0, w_smem ? Hc : 0);
+                        pair && tensors == 1 ? groups : 0, w_floats);
 }
 
 cudaError_t ln_launch_fwd(const LnFwdArgs& a, const LnShape& s, bool fp32w, cudaStream_t st);
