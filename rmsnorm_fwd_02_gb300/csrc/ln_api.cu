@@ -179,17 +179,8 @@ cudaError_t ln_launch_pair(const void* fn, unsigned pairs, unsigned threads, siz
 
 LnShape ln_bwd_shape(int H) {
   static const int cand[][2] = {{1, kLnBwdMulti}, {2, kLnBwdMulti}, {3, kLnBwdWide}};
-  LnShape s = pick_shape(H, 2, cand, 3);
+  const LnShape s = pick_shape(H, 2, cand, 3);
   if (H > kLnMaxH) return s;  // pair widths keep the multi and wide pair builds
-  // The 4-vector class only where the others keep a single row in flight and it keeps two
-  // (H in (3840, 4096]): measured 3 % faster there, and up to 2x slower at narrow widths,
-  // where the other classes already keep many rows in flight with fewer registers a
-  // thread.
-  if (s.groups == 1) {
-    static const int quad[][2] = {{4, kLnBwdQuad}};
-    const LnShape q = pick_shape(H, 2, quad, 1);
-    if (q.groups > 1 && q.stages >= 3) s = q;
-  }
   // the tensor-memory class where it keeps more rows in flight (its column sums leave the
   // registers, so 20 warps fit)
   static const int tmc[][2] = {{2, kLnBwdTm}, {3, kLnBwdTm}, {4, kLnBwdTm}};

@@ -49,7 +49,7 @@ __device__ __forceinline__ void comp_add(f2& acc, f2& cmp, f2 p) {
 }  // namespace
 
 // Launch bounds per class (ln_launch.h): kLnBwdMulti up to 480 consumers, kLnBwdTm up to
-// 608, kLnBwdQuad up to 256, kLnBwdWide up to
+// 608, kLnBwdWide up to
 // 352; each + the producer warp, one CTA an SM.  kPair: the CTA is one of a cluster of two
 // that share each row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp
 // row groups only); both CTAs add the row sums of both halves in the same order.
@@ -198,14 +198,16 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   // sums [16, 24)
   uint32_t tm = 0;
   if constexpr (kTm) {
-    // the weight into shared memory as given (16 bytes a BF16 vector, 32 an FP32 one)
-    constexpr int kWB = kFp32W ? 32 : 16;
+    // the weight into shared memory as FP32, two planes of float4 (columns 0-3 and 4-7
+    // of every vector): conflict-free reads, no conversion per use
+    float4* wp = reinterpret_cast<float4*>(wsm);
     for (int c = tid; c < NV; c += ncons) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.w) +
-                                                        static_cast<size_t>(c) * kWB);
-      uint4* dst = reinterpret_cast<uint4*>(wsm + static_cast<size_t>(c) * kWB);
-      dst[0] = __ldg(src);
-      if constexpr (kFp32W) dst[1] = __ldg(src + 1);
+      Param8<kFp32W> pw;
+      load_param8<kFp32W>(a.w, c, pw);
+      const f2 w0 = param_pair<kFp32W>(pw, 0), w1 = param_pair<kFp32W>(pw, 1);
+      const f2 w2 = param_pair<kFp32W>(pw, 2), w3 = param_pair<kFp32W>(pw, 3);
+      wp[c] = make_float4(f2_lo(w0), f2_hi(w0), f2_lo(w1), f2_hi(w1));
+      wp[NV + c] = make_float4(f2_lo(w2), f2_hi(w2), f2_lo(w3), f2_hi(w3));
     }
     named_bar_sync(14, ncons);
     __syncwarp();
@@ -221,6 +223,21 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       tmem_st16(tm + 32u * v + 16u, z);
     }
   }
+  // this thread's weight pairs for column vector c (its v-th): FP32 planes in shared
+  // memory (kTm) or the registers
+  auto wvec = [&](int v, int c, f2 (&wq)[4]) {
+    if constexpr (kTm) {
+      const float4 lo = reinterpret_cast<const float4*>(wsm)[c];
+      const float4 hi = reinterpret_cast<const float4*>(wsm)[NV + c];
+      wq[0] = f2_make(lo.x, lo.y);
+      wq[1] = f2_make(lo.z, lo.w);
+      wq[2] = f2_make(hi.x, hi.y);
+      wq[3] = f2_make(hi.z, hi.w);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) wq[q] = param_pair<kFp32W>(wv[v], q);
+    }
+  };
   const float inv_h = 1.0f / static_cast<float>(H);
   const int g0 = red_smem ? g : (tid & ~31) / NTg;
   const int32_t ng = (r1 - r0 > g0) ? (r1 - r0 - g0 + G - 1) / G : 0;
@@ -237,8 +254,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
       f2 ga = f2_splat(0.f), gb = f2_splat(0.f), da = f2_splat(0.f), db2 = f2_splat(0.f);
       if (row < r1) {
-        const float mu = stat[s * 2 * SP + (row - ((r0 + j * G) & ~3))];
-        const f2 mu2 = f2_splat(mu);
+        const float nmu = -stat[s * 2 * SP + (row - ((r0 + j * G) & ~3))];
         const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -246,11 +262,12 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
           if (c < NV) {
             const uint4 xv = lds128(st + c * 8);
             const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
-            const Param8<kFp32W> wl = kTm ? smem_param8<kFp32W>(wsm, c) : wv[kTm ? 0 : v];
+            f2 wq[4];
+            wvec(v, c, wq);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), param_pair<kFp32W>(wl, q));
-              const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
+              const f2 gw = f2_mul(bf2_to_f2(u4_get(dv, q)), wq[q]);
+              const f2 dd = bf2_minus(u4_get(xv, q), nmu);
               if (q & 1) {
                 gb = f2_add(gb, gw);
                 db2 = f2_fma(gw, dd, db2);
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
         const int base = (r0 + jj * G) & ~3;
         const float mu = rv ? stat[s * 2 * SP + (row - base)] : 0.f;
         const float rs = rv ? stat[s * 2 * SP + SP + (row - base)] : 0.f;
-        const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
+        const f2 rs2 = f2_splat(rs);
         const f2 c1 = f2_splat(SG * inv_h);
         // xhat*c2 = d * (r^2 SGD / H): one product of d, so the cancelling terms meet in
         // a single fma
@@ -338,13 +355,14 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
           if (live) {
             const uint4 xv = lds128(st + c * 8);
             const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
-            const Param8<kFp32W> wl = kTm ? smem_param8<kFp32W>(wsm, c) : wv[kTm ? 0 : v];
+            f2 wq[4];
+            wvec(v, c, wq);
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const f2 d2 = bf2_to_f2(u4_get(dv, q));
-              const f2 dd = f2_sub(bf2_to_f2(u4_get(xv, q)), mu2);
-              const f2 gw = f2_mul(d2, param_pair<kFp32W>(wl, q));
+              const f2 dd = bf2_minus(u4_get(xv, q), -mu);
+              const f2 gw = f2_mul(d2, wq[q]);
               const f2 t = f2_fma(dd, ncr2, f2_sub(gw, c1));  // g - c1 - xhat*c2, over r
               o[q] = f2_to_bf2(f2_mul(t, rs2));
               const f2 p = f2_mul(f2_mul(d2, dd), rs2);  // dy * xhat
@@ -385,31 +403,54 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     }
   }
 
-  if constexpr (kTm) {
-    // the sums come back to registers, and warp 0 frees the columns once every consumer
-    // has loaded its own
-    __syncwarp();
-    tmem_wait_st();
+  // A column vector's running sums of one quantity (0: dw, with its compensation; 1: db),
+  // from the registers or (kTm) from tensor memory: every thread of the warp calls it, so
+  // the warp-wide tcgen05 loads stay converged.
+  auto sums = [&](int v, int qty, f2 (&acc)[4], f2 (&cmp)[4]) {
+    if constexpr (kTm) {
+      __syncwarp();
+      if (qty == 0) {
+        float t[16];
+        tmem_ld16(tm + 32u * v, t);
+        tmem_wait_ld();
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      float tw[16], tb[8];
-      tmem_ld16(tm + 32u * v, tw);
-      tmem_ld8(tm + 32u * v + 16u, tb);
-      tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) {
+          acc[q] = f2_make(t[2 * q], t[2 * q + 1]);
+          cmp[q] = f2_make(t[8 + 2 * q], t[9 + 2 * q]);
+        }
+      } else {
+        float t[8];
+        tmem_ld8(tm + 32u * v + 16u, t);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[q] = f2_make(t[2 * q], t[2 * q + 1]);
+          cmp[q] = f2_splat(0.f);
+        }
+      }
+    } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        aw[v][q] = f2_make(tw[2 * q], tw[2 * q + 1]);
-        cw[v][q] = f2_make(tw[8 + 2 * q], tw[9 + 2 * q]);
-        ab[v][q] = f2_make(tb[2 * q], tb[2 * q + 1]);
+        acc[q] = qty == 0 ? aw[v][q] : ab[v][q];
+        cmp[q] = qty == 0 ? cw[v][q] : f2_splat(0.f);
       }
     }
-    tmem_fence_before_sync();
-    named_bar_sync(13, ncons);
-    if (tid < 32) {
-      __syncwarp();
-      tmem_fence_after_sync();
-      tmem_dealloc_warp(*tm_slot, tm_ncols);
+  };
+  // kTm: warp 0 frees the columns once every consumer has read its own
+  auto release_tmem = [&]() {
+    if constexpr (kTm) {
+      tmem_fence_before_sync();
+      named_bar_sync(13, ncons);
+      if (tid < 32) {
+        __syncwarp();
+        tmem_fence_after_sync();
+        tmem_dealloc_warp(*tm_slot, tm_ncols);
+      }
     }
+  };
+  if constexpr (kTm) {
+    __syncwarp();
+    tmem_wait_st();
   }
 
   // ---- this CTA's partials: per column (hi, lo) with hi + lo == acc + cmp exactly ----
@@ -419,16 +460,16 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
-      if (c < NV) {
 #pragma unroll
-        for (int qty = 0; qty < 2; ++qty) {
+      for (int qty = 0; qty < 2; ++qty) {
+        f2 acc[4], cmp[4];
+        sums(v, qty, acc, cmp);
+        if (c < NV) {
           f2 hi[4], lo[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const f2 acc = qty == 0 ? aw[v][q] : ab[v][q];
-            const f2 cmp = qty == 0 ? cw[v][q] : f2_splat(0.f);
-            hi[q] = f2_add(acc, cmp);
-            lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
+            hi[q] = f2_add(acc[q], cmp[q]);
+            lo[q] = f2_sub(cmp[q], f2_sub(hi[q], acc[q]));
           }
           ulonglong2* ph = reinterpret_cast<ulonglong2*>(part + qty * H + c * 8);
           ulonglong2* pl = reinterpret_cast<ulonglong2*>(part + 2 * H + qty * H + c * 8);
@@ -439,6 +480,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
         }
       }
     }
+    release_tmem();
     if constexpr (kPair) {
       __syncwarp();
       cluster_sync_all();
@@ -457,14 +499,14 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = lt + v * NTg;
+      f2 acc[4], cmp[4];
+      sums(v, qty, acc, cmp);
       if (c < NV) {
         f2 hi[4], lo[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const f2 acc = qty == 0 ? aw[v][q] : ab[v][q];
-          const f2 cmp = qty == 0 ? cw[v][q] : f2_splat(0.f);
-          hi[q] = f2_add(acc, cmp);
-          lo[q] = f2_sub(cmp, f2_sub(hi[q], acc));
+          hi[q] = f2_add(acc[q], cmp[q]);
+          lo[q] = f2_sub(cmp[q], f2_sub(hi[q], acc[q]));
         }
         ulonglong2* ph = reinterpret_cast<ulonglong2*>(cbuf + (2 * g) * Hc);
         ulonglong2* pl = reinterpret_cast<ulonglong2*>(cbuf + (2 * g + 1) * Hc);
@@ -489,6 +531,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     }
     named_bar_sync(15, ncons);  // cbuf is rewritten by the next quantity
   }
+  release_tmem();
   if constexpr (kPair) {
     __syncwarp();
     cluster_sync_all();
@@ -567,15 +610,14 @@ const void* ln_bwd_ptr_v(bool fp32w) {
                : reinterpret_cast<const void*>(&ln_bwd_rows_kernel<VPT, kCls, false, kPair>);
 }
 
-// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3, kLnBwdQuad for 4,
-// kLnBwdTm for 2, 3 and 4; the pair builds
+// kLnBwdMulti is built for 1 and 2 vectors a thread, kLnBwdWide for 3, kLnBwdTm for 2, 3
+// and 4; the pair builds
 // (half-rows of 4100..8192 columns) for 2 (multi) and 3 (wide).
 const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
   if (s.pair)
     return s.cls == kLnBwdWide ? ln_bwd_ptr_v<3, kLnBwdWide, true>(fp32w)
                                : ln_bwd_ptr_v<2, kLnBwdMulti, true>(fp32w);
   if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide, false>(fp32w);
-  if (s.cls == kLnBwdQuad) return ln_bwd_ptr_v<4, kLnBwdQuad, false>(fp32w);
   if (s.cls == kLnBwdTm)
     return s.vpt == 2 ? ln_bwd_ptr_v<2, kLnBwdTm, false>(fp32w)
                       : (s.vpt == 3 ? ln_bwd_ptr_v<3, kLnBwdTm, false>(fp32w)

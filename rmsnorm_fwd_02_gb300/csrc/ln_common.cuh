@@ -128,21 +128,6 @@ __device__ __forceinline__ f2 bf2_minus(uint32_t u, float nk) {
   return r;
 }
 
-// Column vector c of a parameter array copied to shared memory as given (16 bytes a BF16
-// vector, 32 an FP32 one).
-template <bool kFp32>
-__device__ __forceinline__ Param8<kFp32> smem_param8(const unsigned char* p, int c) {
-  Param8<kFp32> out;
-  if constexpr (kFp32) {
-    const float4* q = reinterpret_cast<const float4*>(p) + 2 * c;
-    out.a = q[0];
-    out.b = q[1];
-  } else {
-    out.u = reinterpret_cast<const uint4*>(p)[c];
-  }
-  return out;
-}
-
 // Elements 2q and 2q+1 of a column vector's parameters, as an FP32 pair (q a constant
 // after unrolling).
 template <bool kFp32>

@@ -11,8 +11,10 @@
 // deviations from their own mean (two passes over its registers), and the threads'
 // (count n, S, M) triples merge pairwise by Chan, Golub and LeVeque's update (1979):
 //   S = S_a + S_b,   M = M_a + M_b + (n_b S_a - n_a S_b)^2 / (n_a n_b (n_a + n_b)).
-// Then mean = K + S/H and var = M/H.  Unlike sum(x^2) - H*mean^2 this keeps the variance's
-// accuracy when |mean| >> std; unlike a two-pass variance over the whole row it needs one
+// Then mean = K + S*(1/H) and var = M*(1/H) (1/H correctly rounded: exact for H a power
+// of 2, else one more rounding than a division).  Unlike sum(x^2) - H*mean^2 this keeps
+// the variance's accuracy when |mean| >> std; unlike a two-pass variance over the whole
+// row it needs one
 // reduction, so the row pipeline is the RMSNorm forward's: the producer warp stages rows
 // into the ring, and split-phase rows let the reduction of row j overlap phase B
 // (normalize and store) of row j-1.
@@ -50,29 +52,48 @@ __device__ __forceinline__ float head_shift(const uint4* h) {
 // lane of the warp has the same count: warp-uniform) each step merges equal counts, and
 // the factor n_b^2 / (n_a n_b (n_a + n_b)) is 1/(2n): q0 = 1/(2 n0), halved per step, no
 // division.  Otherwise the counts travel with the sums and the factor is divided out.
-__device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, float q0,
-                                               bool uniform, int W) {
-  float q = q0;
-  for (int o = W >> 1; o > 0; o >>= 1) {
-    const float Sb = __shfl_xor_sync(kFullMask, S, o);
-    const float Mb = __shfl_xor_sync(kFullMask, M, o);
-    float corr;
-    if (uniform) {
+template <int W>
+__device__ __forceinline__ void stat_butterfly_w(float& S, float& M, float n, float q0,
+                                                 bool uniform) {
+  if (uniform) {
+    float q = q0;
+#pragma unroll
+    for (int o = W >> 1; o > 0; o >>= 1) {
+      const float Sb = __shfl_xor_sync(kFullMask, S, o);
+      const float Mb = __shfl_xor_sync(kFullMask, M, o);
       const float d = __fsub_rn(S, Sb);
-      corr = __fmul_rn(__fmul_rn(d, d), q);
+      const float corr = __fmul_rn(__fmul_rn(d, d), q);
       q = __fmul_rn(q, 0.5f);
-    } else {
+      S = __fadd_rn(S, Sb);
+      M = __fadd_rn(__fadd_rn(M, Mb), corr);
+    }
+  } else {
+#pragma unroll
+    for (int o = W >> 1; o > 0; o >>= 1) {
+      const float Sb = __shfl_xor_sync(kFullMask, S, o);
+      const float Mb = __shfl_xor_sync(kFullMask, M, o);
       const float nb = __shfl_xor_sync(kFullMask, n, o);
       const float nn = __fadd_rn(n, nb);
       const float d = __fsub_rn(__fmul_rn(nb, S), __fmul_rn(n, Sb));
-      corr = (n > 0.f && nb > 0.f)
-                 ? __fdiv_rn(__fmul_rn(d, d), __fmul_rn(__fmul_rn(n, nb), nn))
-                 : 0.f;
+      const float corr = (n > 0.f && nb > 0.f)
+                             ? __fdiv_rn(__fmul_rn(d, d), __fmul_rn(__fmul_rn(n, nb), nn))
+                             : 0.f;
       n = nn;
+      S = __fadd_rn(S, Sb);
+      M = __fadd_rn(__fadd_rn(M, Mb), corr);
     }
-    S = __fadd_rn(S, Sb);
-    M = __fadd_rn(__fadd_rn(M, Mb), corr);
   }
+}
+
+// (the block width as a template argument: the steps unroll)
+__device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, float q0,
+                                               bool uniform, int W) {
+  if (W == 32)
+    stat_butterfly_w<32>(S, M, n, q0, uniform);
+  else if (W == 16)
+    stat_butterfly_w<16>(S, M, n, q0, uniform);
+  else
+    stat_butterfly_w<8>(S, M, n, q0, uniform);
 }
 
 }  // namespace
@@ -220,6 +241,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
   const bool uniform = __all_sync(kFullMask, nvec == __shfl_sync(kFullMask, nvec, 0));
   const int W = NTg < 32 ? NTg : 32;
   const float hf = static_cast<float>(H);  // exact for H < 2^24
+  const float inv_h = 1.0f / hf;           // correctly rounded; exact for H a power of 2
   // Rows of this warp's first group: every lane of a warp runs the same iterations (the
   // shuffles need them all); groups past the chunk's end skip the row work.
   const int g0 = red_smem ? g : (tid & ~31) / NTg;
@@ -321,8 +343,8 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
       }
       if (j < ng) stat_butterfly(St, Mt, n_lane, 0.5f * inv_n, uniform, W);
       if (valid) {
-        const float mean = __fadd_rn(K, __fdiv_rn(Sg, hf));
-        const float rs = __frsqrt_rn(__fadd_rn(__fdiv_rn(Mg, hf), a.eps));
+        const float mean = __fadd_rn(K, __fmul_rn(Sg, inv_h));
+        const float rs = __frsqrt_rn(__fadd_rn(__fmul_rn(Mg, inv_h), a.eps));
         const float nmean = -mean;
         const f2 rs2 = f2_splat(rs);
         const size_t out_row = static_cast<size_t>(row) * H + col0;

@@ -28,19 +28,16 @@ constexpr int kLnMaxWarpsPerGroup = 16;
 //               the dw and db running sums and their compensations take 32 registers a
 //               column vector
 //  kLnFwdPair   forward of one CTA of a pair, up to 256 consumers (9 warps: 168 registers)
-//  kLnBwdQuad   backward with 4-vector threads, up to 256 consumers (9 warps: 168
-//               registers, a few spilled): two 128-thread rows in flight at H = 4096,
-//               where the other classes fit one
 //  kLnBwdTm     backward with each thread's dw sums, their compensations and the db sums
 //               in tensor memory (32 columns of its lane a column vector), up to 608
 //               consumers (20 warps with the producer: 96 registers); single CTAs only
-enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3, kLnBwdQuad = 4,
-       kLnBwdTm = 5 };
+// (class 4 is not used: a register-resident 4-vector backward that the tensor-memory
+// class replaced)
+enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3, kLnBwdTm = 5 };
 constexpr int ln_consumers(int cls) {
   return cls == kLnBwdWide ? 352
-                           : ((cls == kLnFwdPair || cls == kLnBwdQuad)
-                                  ? 256
-                                  : ((cls == kLnBwdTm || cls == kLnFwd) ? 608 : 480));
+                           : (cls == kLnFwdPair ? 256
+                                                : ((cls == kLnBwdTm || cls == kLnFwd) ? 608 : 480));
 }
 // Tensor-memory columns a kLnBwdTm CTA of `cons_warps` consumer warps uses: 32 a column
 // vector a thread (dw sums [0, 8), their compensations [8, 16), db sums [16, 24)), the
@@ -122,7 +119,7 @@ struct LnShape {
   int tensors;  // BF16 tensors staged per row (1 forward, 2 backward)
   int threads;  // groups * ntg + producer warp
   size_t smem;  // dynamic shared memory bytes
-  int cls;      // kLnFwd, kLnBwdMulti, kLnBwdWide, kLnFwdPair, kLnBwdQuad or kLnBwdTm
+  int cls;      // kLnFwd, kLnBwdMulti, kLnBwdWide, kLnFwdPair or kLnBwdTm
   int pair;     // 1: a CTA pair per row chunk, each CTA owning half the columns
 };
 
