@@ -180,7 +180,12 @@ cudaError_t ln_launch_pair(const void* fn, unsigned pairs, unsigned threads, siz
 LnShape ln_bwd_shape(int H) {
   static const int cand[][2] = {{1, kLnBwdMulti}, {2, kLnBwdMulti}, {3, kLnBwdWide}};
   const LnShape s = pick_shape(H, 2, cand, 3);
-  if (H > kLnMaxH) return s;  // pair widths keep the multi and wide pair builds
+  if (H > kLnMaxH) {
+    // pair widths: the 4-vector tensor-memory pair build where it keeps more rows in flight
+    static const int tp[][2] = {{4, kLnBwdTm}};
+    const LnShape t = pick_shape(H, 2, tp, 1);
+    return (t.groups > s.groups && t.stages >= 3) ? t : s;
+  }
   // the tensor-memory class where it keeps more rows in flight (its column sums leave the
   // registers, so 20 warps fit)
   static const int tmc[][2] = {{2, kLnBwdTm}, {3, kLnBwdTm}, {4, kLnBwdTm}};

@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   // and come to registers one column vector at a time; the weight sits in shared memory
   constexpr bool kTm = kCls == kLnBwdTm;
   const LnSmem L = ln_shape_layout(S, 2, G, H, NTg, kPair, kTm);
-  static_assert(!(kTm && kPair), "the tensor-memory class has no pair build");
 
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
     float4* wp = reinterpret_cast<float4*>(wsm);
     for (int c = tid; c < NV; c += ncons) {
       Param8<kFp32W> pw;
-      load_param8<kFp32W>(a.w, c, pw);
+      load_param8<kFp32W>(a.w, (col0 >> 3) + c, pw);  // (a pair: this CTA's half)
       const f2 w0 = param_pair<kFp32W>(pw, 0), w1 = param_pair<kFp32W>(pw, 1);
       const f2 w2 = param_pair<kFp32W>(pw, 2), w3 = param_pair<kFp32W>(pw, 3);
       wp[c] = make_float4(f2_lo(w0), f2_hi(w0), f2_lo(w1), f2_hi(w1));
@@ -616,7 +615,8 @@ const void* ln_bwd_ptr_v(bool fp32w) {
 const void* pick_ln_bwd(const LnShape& s, bool fp32w) {
   if (s.pair)
     return s.cls == kLnBwdWide ? ln_bwd_ptr_v<3, kLnBwdWide, true>(fp32w)
-                               : ln_bwd_ptr_v<2, kLnBwdMulti, true>(fp32w);
+                               : (s.cls == kLnBwdTm ? ln_bwd_ptr_v<4, kLnBwdTm, true>(fp32w)
+                                                    : ln_bwd_ptr_v<2, kLnBwdMulti, true>(fp32w));
   if (s.cls == kLnBwdWide) return ln_bwd_ptr_v<3, kLnBwdWide, false>(fp32w);
   if (s.cls == kLnBwdTm)
     return s.vpt == 2 ? ln_bwd_ptr_v<2, kLnBwdTm, false>(fp32w)

@@ -99,8 +99,8 @@ __device__ __forceinline__ void stat_butterfly(float& S, float& M, float n, floa
 }  // namespace
 
 // One build per vector count and parameter dtype; one CTA an SM, up to 608 consumers +
-// the producer warp (20 warps: 96 registers a thread).  kPair (class kLnFwdPair, up to
-// 256 consumers, 4-vector threads): the CTA is one of a cluster of two that share each
+// the producer warp (20 warps: 96 registers a thread).  kPair (class kLnFwdPair, also up to
+// 608 consumers, 4-vector threads): the CTA is one of a cluster of two that share each
 // row, this one owning the columns [rank*H/2, (rank+1)*H/2) (whole-warp row groups only);
 // the two CTAs merge both halves' warp statistics in the same order, so they compute the
 // same mean and rstd.
@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
       const int s = s_cur;
       mbar_wait_bounded(&full[s], ph, abort_flag, a.err, kErrConsumerWait);
       if (row < r1) {
-        const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+        const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
         // statistics of x - K, K the row's first element (one value for the whole group,
         // and for both CTAs of a pair)
         // (x - K: the mixed-precision fma reads the staged BF16 words directly)
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
       const int32_t row = r0 + jj * G + g;
       const int s = s_prev;
       const bool valid = row < r1;
-      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      const __nv_bfloat16* xs = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
       uint4 hv[VPT];
       const float K = !valid ? 0.f : (kPair ? head_shift(&head[s * G + g]) : row_shift(xs));
 #pragma unroll

@@ -27,17 +27,17 @@ constexpr int kLnMaxWarpsPerGroup = 16;
 //               scheduler partition: 168 registers), for rows past 480 2-vector threads;
 //               the dw and db running sums and their compensations take 32 registers a
 //               column vector
-//  kLnFwdPair   forward of one CTA of a pair, up to 256 consumers (9 warps: 168 registers)
+//  kLnFwdPair   forward of one CTA of a pair, up to 608 consumers (20 warps: 96 registers)
 //  kLnBwdTm     backward with each thread's dw sums, their compensations and the db sums
 //               in tensor memory (32 columns of its lane a column vector), up to 608
-//               consumers (20 warps with the producer: 96 registers); single CTAs only
+//               consumers (20 warps with the producer: 96 registers); single CTAs, and
+//               (4 vectors a thread) one CTA of a pair
 // (class 4 is not used: a register-resident 4-vector backward that the tensor-memory
 // class replaced)
 enum { kLnFwd = 0, kLnBwdMulti = 1, kLnBwdWide = 2, kLnFwdPair = 3, kLnBwdTm = 5 };
 constexpr int ln_consumers(int cls) {
   return cls == kLnBwdWide ? 352
-                           : (cls == kLnFwdPair ? 256
-                                                : ((cls == kLnBwdTm || cls == kLnFwd) ? 608 : 480));
+                           : ((cls == kLnBwdTm || cls == kLnFwd || cls == kLnFwdPair) ? 608 : 480);
 }
 // Tensor-memory columns a kLnBwdTm CTA of `cons_warps` consumer warps uses: 32 a column
 // vector a thread (dw sums [0, 8), their compensations [8, 16), db sums [16, 24)), the

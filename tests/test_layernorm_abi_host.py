@@ -121,7 +121,7 @@ def test_layernorm_plan_fits_its_kernel_build_at_every_width(lib, op):
             assert 2 * warps_both <= 64, ctx          # two slot floats a warp of the pair
         if op == LN_FWD:
             if pair:
-                assert (p["cls"], p["vpt"]) == (3, 4) and p["class_max_threads"] == 288, ctx
+                assert (p["cls"], p["vpt"]) == (3, 4) and p["class_max_threads"] == 640, ctx
             else:
                 assert p["cls"] == 0 and p["vpt"] in (1, 2, 4), ctx
                 assert p["class_max_threads"] == 640, ctx
@@ -129,7 +129,7 @@ def test_layernorm_plan_fits_its_kernel_build_at_every_width(lib, op):
             assert (p["cls"], p["vpt"]) in ((1, 1), (1, 2), (2, 3), (5, 2), (5, 3), (5, 4)), ctx
             assert p["class_max_threads"] == {1: 512, 2: 384, 5: 640}[p["cls"]], ctx
             if pair:
-                assert p["cls"] != 5, ctx              # no pair build of this class
+                assert p["cls"] != 5 or p["vpt"] == 4, ctx   # the one pair build of it
             if p["cls"] == 5:
                 # the tensor-memory class: whole consumer warps, 32 columns of a thread's
                 # lane a column vector, four warps a lane quadrant, within 512 columns
