@@ -39,10 +39,12 @@ __device__ __forceinline__ float two_sum_ln(float a, float b, float& err) {
   return s;
 }
 
-// Running sum with a Fast2Sum compensation term: acc + cmp tracks the sum of every p.
-__device__ __forceinline__ void comp_add(f2& acc, f2& cmp, f2 p) {
-  const f2 t = f2_add(acc, p);
-  cmp = f2_add(cmp, f2_add(f2_sub(acc, t), p));
+// Running sum with a Fast2Sum compensation term: acc + cmp tracks the sum of every a*b.
+// t = acc + a*b in one fma; acc - t is exact once |acc| >= |a*b| (Fast2Sum), and the
+// second fma adds a*b back to it: the addition's error, rounded once, into cmp.
+__device__ __forceinline__ void comp_fma_add(f2& acc, f2& cmp, f2 a, f2 b) {
+  const f2 t = f2_fma(a, b, acc);
+  cmp = f2_add(cmp, f2_fma(a, b, f2_sub(acc, t)));
   acc = t;
 }
 
@@ -364,11 +366,11 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
               const f2 gw = f2_mul(d2, wq[q]);
               const f2 t = f2_fma(dd, ncr2, f2_sub(gw, c1));  // g - c1 - xhat*c2, over r
               o[q] = f2_to_bf2(f2_mul(t, rs2));
-              const f2 p = f2_mul(f2_mul(d2, dd), rs2);  // dy * xhat
+              const f2 ddy = f2_mul(d2, dd);  // dy * xhat = ddy * rstd
               if constexpr (kTm) {
                 f2 av = f2_make(tw[2 * q], tw[2 * q + 1]);
                 f2 cv = f2_make(tw[8 + 2 * q], tw[9 + 2 * q]);
-                comp_add(av, cv, p);
+                comp_fma_add(av, cv, ddy, rs2);
                 const f2 bv2 = f2_add(f2_make(tb[2 * q], tb[2 * q + 1]), d2);  // dy
                 tw[2 * q] = f2_lo(av);
                 tw[2 * q + 1] = f2_hi(av);
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
                 tb[2 * q] = f2_lo(bv2);
                 tb[2 * q + 1] = f2_hi(bv2);
               } else {
-                comp_add(aw[v][q], cw[v][q], p);
+                comp_fma_add(aw[v][q], cw[v][q], ddy, rs2);
                 ab[v][q] = f2_add(ab[v][q], d2);  // dy
               }
             }

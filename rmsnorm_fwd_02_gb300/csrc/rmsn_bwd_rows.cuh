@@ -391,7 +391,6 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       // FP32, and dy*x*rs_lo, 2^-8 smaller, only feeds the compensation term.
       const float rs_hi = __uint_as_float(__float_as_uint(rs) & 0xffff0000u);
       const f2 rs2 = f2_splat(rs), rh2 = f2_splat(rs_hi);
-      const f2 rl2 = f2_splat(__fsub_rn(rs, rs_hi));
       // c = (1/H) sum g*xhat = (rstd/H) sum (dy*w)*x
       // dx = rstd*(g - x*(c*rstd)): xhat*c as one product of x, so the cancelling pair
       // is a single fma; c*rstd is on the scale of dx, so no new overflow or underflow
@@ -428,11 +427,11 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
             dyx[q] = f2_mul(d2, x2);
             if constexpr (!kTm) {
               // dw: running sum of the exact products dy*x*rs_hi with a Fast2Sum
-              // compensation term, which also collects dy*x*rs_lo
-              const f2 p = f2_mul(dyx[q], rh2);
-              const f2 t = f2_add(acc[v][q], p);
-              const f2 e = f2_add(f2_sub(acc[v][q], t), p);
-              cmp[v][q] = f2_fma(dyx[q], rl2, f2_add(cmp[v][q], e));
+              // compensation term, which also collects dy*x*rs_lo.  t = acc + p in one
+              // fma (p is exact); acc - t is exact (Fast2Sum), so dy*x*rs + (acc - t) is
+              // the addition's error plus dy*x*rs_lo, rounded once
+              const f2 t = f2_fma(dyx[q], rh2, acc[v][q]);
+              cmp[v][q] = f2_add(cmp[v][q], f2_fma(dyx[q], rs2, f2_sub(acc[v][q], t)));
               acc[v][q] = t;
             }
           }
@@ -445,11 +444,9 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // the same update, on the loaded cells
               const f2 av = f2_make(tv[2 * q], tv[2 * q + 1]);
-              const f2 p = f2_mul(dyx[q], rh2);
-              const f2 t = f2_add(av, p);
-              const f2 e = f2_add(f2_sub(av, t), p);
-              const f2 cv = f2_fma(dyx[q], rl2,
-                                   f2_add(f2_make(tv[8 + 2 * q], tv[9 + 2 * q]), e));
+              const f2 t = f2_fma(dyx[q], rh2, av);
+              const f2 cv = f2_add(f2_make(tv[8 + 2 * q], tv[9 + 2 * q]),
+                                   f2_fma(dyx[q], rs2, f2_sub(av, t)));
               tv[2 * q] = f2_lo(t);
               tv[2 * q + 1] = f2_hi(t);
               tv[8 + 2 * q] = f2_lo(cv);
