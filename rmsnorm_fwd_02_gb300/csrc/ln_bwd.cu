@@ -226,10 +226,13 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
   }
   // this thread's weight pairs for column vector c (its v-th): FP32 planes in shared
   // memory (kTm) or the registers
+  const uint32_t ring32 = smem_u32(smem);
+  const uint32_t w32 = ring32 + static_cast<uint32_t>(L.w);
+  const uint32_t dy_off = static_cast<uint32_t>(G) * Hc * 2u;  // dy rows after x's in a stage
   auto wvec = [&](int v, int c, f2 (&wq)[4]) {
     if constexpr (kTm) {
-      const float4 lo = reinterpret_cast<const float4*>(wsm)[c];
-      const float4 hi = reinterpret_cast<const float4*>(wsm)[NV + c];
+      const float4 lo = lds128f_at(w32 + 16u * c);
+      const float4 hi = lds128f_at(w32 + 16u * (NV + c));
       wq[0] = f2_make(lo.x, lo.y);
       wq[1] = f2_make(lo.z, lo.w);
       wq[2] = f2_make(hi.x, hi.y);
@@ -256,13 +259,13 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
       f2 ga = f2_splat(0.f), gb = f2_splat(0.f), da = f2_splat(0.f), db2 = f2_splat(0.f);
       if (row < r1) {
         const float nmu = -stat[s * 2 * SP + (row - ((r0 + j * G) & ~3))];
-        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
+        const uint32_t st = ring32 + 2u * static_cast<uint32_t>(s * stage_elems + g * Hc);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
           const int c = lt + v * NTg;
           if (c < NV) {
-            const uint4 xv = lds128(st + c * 8);
-            const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
+            const uint4 xv = lds128_at(st + 16u * c);
+            const uint4 dv = lds128_at(st + dy_off + 16u * c);
             f2 wq[4];
             wvec(v, c, wq);
 #pragma unroll
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
         // xhat*c2 = d * (r^2 SGD / H): one product of d, so the cancelling terms meet in
         // a single fma
         const f2 ncr2 = f2_splat(-(SGD * (rs * inv_h)) * rs);
-        const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * Hc;
+        const uint32_t st = ring32 + 2u * static_cast<uint32_t>(s * stage_elems + g * Hc);
         const size_t out_row = static_cast<size_t>(row) * H + col0;
         if constexpr (kTm) {
           __syncwarp();
@@ -354,8 +357,8 @@ __global__ void __launch_bounds__(ln_max_threads(kCls), 1)
             tmem_wait_ld();
           }
           if (live) {
-            const uint4 xv = lds128(st + c * 8);
-            const uint4 dv = lds128(st + static_cast<size_t>(G) * Hc + c * 8);
+            const uint4 xv = lds128_at(st + 16u * c);
+            const uint4 dv = lds128_at(st + dy_off + 16u * c);
             f2 wq[4];
             wvec(v, c, wq);
             uint32_t o[4];

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
           const int c = lt + v * NTg;
           xr[v] = make_uint4(0u, 0u, 0u, 0u);
           if (c < NV) {
-            xr[v] = lds128(xs + c * 8);
+            xr[v] = lds128_at(smem_u32(xs) + 16u * c);
             s0 = f2_add(s0, bf2_minus(xr[v].x, nK));
             s1 = f2_add(s1, bf2_minus(xr[v].y, nK));
             s0 = f2_add(s0, bf2_minus(xr[v].z, nK));
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(ln_max_threads(kPair ? kLnFwdPair : kLnFwd), 1
       for (int v = 0; v < VPT; ++v) {
         const int c = lt + v * NTg;
         hv[v] = make_uint4(0u, 0u, 0u, 0u);
-        if (valid && c < NV) hv[v] = lds128(xs + c * 8);
+        if (valid && c < NV) hv[v] = lds128_at(smem_u32(xs) + 16u * c);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp has its vectors of the stage

@@ -289,10 +289,14 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
     named_bar_sync(14, ncons);
   }
   // this thread's weight pairs for column vector c (its v-th)
+  // shared-window addresses: the ring, and the weight planes
+  const uint32_t ring32 = smem_u32(smem);
+  const uint32_t w32 = ring32 + static_cast<uint32_t>(L.w);
+  const uint32_t dy_off = static_cast<uint32_t>(G) * H * 2u;  // dy rows after x's in a stage
   auto wvec = [&](int v, int c, f2 (&p)[4]) {
     if constexpr (kWSmem) {
-      const float4 a4 = reinterpret_cast<const float4*>(wsm)[c];
-      const float4 b4 = reinterpret_cast<const float4*>(wsm)[NV + c];
+      const float4 a4 = lds128f_at(w32 + 16u * c);
+      const float4 b4 = lds128f_at(w32 + 16u * (NV + c));
       p[0] = f2_make(a4.x, a4.y);
       p[1] = f2_make(a4.z, a4.w);
       p[2] = f2_make(b4.x, b4.y);
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   // sum (dy*w)*x (and, kRc, of sum x^2), reduced over the group (sub-warp groups: returned;
   // whole-warp groups: published to the row's reduction slots).
   auto phase_a = [&](int32_t j, int s, bool valid) -> RowSums {
-    const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+    const uint32_t st = ring32 + 2u * static_cast<uint32_t>(s * stage_elems + g * H);
     f2 dot0 = f2_splat(0.f), dot1 = f2_splat(0.f);
     f2 ss0 = f2_splat(0.f), ss1 = f2_splat(0.f);
     if (valid) {
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       for (int v = 0; v < VPT; ++v) {
         const int c = lt + v * NTg;
         if (c < NV) {
-          const uint4 xv = lds128(st + c * 8);
-          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+          const uint4 xv = lds128_at(st + 16u * c);
+          const uint4 dv = lds128_at(st + dy_off + 16u * c);
           f2 wl[4];
           wvec(v, c, wl);
           // (dy*x)*w: dy*x exact from the BF16 words, one rounding in the fma with w
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       // dx = rstd*(g - x*(c*rstd)): xhat*c as one product of x, so the cancelling pair
       // is a single fma; c*rstd is on the scale of dx, so no new overflow or underflow
       const f2 ncr2 = f2_splat(-(dot * (rs * inv_h)) * rs);
-      const __nv_bfloat16* st = ring + s * stage_elems + static_cast<size_t>(g) * H;
+      const uint32_t st = ring32 + 2u * static_cast<uint32_t>(s * stage_elems + g * H);
       const size_t out_row = static_cast<size_t>(row) * H;
       if constexpr (kTm) {
         __syncwarp();
@@ -409,10 +413,10 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
         if constexpr (kTm) tmem_ld16(tm + 16u * v, tv);
         f2 dyx[4];
         if (live) {
-          const uint4 xv = lds128(st + c * 8);
-          const uint4 dv = lds128(st + static_cast<size_t>(G) * H + c * 8);
+          const uint4 xv = lds128_at(st + 16u * c);
+          const uint4 dv = lds128_at(st + dy_off + 16u * c);
           uint4 hv = make_uint4(0u, 0u, 0u, 0u);
-          if constexpr (kDh) hv = lds128(st + static_cast<size_t>(2 * G) * H + c * 8);
+          if constexpr (kDh) hv = lds128_at(st + 2u * dy_off + 16u * c);
           f2 wl[4];
           wvec(v, c, wl);
           uint32_t o[4];

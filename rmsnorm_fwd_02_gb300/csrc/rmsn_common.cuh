@@ -265,6 +265,22 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
 }
 
+// 16 bytes of shared memory at the shared-window address a (32-bit addressing).
+__device__ __forceinline__ uint4 lds128_at(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f_at(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
+}
+
 __device__ __forceinline__ void stg128(void* p, uint4 v) {
   *reinterpret_cast<uint4*>(p) = v;
 }
