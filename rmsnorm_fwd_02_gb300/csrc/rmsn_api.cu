@@ -293,11 +293,18 @@ Shape bwd_shape(int H, bool with_dh) {
   // past 3 x 240 vectors: 4-vector threads in two row groups of up to 240 (H up to 7680)
   // while the ring still holds three stages of them (measured: with two stages the ring
   // runs dry, and one wide group does better), else one wide group
+  Shape best = make_shape(H, tensors, nv <= 768 ? 2 : 4, true, /*allow_multi=*/false);
   if (busy(4) > 0) {
     const Shape s = make_shape(H, tensors, 4, true);
-    if (s.stages >= 3) return s;
+    if (s.stages >= 3) best = s;
   }
-  return make_shape(H, tensors, nv <= 768 ? 2 : 4, true, /*allow_multi=*/false);
+  // the tensor-memory class with 4-vector rows of up to 304 threads (two or more rows a
+  // stage in its 608 consumers) where it keeps more rows in flight at three stages
+  const Shape t = make_shape(H, tensors, 4, true, true, /*tm=*/true);
+  if (t.ntg <= kTmConsumers / 2 && t.stages >= 3 && t.smem <= kMaxSmemBytes &&
+      t.groups > best.groups)
+    return t;
+  return best;
 }
 
 cudaError_t prepare_kernel(const void* fn, size_t smem) {
