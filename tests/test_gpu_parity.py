@@ -111,10 +111,11 @@ def test_bwd_rstd_not_16_byte_aligned(H, T):
 
 
 @pytest.mark.parametrize("H,T", [(8, 5003), (256, 4099), (264, 4500), (1000, 1100), (2816, 400),
-                                 (5632, 190), (7680, 140)])
+                                 (5632, 190), (7680, 140), (8192, 4099), (1536, 20011)])
 def test_more_ragged_widths_and_row_counts(H, T):
     # ragged row counts at widths of every backward and forward build (8-lane, 16-lane and
-    # whole-warp groups, 2- to 4-vector threads, the wide class)
+    # whole-warp groups, 2- to 4-vector threads, the wide class; the tensor-memory class at
+    # H = 1536 and 8192 over many ring stages a CTA)
     parity.run_case(synth.make_case(13, T, H, w_fp32=(H % 16 == 0), label=f"ragged{H}_T{T}"))
 
 
