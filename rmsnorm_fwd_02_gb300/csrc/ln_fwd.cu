@@ -424,13 +424,6 @@ const void* pick_ln_fwd(const LnShape& s, bool fp32w) {
 
 }  // namespace lnorm
 
-namespace rmsn {
-cudaError_t prepare_kernel(const void* fn, size_t smem);       // rmsn_api.cu
-int blocks_per_sm(const void* fn, int threads, size_t smem);   // rmsn_api.cu
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       void** args);                           // rmsn_api.cu
-}  // namespace rmsn
-
 namespace lnorm {
 
 int ln_fwd_blocks_per_sm(const LnShape& s, bool fp32w) {

@@ -80,11 +80,6 @@ const void* bwd_rows_fn(const Shape& s, bool fp32w, bool dh, bool rc) {
   return rc ? bwd_rows_fn_rc(s, fp32w, dh) : bwd_rows_fn_rs(s, fp32w, dh);
 }
 
-cudaError_t prepare_kernel(const void* fn, size_t smem);
-int blocks_per_sm(const void* fn, int threads, size_t smem);
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       void** args);
-
 int bwd_blocks_per_sm(const Shape& s, bool fp32w, bool rc) {
   return blocks_per_sm(bwd_rows_fn(s, fp32w, s.tensors == 3, rc), s.threads, s.smem);
 }

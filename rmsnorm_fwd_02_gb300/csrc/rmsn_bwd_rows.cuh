@@ -124,15 +124,10 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
   uint32_t* tm_slot = reinterpret_cast<uint32_t*>(smem + L.abort_flag) + 2;
   const uint32_t tm_ncols = kTm ? tmem_alloc_cols(bwd_tm_cols(ncons / 32, VPT)) : 0u;
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
-    }
-    if (red_smem)
-      for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
-    *abort_flag = 0;
-    fence_barrier_init();
+  if (tid >= ncons) {  // the producer warp (consumer warp 0 takes the tensor memory)
+    init_row_barriers_warp(full, empty, S, static_cast<uint32_t>(G * NTg / 32), redb,
+                           red_smem ? kRedBufs * G : 0, static_cast<uint32_t>(NW), tid - ncons);
+    if (tid == ncons) *abort_flag = 0;
   }
   if constexpr (kTm) {
     // consumer warp 0 takes the columns (one CTA an SM: nothing else holds them); the
@@ -539,45 +534,81 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
         pl[1] = make_ulonglong2(lo[2].v, lo[3].v);
       }
     }
-    return;
-  }
-  // several row groups: combine them through shared memory in group order.  The ring is
-  // free once every consumer is past its loop: each stage was waited on (full) by every
-  // group that had a row in it before that group finished.
-  named_bar_sync(15, ncons);
-  // cb: [G][2][H] (hi, lo), each H-slab stored as two planes of float4 (columns 0-3 and
-  // 4-7 of every vector) so that a warp's stores of one plane are contiguous
-  float* cb = reinterpret_cast<float*>(smem);
+  } else {
+    // several row groups: combine them through shared memory in group order.  The ring
+    // is free once every consumer is past its loop: each stage was waited on (full) by
+    // every group that had a row in it before that group finished.
+    named_bar_sync(15, ncons);
+    // cb: [G][2][H] (hi, lo), each H-slab stored as two planes of float4 (columns 0-3 and
+    // 4-7 of every vector) so that a warp's stores of one plane are contiguous
+    float* cb = reinterpret_cast<float*>(smem);
 #pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    const int c = lt + v * NTg;
-    if (c < NV) {
-      f2 hi[4], lo[4];
+    for (int v = 0; v < VPT; ++v) {
+      const int c = lt + v * NTg;
+      if (c < NV) {
+        f2 hi[4], lo[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        hi[q] = f2_add(acc[v][q], cmp[v][q]);
-        lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
+        for (int q = 0; q < 4; ++q) {
+          hi[q] = f2_add(acc[v][q], cmp[v][q]);
+          lo[q] = f2_sub(cmp[v][q], f2_sub(hi[q], acc[v][q]));
+        }
+        ulonglong2* ph = reinterpret_cast<ulonglong2*>(cb + (2 * g) * H);
+        ulonglong2* pl = reinterpret_cast<ulonglong2*>(cb + (2 * g + 1) * H);
+        ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
+        ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
+        pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
+        pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
       }
-      ulonglong2* ph = reinterpret_cast<ulonglong2*>(cb + (2 * g) * H);
-      ulonglong2* pl = reinterpret_cast<ulonglong2*>(cb + (2 * g + 1) * H);
-      ph[c] = make_ulonglong2(hi[0].v, hi[1].v);
-      ph[NV + c] = make_ulonglong2(hi[2].v, hi[3].v);
-      pl[c] = make_ulonglong2(lo[0].v, lo[1].v);
-      pl[NV + c] = make_ulonglong2(lo[2].v, lo[3].v);
     }
-  }
-  named_bar_sync(15, ncons);
-  for (int col = tid; col < H; col += ncons) {
-    const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
-    float sacc = 0.f, e = 0.f;
-    for (int gi = 0; gi < G; ++gi) {
-      float err;
-      sacc = two_sum(sacc, cb[(2 * gi) * H + at], err);
-      e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + at]));
+    named_bar_sync(15, ncons);
+    // Per column: TwoSum of the groups' hi in group order, their lo and the errors summed
+    // beside.  Where that keeps at least half the consumers busy, a thread takes one
+    // float4 of a plane (u < NV: columns 8u..8u+3; else columns 8(u-NV)+4..+7), four
+    // independent columns; otherwise (narrow rows, many groups) a column a thread.
+    // Either way the slabs' loads are issued ahead of the additions.
+    if (H < 2 * ncons) {
+      for (int col = tid; col < H; col += ncons) {
+        const int at = ((col & 7) >> 2) * (4 * NV) + (col >> 3) * 4 + (col & 3);
+        float sacc = 0.f, e = 0.f;
+#pragma unroll 4
+        for (int gi = 0; gi < G; ++gi) {
+          float err;
+          sacc = two_sum(sacc, cb[(2 * gi) * H + at], err);
+          e = __fadd_rn(e, __fadd_rn(err, cb[(2 * gi + 1) * H + at]));
+        }
+        const float hi = __fadd_rn(sacc, e);
+        part[col] = hi;
+        part[H + col] = __fsub_rn(e, __fsub_rn(hi, sacc));
+      }
+    } else {
+      const float4* cb4 = reinterpret_cast<const float4*>(smem);
+      const int slab4 = H / 4;  // float4s a slab
+      for (int u = tid; u < 2 * NV; u += ncons) {
+        const int col0 = u < NV ? 8 * u : 8 * (u - NV) + 4;
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int gi = 0; gi < G; ++gi) {
+          const float4 h4 = cb4[(2 * gi) * slab4 + u];
+          const float4 l4 = cb4[(2 * gi + 1) * slab4 + u];
+          const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float err;
+            sacc[i] = two_sum(sacc[i], hv[i], err);
+            e[i] = __fadd_rn(e[i], __fadd_rn(err, lv[i]));
+          }
+        }
+        float hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          hi[i] = __fadd_rn(sacc[i], e[i]);
+          lo[i] = __fsub_rn(e[i], __fsub_rn(hi[i], sacc[i]));
+        }
+        *reinterpret_cast<float4*>(part + col0) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<float4*>(part + H + col0) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+      }
     }
-    const float hi = __fadd_rn(sacc, e);
-    part[col] = hi;
-    part[H + col] = __fsub_rn(e, __fsub_rn(hi, sacc));
   }
 }
 

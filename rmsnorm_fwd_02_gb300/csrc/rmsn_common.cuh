@@ -119,6 +119,26 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// A row kernel's barriers, initialised by the 32 lanes of one warp (a barrier a lane, each
+// lane fencing its own inits): the ring's S full barriers (one arrival: the producer's
+// expect-tx), its S empty barriers (`empty_count` arrivals) and `nred` per-row reduction
+// barriers (`red_count` arrivals).  One thread doing them all in series costs ~7 ns a
+// barrier, which the kernel's start waits on.  The caller's __syncthreads() publishes them.
+__device__ __forceinline__ void init_row_barriers_warp(uint64_t* full, uint64_t* empty, int S,
+                                                       uint32_t empty_count, uint64_t* redb,
+                                                       int nred, uint32_t red_count,
+                                                       int lane) {
+  for (int i = lane; i < 2 * S + nred; i += 32) {
+    if (i < S)
+      mbar_init(&full[i], 1u);
+    else if (i < 2 * S)
+      mbar_init(&empty[i - S], empty_count);
+    else
+      mbar_init(&redb[i - 2 * S], red_count);
+  }
+  fence_barrier_init();
+}
+
 // L2 policy for data that is read exactly once.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
@@ -418,5 +438,15 @@ __device__ __forceinline__ void copy_rows_contig(__nv_bfloat16* dst, const __nv_
   bulk_g2s(dst, src + static_cast<int64_t>(ra) * H,
            static_cast<uint32_t>(rb - ra) * static_cast<uint32_t>(H) * 2u, bar, pol);
 }
+
+// ---- host helpers of every kernel translation unit (defined in rmsn_api.cu) ----
+// Opts fn into the shared-memory size the row kernels use (once per device).
+cudaError_t prepare_kernel(const void* fn, size_t smem);
+// Resident CTAs an SM of fn at this block size and shared memory (cached per device).
+int blocks_per_sm(const void* fn, int threads, size_t smem);
+// Launches fn with programmatic dependent launch (its prologue may overlap the previous
+// kernel on the stream).
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       void** args);
 
 }  // namespace rmsn

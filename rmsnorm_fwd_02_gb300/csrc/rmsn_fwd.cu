@@ -71,15 +71,10 @@ __global__ void __launch_bounds__(fwd_max_threads(kCls, VPT), fwd_design_blocks_
   const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(k + 1) * a.R) / a.P);
   const int32_t nstage = (r1 - r0 + G - 1) / G;
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], static_cast<uint32_t>(G * NTg / 32));  // one arrival per warp
-    }
-    if (red_smem)
-      for (int i = 0; i < kRedBufs * G; ++i) mbar_init(&redb[i], static_cast<uint32_t>(NW));
-    *abort_flag = 0;
-    fence_barrier_init();
+  if (tid >= ncons) {  // the producer warp
+    init_row_barriers_warp(full, empty, S, static_cast<uint32_t>(G * NTg / 32), redb,
+                           red_smem ? kRedBufs * G : 0, static_cast<uint32_t>(NW), tid - ncons);
+    if (tid == ncons) *abort_flag = 0;
   }
   __syncthreads();
   // Inputs may come from the kernel before us on the stream: wait for it before any
@@ -262,10 +257,6 @@ static const void* pick_fwd(const Shape& s, bool fp32w, bool res) {
   }
 }
 
-cudaError_t prepare_kernel(const void* fn, size_t smem);       // rmsn_api.cu
-int blocks_per_sm(const void* fn, int threads, size_t smem);   // rmsn_api.cu
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       void** args);                           // rmsn_api.cu
 
 int fwd_blocks_per_sm(const Shape& s, bool fp32w) {
   return blocks_per_sm(pick_fwd(s, fp32w, s.tensors == 2), s.threads, s.smem);

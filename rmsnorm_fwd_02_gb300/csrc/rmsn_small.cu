@@ -223,8 +223,6 @@ const void* small_ptr_v(bool fp32w, bool dh) {
 
 }  // namespace
 
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       void** args);  // rmsn_api.cu
 
 bool bwd_is_small(int64_t R) { return R > 0 && R <= kSmallMaxRows; }
 
