@@ -441,7 +441,7 @@ int bwd_common(const void* x, const void* dy, const void* dh, const float* rstd,
     if (launch_bwd_rows(a, s, fp32w, stream_) != cudaSuccess) return RMSN_ERR_CUDA;
   }
   unsigned* ctl = (deterministic || R == 0) ? nullptr : static_cast<unsigned*>(workspace);
-  if (launch_dw_finish(part, dw, P, H, ctl, stream_) != cudaSuccess)
+  if (launch_dw_finish(part, dw, P, H, ctl, g_sms[dev], stream_) != cudaSuccess)
     return RMSN_ERR_CUDA;
   return RMSN_OK;
 }

@@ -16,7 +16,12 @@ namespace rmsn {
 // kFinishSlices slices takes k in [i*P/slices, (i+1)*P/slices) in increasing k, then the
 // slice sums are combined by a pairwise tree in slice order (i with i + stride, stride
 // halving).  TwoSum carries the error terms throughout.  Each thread walks only ~P/32
-// partials with four loads in flight, so the kernel is a short tail.
+// partials, so the kernel is a short tail.  Two builds add them the same way and differ
+// only in how the loads are batched: kOneTrip loads up to five (hi, lo) pairs at once, so
+// a slice of P <= 160 partials takes one round trip to L2 (64 registers: one 1024-thread
+// CTA an SM, taken when the grid fits one wave), the other four at a time and the rest one
+// by one (32 registers: two CTAs an SM).
+template <bool kOneTrip>
 __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
     rmsn_dw_finish_kernel(const float* __restrict__ part, float* __restrict__ dw, int P, int H,
                           unsigned* ctl) {
@@ -35,25 +40,47 @@ __global__ void __launch_bounds__(kFinishCols* kFinishSlices)
     const int ka = (sl * P) / kFinishSlices;
     const int kb = ((sl + 1) * P) / kFinishSlices;
     const float* p = part + static_cast<size_t>(ka) * 2 * H + col;
-    int kk = ka;
-    for (; kk + 4 <= kb; kk += 4, p += static_cast<size_t>(8) * H) {
-      float hi[4], lo[4];
+    if constexpr (kOneTrip) {
+      for (int kk = ka; kk < kb; kk += 5, p += static_cast<size_t>(10) * H) {
+        const int n = kb - kk;
+        float hi[5], lo[5];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        hi[u] = p[static_cast<size_t>(2 * u) * H];
-        lo[u] = p[static_cast<size_t>(2 * u + 1) * H];
+        for (int u = 0; u < 5; ++u) {
+          if (u < n) {
+            hi[u] = p[static_cast<size_t>(2 * u) * H];
+            lo[u] = p[static_cast<size_t>(2 * u + 1) * H];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 5; ++u) {
+          if (u < n) {
+            float err;
+            s = two_sum(s, hi[u], err);
+            e = __fadd_rn(e, __fadd_rn(err, lo[u]));
+          }
+        }
       }
+    } else {
+      int kk = ka;
+      for (; kk + 4 <= kb; kk += 4, p += static_cast<size_t>(8) * H) {
+        float hi[4], lo[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 4; ++u) {
+          hi[u] = p[static_cast<size_t>(2 * u) * H];
+          lo[u] = p[static_cast<size_t>(2 * u + 1) * H];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float err;
+          s = two_sum(s, hi[u], err);
+          e = __fadd_rn(e, __fadd_rn(err, lo[u]));
+        }
+      }
+      for (; kk < kb; ++kk, p += static_cast<size_t>(2) * H) {
         float err;
-        s = two_sum(s, hi[u], err);
-        e = __fadd_rn(e, __fadd_rn(err, lo[u]));
+        s = two_sum(s, p[0], err);
+        e = __fadd_rn(e, __fadd_rn(err, p[H]));
       }
-    }
-    for (; kk < kb; ++kk, p += static_cast<size_t>(2) * H) {
-      float err;
-      s = two_sum(s, p[0], err);
-      e = __fadd_rn(e, __fadd_rn(err, p[H]));
     }
   }
   sh[sl][cl] = s;
@@ -95,10 +122,12 @@ cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaSt
 }
 
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, unsigned* ctl,
-                             cudaStream_t st) {
-  const void* fn = reinterpret_cast<const void*>(&rmsn_dw_finish_kernel);
+                             int sms, cudaStream_t st) {
   void* args[] = {&part, &dw, &P, &H, &ctl};
   const unsigned grid = static_cast<unsigned>((H + kFinishCols - 1) / kFinishCols);
+  const void* fn = grid <= static_cast<unsigned>(sms)
+                       ? reinterpret_cast<const void*>(&rmsn_dw_finish_kernel<true>)
+                       : reinterpret_cast<const void*>(&rmsn_dw_finish_kernel<false>);
   return launch_pdl(fn, dim3(grid), dim3(kFinishCols * kFinishSlices), 0, st, args);
 }
 

@@ -145,9 +145,11 @@ int bwd_blocks_per_sm(const Shape& s, bool fp32w, bool rc);
 // The row pass, either mode: a.ctl null (deterministic: fixed chunks) or the
 // non-deterministic pool's words.
 cudaError_t launch_bwd_rows(const BwdArgs& a, const Shape& s, bool fp32w, cudaStream_t st);
-// ctl: the non-deterministic pool words to clear once the partials are summed, or null.
+// ctl: the non-deterministic pool words to clear once the partials are summed, or null;
+// sms: the GPU's SM count (the finish build that takes a whole SM a CTA runs only where
+// its grid fits one wave).
 cudaError_t launch_dw_finish(const float* part, float* dw, int P, int H, unsigned* ctl,
-                             cudaStream_t st);
+                             int sms, cudaStream_t st);
 
 // The non-deterministic workspace starts with the pool's two words (a 16-byte slot),
 // followed by the P partials; the fixed-order finish adds the partials and clears the
