@@ -17,8 +17,10 @@
  * order); deterministic == 0 gives each CTA a fixed prefix of rows and hands the last
  * rows out to the CTAs as they free up (no CTA idles while another still has a queue of
  * rows), so a CTA's dw partial covers rows that vary from run to run and dw may differ
- * between runs in its last bits (both modes keep dw within the same budget).  dx is the
- * same in both modes, bit for bit.
+ * between runs in its last bits (both modes keep dw within the same budget); where a CTA
+ * would own fewer than eight ring depths of rows it takes the deterministic partition
+ * instead (too few rows for the hand-out to even the CTAs out).  dx is the same in both
+ * modes, bit for bit.
  *
  * Rows and views (same PR, description: per-head views [T,24,256] strided and [T,4,256]
  * contiguous with a shared w[256]).  A normalized row is a pair (token t, head h),

@@ -7,7 +7,8 @@
 // free to be faster): each CTA owns a fixed prefix and the last rows are handed out from a
 // counter in the workspace as CTAs free up, so no CTA idles while another still holds a
 // queue of rows; dw's partials then cover rows that vary from run to run, so its last bits
-// may too.  dx never depends on the partition: it is bit-identical across the modes.
+// may too (with fewer than eight ring depths of rows a CTA, the deterministic chunks).  dx
+// never depends on the partition: it is bit-identical across the modes.
 #include "rmsn_bwd_rows.cuh"
 
 namespace rmsn {

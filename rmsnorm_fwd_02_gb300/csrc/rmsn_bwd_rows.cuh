@@ -85,8 +85,11 @@ struct RowSums {
 //    another still holds a queue.  CTA 0 opens the pool (sets the counter, then publishes
 //    the call's tag in a.ctl[0]) before its own rows; a CTA that reaches the pool before
 //    it is open takes nothing from it, and CTA 0 itself always drains it, so no CTA ever
-//    waits on another.  (Below 4 stages a CTA the prefix is the deterministic chunk and
-//    the pool is empty.)
+//    waits on another.  Below 8*S stages a CTA (S the ring depth) the partition is the
+//    deterministic one and the pool stays shut: when the pool runs dry every CTA still
+//    holds S staged chunks, taken a ring's depth before it reaches them, and over so few
+//    stages that spreads the CTAs' ends more than the pool evens them out (measured at
+//    H=1536, 26 stages a CTA, S=4: 1.7 us behind the deterministic chunks).
 // Either way CTA k writes its dw partial to a.part[k], and dx does not depend on the
 // partition.
 template <int VPT, int kCls, bool kFp32W, bool kDh, bool kRc>
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(bwd_max_threads(kCls, VPT), bwd_design_blocks_
       const uint32_t per = static_cast<uint32_t>(a.P) * static_cast<uint32_t>(G);
       const uint32_t nfull = R / per;          // whole stages every CTA could own
       uint32_t pa, pb, pool;                   // this CTA's own rows [pa, pb), pool start
-      if (nfull >= 4 && a.ctl != nullptr) {  // non-deterministic: prefix and pool
+      if (nfull >= 8u * static_cast<uint32_t>(S) && a.ctl != nullptr) {  // prefix and pool
         const uint32_t Ns = nfull - 2;
         pa = static_cast<uint32_t>(k) * Ns * G;
         pb = pa + Ns * G;

@@ -165,7 +165,9 @@ def test_autograd_wrapper_matches_direct_calls():
 def test_cuda_graph_replay_matches_direct_calls(det):
     # forward + backward enqueued on a side stream under stream capture (the launches use
     # programmatic dependent launch attributes) and replayed: the same bits as direct calls
-    c = synth.plain(8192)
+    # (T=16384: 35 stages a CTA, so the non-deterministic backward opens its row pool, whose
+    # per-call tag a replay repeats)
+    c = synth.plain(16384)
     dc = parity.DeviceCase(c)
     R, H = c.R, c.H
     nbytes = N.rmsnorm_train_bwd_workspace_bytes(c.T, 1, H, det)
@@ -210,7 +212,9 @@ def test_cuda_graph_replay_matches_direct_calls(det):
 
 @pytest.mark.parametrize("mk", [lambda: synth.stress(4096, 1536), lambda: synth.plain(300),
                                 lambda: synth.heads_strided(512),
-                                lambda: synth.make_case(9, 2000, 8192, w_fp32=True)])
+                                lambda: synth.make_case(9, 2000, 8192, w_fp32=True),
+                                lambda: synth.plain(16384)],   # the row pool opened
+                         ids=["stress4096", "plain300", "heads512", "w32_H8192", "plain16384"])
 def test_nondet_workspace_needs_no_initial_contents_and_is_reusable(mk):
     # the non-deterministic backward zeroes its own row counter on the stream: a workspace
     # full of garbage, and the same workspace reused by calls queued back to back, give dx
